@@ -1,0 +1,172 @@
+"""Plain fp64 CPU oracle for the KDA layer core.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg may import this package.  The CUDA library never
+calls it, shares no code with it, and has no CPU fallback.
+
+The arithmetic lives in ``kda_oracle.c`` (sequential double-precision loops,
+one routine per step of the method, each citing the page it follows).  This
+module only compiles that file with the host C compiler (``gcc -O2``, no
+fast-math), and marshals numpy arrays into it.  ``chunked.py`` holds a second,
+chunk-wise fp64 form of the recurrence that exists only to pin the chunk
+algebra (it is compared against the recurrence for every chunk size).
+
+Parity status: every routine here is pinned by ``tests/test_oracle_pins.py``
+(invariants, closed forms, library special cases and brute force on tiny
+inputs).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (if stale)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_BUILD)
+    os.close(fd)
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        D = ctypes.c_double
+        lib.oracle_kda_prefill.argtypes = [I, I, I, I, P, P, P, P, P, P, P, D, P, P, I]
+        lib.oracle_kda_decode_step.argtypes = [I, I, I, I, P, P, P, P, P, P, D, P, I]
+        lib.oracle_kda_frontend.argtypes = [I, I, I, P, P, P, P, P, P, P, P, P, D,
+                                            P, P, P, P, P, I]
+        lib.oracle_kda_output_gate.argtypes = [ctypes.c_long, I, P, P, D, P, I]
+        for f in (lib.oracle_kda_prefill, lib.oracle_kda_decode_step,
+                  lib.oracle_kda_frontend, lib.oracle_kda_output_gate):
+            f.restype = I
+        _lib = lib
+    return _lib
+
+
+def _f64(x):
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, scale=None,
+                n_threads=None):
+    """Token-by-token KDA recurrence over packed sequences (fp64).
+
+    q, k: [T, H, dk]; v: [T, H, dv]; log_alpha: [T, H, dk]; beta: [T, H];
+    cu_seqlens: [N+1] int; S0: [N, H, dk, dv] or None (zeros).
+    Returns (o [T, H, dv], S_final [N, H, dk, dv]) as float64.
+    """
+    q, k, v, la, beta = map(_f64, (q, k, v, log_alpha, beta))
+    T, H, dk = q.shape
+    dv = v.shape[2]
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    N = cu.shape[0] - 1
+    if scale is None:
+        scale = 1.0 / np.sqrt(128.0)
+    S0a = None if S0 is None else _f64(S0)
+    o = np.zeros((T, H, dv), np.float64)
+    Sf = np.zeros((N, H, dk, dv), np.float64)
+    rc = _load().oracle_kda_prefill(N, H, dk, dv, _ptr(cu), _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(la), _ptr(beta), _ptr(S0a), float(scale),
+                                    _ptr(o), _ptr(Sf), n_threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_kda_prefill: invalid arguments")
+    return o, Sf
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, S, scale=None, n_threads=None):
+    """One recurrence step per (request, head).  Returns (o, S_new); S is not modified.
+
+    q, k: [B, H, dk]; v: [B, H, dv]; log_alpha: [B, H, dk]; beta: [B, H];
+    S: [B, H, dk, dv].
+    """
+    q, k, v, la, beta = map(_f64, (q, k, v, log_alpha, beta))
+    S_new = _f64(S).copy()
+    B, H, dk = q.shape
+    dv = v.shape[2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(128.0)
+    o = np.zeros((B, H, dv), np.float64)
+    rc = _load().oracle_kda_decode_step(B, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(la),
+                                        _ptr(beta), _ptr(S_new), float(scale), _ptr(o),
+                                        n_threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_kda_decode_step: invalid arguments")
+    return o, S_new
+
+
+def kda_frontend(qp, kp, vp, conv_w, z, A, b, beta_logit, cu_seqlens, l2_eps=1e-6,
+                 n_threads=None):
+    """ShortConv + SiLU + L2 (q, k), ShortConv + SiLU (v), decay and write strength.
+
+    qp, kp, vp, z: [T, H, d]; conv_w: [3, H*d, 4]; A: [H]; b: [H, d];
+    beta_logit: [T, H].  Returns (q_hat, k_hat, v, log_alpha, beta) as float64.
+    """
+    qp, kp, vp, conv_w, z, A, b, bl = map(_f64, (qp, kp, vp, conv_w, z, A, b, beta_logit))
+    T, H, d = qp.shape
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    N = cu.shape[0] - 1
+    outs = [np.zeros((T, H, d)) for _ in range(4)]
+    beta = np.zeros((T, H))
+    rc = _load().oracle_kda_frontend(N, H, d, _ptr(cu), _ptr(qp), _ptr(kp), _ptr(vp),
+                                     _ptr(conv_w), _ptr(z), _ptr(A), _ptr(b), _ptr(bl),
+                                     float(l2_eps), _ptr(outs[0]), _ptr(outs[1]),
+                                     _ptr(outs[2]), _ptr(outs[3]), _ptr(beta),
+                                     n_threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_kda_frontend: invalid arguments")
+    return outs[0], outs[1], outs[2], outs[3], beta
+
+
+def kda_output_gate(o_tilde, g, eps=1e-6, n_threads=None):
+    """sigma(g) * RMSNorm(o~) per head over the last axis (unit weight)."""
+    ot, g = _f64(o_tilde), _f64(g)
+    d = ot.shape[-1]
+    rows = ot.size // d
+    out = np.zeros_like(ot)
+    rc = _load().oracle_kda_output_gate(rows, d, _ptr(ot), _ptr(g), float(eps), _ptr(out),
+                                        n_threads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_kda_output_gate: invalid arguments")
+    return out
+
+
+def kda_layer_core(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=None,
+                   scale=None, l2_eps=1e-6, rms_eps=1e-6, n_threads=None):
+    """Front end, then the recurrence, then the output gate (all fp64).
+
+    Returns (o_gated [T, H, d], S_final [N, H, d, d]).
+    """
+    qh, kh, vv, la, beta = kda_frontend(qp, kp, vp, conv_w, z, A, b, beta_logit,
+                                        cu_seqlens, l2_eps, n_threads)
+    ot, Sf = kda_prefill(qh, kh, vv, la, beta, cu_seqlens, S0, scale, n_threads)
+    return kda_output_gate(ot, g, rms_eps, n_threads), Sf
