@@ -1,0 +1,336 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA hot path on GB300.
+
+Default workload (one "step"): kda_prefill over B=1, H=96, T=8192, bf16
+q/k/v, fp32 log_alpha/beta, S0 = 0, bf16 output and fp32 S_final, with the
+inputs resident in HBM.  The same JSON line also carries the decode step
+(256 requests x 96 heads, 1.6 GB of fp32 state updated in place), measured the
+same way.
+
+Prints ONE JSON line (rank 0).  Multi-GPU (torchrun): every rank runs its own
+replica of the workload (weak scaling, no collective on the data path).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "KDA prefill tokens/s (% bf16 TC peak); decode tokens/s (% HBM GB/s)"
+UNIT = "tokens/s"
+D = 128
+# Algorithmic cost per (token, head) at chunk 64, d = 128 (bf16 q/k/v/o, fp32 log_alpha, beta):
+PREFILL_BYTES_PER_TOKEN_HEAD = 3 * D * 2 + D * 4 + 4 + D * 2          # 1540 B
+PREFILL_FLOP_PER_TOKEN_HEAD = 2 * (3 * D * D + 2.5 * 64 * D)          # 139,264 FLOP
+STATE_BYTES = D * D * 4                                               # 64 KiB per (seq, head)
+# Decode, per (request, head): state read + write, q/k/v bf16, log_alpha fp32, beta, o bf16
+DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * D * 2 + D * 4 + 4 + D * 2  # 132,612 B
+DECODE_FLOP_PER_UNIT = 2 * 4 * D * D
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+        if shutil.which("nvidia-smi") is None:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.f = open(self.path, "w")
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+             "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+            stderr=subprocess.DEVNULL)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        med = statistics.median(sm) if sm else None
+        return {"sm_mhz": med, "sm_max_mhz": smax, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_launches(fn, steps, warmup, world):
+    """Per-launch CUDA-event times on the launching (current) stream."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s, e in ev:
+        s.record(stream)
+        fn()
+        e.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    total_ms = t0.elapsed_time(t1)
+    per = [s.elapsed_time(e) for s, e in ev]
+    return total_ms, per
+
+
+def cpu_baseline_prefill(inp, heads, tokens):
+    """The fp64 oracle as it stands, on a bounded sample of the prefill workload."""
+    import numpy as np
+    import oracle
+    f = lambda t: t[:tokens, heads].double().cpu().numpy()
+    args = [f(inp.q), f(inp.k), f(inp.v), f(inp.log_alpha), f(inp.beta)]
+    cores = oracle.default_threads()
+    t = time.perf_counter()
+    oracle.kda_prefill(*args, np.array([0, tokens], np.int32), n_threads=cores)
+    dt = time.perf_counter() - t
+    head_tokens = tokens * len(heads)
+    return dt, head_tokens, min(cores, len(heads))
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the fp64 CPU oracle, timed on the host cores."""
+    if rank != 0:
+        return
+    from gated_delta_rule_kda_gb300 import synthetic
+    import oracle
+    oracle.build()
+    H_sample, T_sample = 16, 1024
+    inp = synthetic.prefill_inputs([T_sample], H_sample, torch.bfloat16,
+                                   seed=synthetic.BASE_SEED + 2, device="cpu")
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, head_tokens, cores = cpu_baseline_prefill(inp, list(range(H_sample)), T_sample)
+        if i >= args.warmup:
+            times.append(dt)
+    mean = sum(times) / len(times)
+    value = head_tokens / mean / 96.0
+    sample = (f"oracle on {H_sample} heads x {T_sample} tokens per step, "
+              f"scaled to 96-head tokens")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": mean * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(n):
+    return {"workload": "KDA prefill B=1 H=96 T=8192 d=128 bf16 (chunk 64), S0=0, "
+                        "bf16 o + fp32 S_final", "global_batch": n, "seq_len": 8192,
+            "heads": 96, "head_dim": 128, "parallelism": f"replicas x{n}",
+            "l2": "inputs larger than L2 (1.2 GB per step), no flush",
+            "decode_workload": "256 requests x 96 heads, fp32 state 1.61 GB in place"}
+
+
+def run_ours(args, world, rank, local):
+    from gated_delta_rule_kda_gb300 import kda, synthetic
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm, tc, tc_sus, peak_kind = peaks()
+
+    # ---------------- prefill (the step) ----------------
+    inp = synthetic.workload(2, device=dev)
+    T, H = inp.q.shape[:2]
+    o = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    Sf = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+
+    def prefill_step():
+        kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.cu_seqlens, None,
+                        o=o, S_final=Sf)
+
+    clocks = ClockSampler(local if world > 1 else torch.cuda.current_device())
+    total_ms, per = time_launches(prefill_step, args.steps, args.warmup, world)
+    clk = clocks.stop()
+    ms_step = max_over_ranks(total_ms / args.steps, world)
+    tokens_per_step = T
+    value = world * tokens_per_step / (ms_step / 1e3)
+    launch_ms = sum(per) / len(per)
+    alg_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
+    alg_flop = T * H * PREFILL_FLOP_PER_TOKEN_HEAD
+    achieved = alg_bytes / (launch_ms / 1e3) / 1e9
+    tflops = alg_flop / (launch_ms / 1e3) / 1e12
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None, "peak_kind": peak_kind,
+                "kernel": "kda_prefill", "tc_achieved_tflops": tflops, "tc_peak_tflops": tc,
+                "tc_frac": tflops / tc,
+                "binding_roofline_frac": max(alg_bytes / (hbm * 1e9),
+                                             alg_flop / (tc * 1e12)) / (launch_ms / 1e3)}
+
+    # ---------------- end to end through the C ABI with host buffers ----------------
+    host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "log_alpha", "beta")}
+    dev_bufs = {n: getattr(inp, n) for n in host}
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    S_host = torch.empty(Sf.shape, dtype=Sf.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * o_host.element_size() + S_host.numel() * S_host.element_size()
+
+    def e2e_step():
+        for n, t in host.items():
+            dev_bufs[n].copy_(t, non_blocking=True)
+        prefill_step()
+        o_host.copy_(o, non_blocking=True)
+        S_host.copy_(Sf, non_blocking=True)
+
+    e2e_steps = max(2, min(args.steps, 5))
+    e2e_total, _ = time_launches(e2e_step, e2e_steps, 1, world)
+    e2e_ms = max_over_ranks(e2e_total / e2e_steps, world)
+    e2e = {"value": world * tokens_per_step / (e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    del host, o_host, S_host
+
+    # ---------------- decode (second half of the metric) ----------------
+    del inp, o, Sf
+    torch.cuda.empty_cache()
+    dinp = synthetic.workload(3, device=dev)
+    od = torch.empty((256, 96, D), dtype=torch.bfloat16, device=dev)
+
+    def decode_step():
+        kda.kda_decode_step(dinp.q, dinp.k, dinp.v, dinp.log_alpha, dinp.beta, dinp.S, o=od)
+
+    d_total, d_per = time_launches(decode_step, args.steps, args.warmup, world)
+    d_ms = max_over_ranks(d_total / args.steps, world)
+    d_launch = sum(d_per) / len(d_per)
+    units = 256 * 96
+    d_bytes = units * DECODE_BYTES_PER_UNIT
+    d_ach = d_bytes / (d_launch / 1e3) / 1e9
+    decode = {"tokens_per_s": world * 256 / (d_ms / 1e3), "ms_per_step": d_ms,
+              "roofline": {"bound": "hbm", "achieved": d_ach, "peak": hbm, "unit": "GB/s",
+                           "frac": d_ach / hbm, "traffic": None, "peak_kind": peak_kind,
+                           "kernel": "kda_decode_step"}}
+    del dinp, od
+    torch.cuda.empty_cache()
+
+    # ---------------- CPU baseline: the oracle on a bounded sample ----------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from gated_delta_rule_kda_gb300 import synthetic as syn
+        H_sample, T_sample = 32, 2048
+        cinp = syn.prefill_inputs([T_sample], H_sample, torch.bfloat16,
+                                  seed=syn.BASE_SEED + 2, device="cpu")
+        dt, head_tokens, cores = cpu_baseline_prefill(cinp, list(range(H_sample)), T_sample)
+        cpu = {"value": head_tokens / dt / 96.0, "unit": UNIT, "cores": cores,
+               "kind": "oracle",
+               "sample": f"{H_sample} heads x {T_sample} tokens of the prefill workload, "
+                         f"{dt:.1f} s, scaled to 96-head tokens"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
+            "clocks": clk, "gpu_launches": args.steps,
+            "kernel_ms_mean": launch_ms,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,183 @@
+// C ABI of libkda: argument validation on the host, then kernel launches.
+// Nothing here allocates device memory.
+#include <atomic>
+#include <cstring>
+
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+// Device status word ([0] = kda_status, [1] = detail); see kda_get_device_status.
+__device__ uint32_t g_status_word[2];
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint32_t *> g_status_ptr[kMaxDevices];
+
+DeviceStatus device_status() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return {nullptr};
+    uint32_t *p = g_status_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return {nullptr};
+        p = static_cast<uint32_t *>(addr);
+        g_status_ptr[dev].store(p, std::memory_order_release);
+    }
+    return {p};
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool ok_ptr(const void *p) { return p != nullptr && aligned16(p); }
+bool ok_opt_ptr(const void *p) { return p == nullptr || aligned16(p); }
+bool ok_dtype(kda_dtype d) { return d == KDA_BF16 || d == KDA_FP32; }
+
+bool overlap(const void *a, const void *b, size_t bytes) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bytes && y < x + bytes;
+}
+
+kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+const char *kda_status_string(kda_status status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARGUMENT: return "KDA_ERR_INVALID_ARGUMENT";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_DEVICE_TIMEOUT: return "KDA_ERR_DEVICE_TIMEOUT";
+        case KDA_ERR_DEVICE_CHECK: return "KDA_ERR_DEVICE_CHECK";
+    }
+    return "KDA_UNKNOWN_STATUS";
+}
+
+int32_t kda_version(void) { return 100; }
+
+size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                  kda_dtype in_dtype) {
+    (void)num_seqs; (void)total_tokens; (void)num_heads; (void)in_dtype;
+    return 0;
+}
+
+kda_status kda_prefill(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
+                       int32_t total_tokens, int32_t num_heads, const void *q, const void *k,
+                       const void *v, const float *log_alpha, const float *beta,
+                       const float *S0, const int32_t *cu_seqlens, float scale, void *o,
+                       float *S_final, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_ptr(cu_seqlens)) return KDA_ERR_INVALID_ARGUMENT;
+    if (total_tokens > 0) {
+        if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(log_alpha) || !ok_ptr(beta) ||
+            !ok_ptr(o))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if (!ok_opt_ptr(S0) || !ok_opt_ptr(S_final)) return KDA_ERR_INVALID_ARGUMENT;
+    const size_t state_bytes = (size_t)num_seqs * num_heads * kD * kD * sizeof(float);
+    if (S0 && S_final && S0 != S_final && overlap(S0, S_final, state_bytes))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (num_heads > 65535 || num_seqs > 65535) return KDA_ERR_UNSUPPORTED;
+    const size_t need = kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, in_dtype);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+        return KDA_ERR_WORKSPACE;
+
+    PrefillArgs a;
+    a.in_dtype = in_dtype; a.out_dtype = out_dtype;
+    a.num_seqs = num_seqs; a.total_tokens = total_tokens; a.num_heads = num_heads;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S0 = S0;
+    a.cu_seqlens = cu_seqlens; a.scale = scale; a.o = o; a.S_final = S_final;
+    a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    a.status = device_status();
+    return from_cuda(launch_prefill_recurrent(a, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_decode_step(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batch,
+                           int32_t num_heads, const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *beta, float *S_inout,
+                           float scale, void *o, void *stream) {
+    if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (batch < 1 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(log_alpha) || !ok_ptr(beta) ||
+        !ok_ptr(S_inout) || !ok_ptr(o))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if ((int64_t)batch * num_heads > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    DecodeArgs a;
+    a.in_dtype = in_dtype; a.out_dtype = out_dtype;
+    a.batch = batch; a.num_heads = num_heads;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta;
+    a.S = S_inout; a.scale = scale; a.o = o;
+    a.status = device_status();
+    return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_frontend(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                        const void *qp, const void *kp, const void *vp, const float *conv_w,
+                        const void *z, const float *A, const float *b, const void *beta_logit,
+                        const int32_t *cu_seqlens, float l2_eps, kda_dtype out_dtype,
+                        void *q_hat, void *k_hat, void *v_out, float *log_alpha, float *beta,
+                        void *stream) {
+    if (!ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_ptr(cu_seqlens) || !ok_ptr(conv_w) || !ok_ptr(A) || !ok_opt_ptr(b))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (total_tokens > 0) {
+        if (!ok_ptr(qp) || !ok_ptr(kp) || !ok_ptr(vp) || !ok_ptr(z) || !ok_ptr(beta_logit) ||
+            !ok_ptr(q_hat) || !ok_ptr(k_hat) || !ok_ptr(v_out) || !ok_ptr(log_alpha) ||
+            !ok_ptr(beta))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if ((int64_t)total_tokens * num_heads / 8 >= 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    FrontendArgs a;
+    a.num_seqs = num_seqs; a.total_tokens = total_tokens; a.num_heads = num_heads;
+    a.qp = static_cast<const __nv_bfloat16 *>(qp);
+    a.kp = static_cast<const __nv_bfloat16 *>(kp);
+    a.vp = static_cast<const __nv_bfloat16 *>(vp);
+    a.z = static_cast<const __nv_bfloat16 *>(z);
+    a.beta_logit = static_cast<const __nv_bfloat16 *>(beta_logit);
+    a.conv_w = conv_w; a.A = A; a.b = b; a.cu_seqlens = cu_seqlens; a.l2_eps = l2_eps;
+    a.out_dtype = out_dtype; a.q_hat = q_hat; a.k_hat = k_hat; a.v_out = v_out;
+    a.log_alpha = log_alpha; a.beta = beta;
+    return from_cuda(launch_frontend(a, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_output_gate(int64_t num_rows, kda_dtype in_dtype, const void *o_tilde,
+                           const void *g, float eps, kda_dtype out_dtype, void *out,
+                           void *stream) {
+    if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype) || num_rows < 0)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (num_rows > 0 && (!ok_ptr(o_tilde) || !ok_ptr(g) || !ok_ptr(out)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (num_rows / 8 >= 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    GateArgs a;
+    a.num_rows = num_rows; a.in_dtype = in_dtype; a.out_dtype = out_dtype;
+    a.o_tilde = o_tilde; a.g = static_cast<const __nv_bfloat16 *>(g); a.eps = eps; a.out = out;
+    return from_cuda(launch_output_gate(a, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_get_device_status(void *stream, uint32_t *detail) {
+    if (detail) *detail = 0;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    DeviceStatus st = device_status();
+    if (st.word == nullptr) return KDA_ERR_CUDA;
+    uint32_t host[2] = {0, 0};
+    if (cudaMemcpy(host, st.word, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (host[0] != 0) {
+        const uint32_t zero[2] = {0, 0};
+        if (cudaMemcpy(st.word, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    if (detail) *detail = host[1];
+    return static_cast<kda_status>(host[0]);
+}
+
+}  // extern "C"

@@ -1,0 +1,119 @@
+// Shared device helpers and launcher declarations of libkda (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int kD = KDA_HEAD_DIM;  // d_k = d_v = 128
+
+// Device status word: [0] = kda_status code, [1] = kernel-specific detail.
+// The first writer wins (atomicCAS on [0]).
+struct DeviceStatus {
+    uint32_t *word;
+};
+
+__device__ __forceinline__ void record_status(DeviceStatus st, uint32_t code, uint32_t detail) {
+    if (st.word == nullptr) return;
+    if (atomicCAS(st.word, 0u, code) == 0u) atomicExch(st.word + 1, detail);
+}
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+    static __device__ __forceinline__ float load(const float *p) { return *p; }
+    static __device__ __forceinline__ void store(float *p, float x) { *p = x; }
+};
+template <>
+struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, float x) {
+        *p = __float2bfloat16_rn(x);
+    }
+};
+
+// Load 4 consecutive elements (16-byte aligned for fp32, 8-byte for bf16).
+__device__ __forceinline__ float4 load4(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+    uint2 raw = *reinterpret_cast<const uint2 *>(p);
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&raw.x);
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&raw.y);
+    float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+    return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+__device__ __forceinline__ void store4(float *p, float4 x) {
+    *reinterpret_cast<float4 *>(p) = x;
+}
+__device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 x) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(x.z, x.w);
+    uint2 raw;
+    raw.x = *reinterpret_cast<uint32_t *>(&a);
+    raw.y = *reinterpret_cast<uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = raw;
+}
+
+// ---------------------------------------------------------------------------
+// Launcher argument blocks (host side).  Pointers are device pointers that the
+// ABI layer has already validated.
+// ---------------------------------------------------------------------------
+struct DecodeArgs {
+    kda_dtype in_dtype, out_dtype;
+    int32_t batch, num_heads;
+    const void *q, *k, *v;
+    const float *log_alpha, *beta;
+    float *S;
+    float scale;
+    void *o;
+    DeviceStatus status;
+};
+
+struct PrefillArgs {
+    kda_dtype in_dtype, out_dtype;
+    int32_t num_seqs, total_tokens, num_heads;
+    const void *q, *k, *v;
+    const float *log_alpha, *beta, *S0;
+    const int32_t *cu_seqlens;
+    float scale;
+    void *o;
+    float *S_final;
+    void *workspace;
+    size_t workspace_bytes;
+    DeviceStatus status;
+};
+
+struct FrontendArgs {
+    int32_t num_seqs, total_tokens, num_heads;
+    const __nv_bfloat16 *qp, *kp, *vp, *z, *beta_logit;
+    const float *conv_w, *A, *b;
+    const int32_t *cu_seqlens;
+    float l2_eps;
+    kda_dtype out_dtype;
+    void *q_hat, *k_hat, *v_out;
+    float *log_alpha, *beta;
+};
+
+struct GateArgs {
+    int64_t num_rows;
+    kda_dtype in_dtype, out_dtype;
+    const void *o_tilde;
+    const __nv_bfloat16 *g;
+    float eps;
+    void *out;
+};
+
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_prefill_recurrent(const PrefillArgs &a, cudaStream_t stream);
+cudaError_t launch_frontend(const FrontendArgs &a, cudaStream_t stream);
+cudaError_t launch_output_gate(const GateArgs &a, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,205 @@
+"""Thin ctypes binding of ``libkda.so`` (the C ABI in ``include/kda.h``).
+
+Argument marshalling only: torch tensors supply device pointers and the
+current CUDA stream, and every step of the computation runs in the library's
+kernels.  Importing this module loads the library and raises ``ImportError``
+when it has not been built (``python -m gated_delta_rule_kda_gb300.build``):
+there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+KDA_OK = 0
+KDA_BF16 = 0
+KDA_FP32 = 1
+HEAD_DIM = 128
+DEFAULT_SCALE = 1.0 / math.sqrt(128.0)
+
+STATUS_NAMES = {
+    0: "KDA_OK",
+    1: "KDA_ERR_INVALID_ARGUMENT",
+    2: "KDA_ERR_UNSUPPORTED",
+    3: "KDA_ERR_WORKSPACE",
+    4: "KDA_ERR_CUDA",
+    5: "KDA_ERR_DEVICE_TIMEOUT",
+    6: "KDA_ERR_DEVICE_CHECK",
+}
+
+# Every entry point include/kda.h declares (checked by tests on CPU).
+EXPORTED = (
+    "kda_status_string",
+    "kda_version",
+    "kda_prefill_workspace_size",
+    "kda_prefill",
+    "kda_decode_step",
+    "kda_frontend",
+    "kda_output_gate",
+    "kda_get_device_status",
+)
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(f"libkda.so is not built ({_LIB_PATH}); run "
+                          "`python -m gated_delta_rule_kda_gb300.build` first")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, I32, I64, F, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                          ctypes.c_size_t)
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_version.argtypes = []
+    lib.kda_version.restype = I32
+    lib.kda_prefill_workspace_size.argtypes = [I32, I32, I32, ctypes.c_int]
+    lib.kda_prefill_workspace_size.restype = SZ
+    lib.kda_prefill.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, I32, P, P, P, P, P, P, P,
+                                F, P, P, P, SZ, P]
+    lib.kda_prefill.restype = ctypes.c_int
+    lib.kda_decode_step.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, P, P, P, P, P, P, F,
+                                    P, P]
+    lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_frontend.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, F, ctypes.c_int,
+                                 P, P, P, P, P, P]
+    lib.kda_frontend.restype = ctypes.c_int
+    lib.kda_output_gate.argtypes = [I64, ctypes.c_int, P, P, F, ctypes.c_int, P, P]
+    lib.kda_output_gate.restype = ctypes.c_int
+    lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.kda_get_device_status.restype = ctypes.c_int
+    return lib
+
+
+_lib = _load()
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _dtype_code(d: torch.dtype) -> int:
+    return KDA_BF16 if d == torch.bfloat16 else KDA_FP32
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, rc: int):
+    if rc != KDA_OK:
+        raise KdaError(fn, rc)
+
+
+def kda_prefill_workspace_size(num_seqs: int, total_tokens: int, num_heads: int,
+                               in_dtype: torch.dtype = torch.bfloat16) -> int:
+    return int(_lib.kda_prefill_workspace_size(num_seqs, total_tokens, num_heads,
+                                               _dtype_code(in_dtype)))
+
+
+def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, scale=DEFAULT_SCALE, *,
+                out_dtype=None, o=None, S_final=None, want_state=True, workspace=None,
+                stream=None):
+    """Packed-varlen prefill.  Returns (o, S_final or None).
+
+    q, k, v [T, H, 128] (bf16 or fp32); log_alpha [T, H, 128] fp32; beta [T, H] fp32;
+    cu_seqlens [N+1] int32 (device); S0 [N, H, 128, 128] fp32 or None.
+    S_final may be S0 itself (in-place resume)."""
+    T, H, _ = q.shape
+    N = cu_seqlens.shape[0] - 1
+    out_dtype = out_dtype or q.dtype
+    if o is None:
+        o = torch.empty((T, H, HEAD_DIM), dtype=out_dtype, device=q.device)
+    if S_final is None and want_state:
+        S_final = torch.empty((N, H, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=q.device)
+    need = kda_prefill_workspace_size(N, T, H, q.dtype)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _lib.kda_prefill(_dt(q), _dtype_code(o.dtype), N, T, H, _p(q), _p(k), _p(v),
+                          _p(log_alpha), _p(beta), _p(S0), _p(cu_seqlens), float(scale), _p(o),
+                          _p(S_final), _p(workspace), wbytes, _stream(stream))
+    _check("kda_prefill", rc)
+    return o, S_final
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, S_inout, scale=DEFAULT_SCALE, *, out_dtype=None,
+                    o=None, stream=None):
+    """One decode step; S_inout [B, H, 128, 128] fp32 is updated in place.  Returns o."""
+    B, H, _ = q.shape
+    out_dtype = out_dtype or q.dtype
+    if o is None:
+        o = torch.empty((B, H, HEAD_DIM), dtype=out_dtype, device=q.device)
+    rc = _lib.kda_decode_step(_dt(q), _dtype_code(o.dtype), B, H, _p(q), _p(k), _p(v),
+                              _p(log_alpha), _p(beta), _p(S_inout), float(scale), _p(o),
+                              _stream(stream))
+    _check("kda_decode_step", rc)
+    return o
+
+
+def kda_frontend(qp, kp, vp, conv_w, z, A, b, beta_logit, cu_seqlens, l2_eps=1e-6, *,
+                 out_dtype=torch.bfloat16, stream=None):
+    """Returns (q_hat, k_hat, v, log_alpha, beta)."""
+    T, H, _ = qp.shape
+    N = cu_seqlens.shape[0] - 1
+    dev = qp.device
+    q_hat = torch.empty((T, H, HEAD_DIM), dtype=out_dtype, device=dev)
+    k_hat = torch.empty_like(q_hat)
+    v_out = torch.empty_like(q_hat)
+    log_alpha = torch.empty((T, H, HEAD_DIM), dtype=torch.float32, device=dev)
+    beta = torch.empty((T, H), dtype=torch.float32, device=dev)
+    rc = _lib.kda_frontend(N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A), _p(b),
+                           _p(beta_logit), _p(cu_seqlens), float(l2_eps),
+                           _dtype_code(out_dtype), _p(q_hat), _p(k_hat), _p(v_out),
+                           _p(log_alpha), _p(beta), _stream(stream))
+    _check("kda_frontend", rc)
+    return q_hat, k_hat, v_out, log_alpha, beta
+
+
+def kda_output_gate(o_tilde, g, eps=1e-6, *, out_dtype=torch.bfloat16, out=None, stream=None):
+    rows = o_tilde.numel() // HEAD_DIM
+    if out is None:
+        out = torch.empty(o_tilde.shape, dtype=out_dtype, device=o_tilde.device)
+    rc = _lib.kda_output_gate(rows, _dt(o_tilde), _p(o_tilde), _p(g), float(eps),
+                              _dtype_code(out.dtype), _p(out), _stream(stream))
+    _check("kda_output_gate", rc)
+    return out
+
+
+def kda_get_device_status(stream=None):
+    """Synchronises the stream; returns (status_code, detail) and clears the word."""
+    detail = ctypes.c_uint32(0)
+    rc = _lib.kda_get_device_status(_stream(stream), ctypes.byref(detail))
+    return int(rc), int(detail.value)

@@ -1,0 +1,191 @@
+/*
+ * kda.h - C ABI of libkda.so: Kimi Delta Attention (KDA) on one NVIDIA GB300
+ * (sm_103a).
+ *
+ * The method, per head with d_k = d_v = 128 and per token t, in order
+ * ("Kimi K3 · KDA layer", OpenModelAtlas, KDA equation list; "Kimi K3:
+ * Architecture and SGLang Day-0 Support", section "Math details: how KDA
+ * gates and rewrites the same S"):
+ *
+ *     S  <- Diag(alpha_t) S                       decay, row j scaled by alpha_t[j]
+ *     S  <- S + beta_t k_t (v_t - S^T k_t)^T      delta-rule write
+ *     o~_t = scale * S^T q_t                      readout of the updated state
+ *
+ * with alpha_t = exp(log_alpha_t).  The state S is d_k x d_v fp32, row j =
+ * key channel j, column c = value channel c.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates, frees or retains them beyond the call.
+ *   - Every tensor pointer must be 16-byte aligned; tensors are dense and
+ *     row-major.  Token tensors are token-major [t][h][i] with i (the 128
+ *     channels) contiguous; states are [n][h][j][c].
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls are asynchronous on that stream.
+ *   - Argument errors are detected on the host before any launch and return
+ *     KDA_ERR_INVALID_ARGUMENT (or KDA_ERR_UNSUPPORTED / KDA_ERR_WORKSPACE);
+ *     nothing is written in that case.  A failed launch returns KDA_ERR_CUDA.
+ *   - Kernels never trap.  A device-side check or a bounded wait that gives
+ *     up records a code in a device status word; kda_get_device_status reads
+ *     and clears it.
+ *   - Contents are not validated on the host (values of cu_seqlens, the
+ *     range of log_alpha): those are the caller's contract.
+ *   - The library holds no mutable host state; calls are thread-safe.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_HEAD_DIM 128 /* d_k = d_v, fixed */
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARGUMENT = 1, /* null/misaligned pointer, bad size or dtype */
+    KDA_ERR_UNSUPPORTED = 2,      /* a valid request this build does not implement */
+    KDA_ERR_WORKSPACE = 3,        /* workspace missing or smaller than required */
+    KDA_ERR_CUDA = 4,             /* a CUDA runtime call or launch failed */
+    KDA_ERR_DEVICE_TIMEOUT = 5,   /* a kernel's bounded wait gave up */
+    KDA_ERR_DEVICE_CHECK = 6      /* a kernel's self-check failed */
+} kda_status;
+
+typedef enum {
+    KDA_BF16 = 0, /* bfloat16, round-to-nearest-even on output */
+    KDA_FP32 = 1
+} kda_dtype;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *kda_status_string(kda_status status);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t kda_version(void);
+
+/*
+ * Bytes of scratch that kda_prefill needs for these sizes (0 = none; the
+ * workspace pointer may then be NULL).
+ */
+size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                  kda_dtype in_dtype);
+
+/*
+ * kda_prefill - the recurrence over packed variable-length sequences.
+ *
+ * Computes, for every sequence n (tokens [cu_seqlens[n], cu_seqlens[n+1]))
+ * and head h, the token-by-token recurrence above starting from S0[n][h]
+ * (zeros when S0 is NULL), writes o~ for every token, and the state after
+ * the sequence's last token to S_final[n][h] (skipped when S_final is NULL).
+ * Implemented chunk-wise (parallel inside a chunk, recurrent across chunks:
+ * "Kimi K3's Architecture: Kimi Delta Attention, Attention Residuals, and
+ * 896 Experts", section "Channel-wise decay, and the floor K3 puts under
+ * it"), which is an exact rewrite of the recurrence up to rounding.
+ *
+ *   in_dtype     element type of q, k, v (KDA_BF16 or KDA_FP32)
+ *   out_dtype    element type of o
+ *   num_seqs     N >= 1
+ *   total_tokens T >= 0, must equal cu_seqlens[N]
+ *   num_heads    H >= 1
+ *   q, k         [T][H][128] in_dtype; expected unit-norm per head
+ *   v            [T][H][128] in_dtype
+ *   log_alpha    [T][H][128] fp32, each in [-5, 0] (the pages' decay floor
+ *                g_min = -5; values below it are outside the contract)
+ *   beta         [T][H] fp32 write strength
+ *   S0           [N][H][128][128] fp32, or NULL for zero initial states
+ *   cu_seqlens   [N+1] int32 (device): 0 = cu[0] <= cu[1] <= ... <= cu[N] = T
+ *   scale        readout scale, 1/sqrt(128) in the pages
+ *   o            [T][H][128] out_dtype
+ *   S_final      [N][H][128][128] fp32 or NULL; may alias S0 exactly (in-place
+ *                resume); partial overlap is not allowed
+ *   workspace    device scratch of at least kda_prefill_workspace_size() bytes
+ *
+ * A zero-length sequence writes no output and S_final[n] = S0[n] (or zeros).
+ * Results do not depend on how sequences are packed: a sequence gives the
+ * same bits alone or packed with others, in any order.
+ */
+kda_status kda_prefill(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
+                       int32_t total_tokens, int32_t num_heads, const void *q, const void *k,
+                       const void *v, const float *log_alpha, const float *beta,
+                       const float *S0, const int32_t *cu_seqlens, float scale, void *o,
+                       float *S_final, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * kda_decode_step - one token per request, state updated in place.
+ *
+ * One step of the recurrence for each (request b, head h): "each step reads
+ * and writes only S" ("Kimi K3: Architecture and SGLang Day-0 Support",
+ * section "Attention mechanisms in detail: linear attention").  The state is
+ * streamed through HBM exactly once (one read, one write).
+ *
+ *   batch       B >= 1 requests
+ *   q, k, v     [B][H][128] in_dtype
+ *   log_alpha   [B][H][128] fp32 (may be -inf: alpha = 0 resets the state)
+ *   beta        [B][H] fp32
+ *   S_inout     [B][H][128][128] fp32, read then overwritten
+ *   o           [B][H][128] out_dtype
+ */
+kda_status kda_decode_step(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batch,
+                           int32_t num_heads, const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *beta, float *S_inout,
+                           float scale, void *o, void *stream);
+
+/*
+ * kda_frontend - inputs of the recurrence from the pre-convolution
+ * projections ("Kimi K3 · KDA layer", KDA equation list; "Inside Kimi K3:
+ * How KDA, AttnRes, and 896 Experts Work", section "Short convolutions give
+ * KDA local order before recurrence"):
+ *
+ *   x^c_t   = SiLU( sum_{j=0..3} w_j * x^p_{t-j} )   x in {q, k, v}, per channel
+ *   q^, k^  = x^c / sqrt(sum x^c^2 + l2_eps)          per head, 128 channels
+ *   log_alpha = -5 * sigmoid( e^{A_h} (z + b) )
+ *   beta      = sigmoid(beta_logit)
+ *
+ * Tokens before the start of their own sequence count as zero.  Tap j = 0
+ * multiplies the current token.
+ *
+ *   qp, kp, vp  [T][H][128] bf16
+ *   conv_w      [3][H*128][4] fp32 (stream q/k/v, channel h*128+i, tap j)
+ *   z           [T][H][128] bf16
+ *   A           [H] fp32
+ *   b           [H][128] fp32, or NULL for zeros
+ *   beta_logit  [T][H] bf16
+ *   out_dtype   element type of q_hat, k_hat, v_out
+ *   q_hat, k_hat, v_out  [T][H][128] out_dtype
+ *   log_alpha   [T][H][128] fp32;  beta [T][H] fp32
+ */
+kda_status kda_frontend(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                        const void *qp, const void *kp, const void *vp, const float *conv_w,
+                        const void *z, const float *A, const float *b, const void *beta_logit,
+                        const int32_t *cu_seqlens, float l2_eps, kda_dtype out_dtype,
+                        void *q_hat, void *k_hat, void *v_out, float *log_alpha, float *beta,
+                        void *stream);
+
+/*
+ * kda_output_gate - o^g = sigmoid(g) * RMSNorm(o~) per head over its 128
+ * channels, RMSNorm(x) = x / sqrt(mean(x^2) + eps), unit weight ("Kimi K3 ·
+ * KDA layer", KDA equation list).
+ *
+ *   num_rows   T*H rows of 128 channels
+ *   o_tilde    [rows][128] in_dtype;  g [rows][128] bf16;  out [rows][128] out_dtype
+ */
+kda_status kda_output_gate(int64_t num_rows, kda_dtype in_dtype, const void *o_tilde,
+                           const void *g, float eps, kda_dtype out_dtype, void *out,
+                           void *stream);
+
+/*
+ * kda_get_device_status - synchronises `stream`, then returns and clears the
+ * device status word: KDA_OK, KDA_ERR_DEVICE_TIMEOUT or KDA_ERR_DEVICE_CHECK
+ * (KDA_ERR_CUDA if the synchronisation itself fails).  If detail is not
+ * NULL it receives the kernel-specific code recorded with the status (0 if
+ * none).
+ */
+kda_status kda_get_device_status(void *stream, uint32_t *detail);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads,
+exports every entry point include/kda.h declares, and rejects bad arguments
+on the host before any launch (nothing is dereferenced in these calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kda():
+    from gated_delta_rule_kda_gb300 import build
+    build.build()
+    from gated_delta_rule_kda_gb300 import kda as mod
+    return mod
+
+
+def declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(kda_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(kda):
+    declared = declared_symbols()
+    assert declared, "no declarations parsed"
+    assert declared == set(kda.EXPORTED)
+    lib = kda.library()
+    for name in declared:
+        assert hasattr(lib, name), name
+    # and the shared object's dynamic symbol table really has them
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", kda.library_path()], capture_output=True,
+                         text=True).stdout
+    for name in declared:
+        assert re.search(rf"\bT {name}$", out, re.M), f"{name} not exported"
+
+
+def test_status_strings(kda):
+    lib = kda.library()
+    for code, name in kda.STATUS_NAMES.items():
+        assert lib.kda_status_string(code).decode() == name
+    assert lib.kda_version() >= 100
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation first
+MIS = 0x10008   # misaligned
+
+
+def _prefill(lib, **kw):
+    a = dict(in_dt=0, out_dt=0, N=1, T=4, H=2, q=FAKE, k=FAKE, v=FAKE, la=FAKE, beta=FAKE,
+             S0=None, cu=FAKE, scale=0.1, o=FAKE, Sf=None, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.kda_prefill(a["in_dt"], a["out_dt"], a["N"], a["T"], a["H"], a["q"], a["k"],
+                           a["v"], a["la"], a["beta"], a["S0"], a["cu"], a["scale"], a["o"],
+                           a["Sf"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(in_dt=7), dict(out_dt=-1), dict(N=0), dict(H=0), dict(T=-1),
+    dict(q=None), dict(k=MIS), dict(v=None), dict(la=MIS), dict(beta=None), dict(o=None),
+    dict(cu=None), dict(S0=MIS), dict(Sf=MIS),
+    dict(S0=FAKE, Sf=FAKE + 64),   # partial overlap of S0 and S_final
+])
+def test_prefill_rejects_bad_arguments(kda, bad):
+    assert _prefill(kda.library(), **bad) == 1  # KDA_ERR_INVALID_ARGUMENT
+
+
+def test_prefill_too_many_heads_unsupported(kda):
+    assert _prefill(kda.library(), H=70000) == 2
+
+
+@pytest.mark.parametrize("bad", [dict(B=0), dict(H=0), dict(q=None), dict(S=MIS), dict(o=None),
+                                 dict(in_dt=3)])
+def test_decode_rejects_bad_arguments(kda, bad):
+    a = dict(in_dt=0, out_dt=0, B=2, H=2, q=FAKE, k=FAKE, v=FAKE, la=FAKE, beta=FAKE, S=FAKE,
+             o=FAKE)
+    a.update(bad)
+    rc = kda.library().kda_decode_step(a["in_dt"], a["out_dt"], a["B"], a["H"], a["q"], a["k"],
+                                       a["v"], a["la"], a["beta"], a["S"], 0.1, a["o"], None)
+    assert rc == 1
+
+
+def test_frontend_and_gate_reject_bad_arguments(kda):
+    lib = kda.library()
+    rc = lib.kda_frontend(1, 4, 2, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, FAKE, FAKE, 1e-6, 0,
+                          FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    assert rc == 1
+    rc = lib.kda_frontend(1, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, MIS, FAKE, FAKE, 1e-6, 0,
+                          FAKE, FAKE, FAKE, FAKE, FAKE, None)
+    assert rc == 1
+    assert lib.kda_output_gate(8, 0, None, FAKE, 1e-6, 0, FAKE, None) == 1
+    assert lib.kda_output_gate(8, 0, FAKE, FAKE, 1e-6, 9, FAKE, None) == 1
+    assert lib.kda_output_gate(-1, 0, FAKE, FAKE, 1e-6, 0, FAKE, None) == 1
+
+
+def test_workspace_size_is_callable(kda):
+    assert kda.kda_prefill_workspace_size(1, 8192, 96) >= 0
