@@ -311,6 +311,32 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def run_only(args, local):
+    """One kernel on its own (for ncu): W warm-up + K launches, one summary line."""
+    from gated_delta_rule_kda_gb300 import kda, synthetic
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if args.only == "prefill":
+        T = 2048 if args.small else 8192
+        inp = synthetic.prefill_inputs([T], 96, torch.bfloat16, seed=synthetic.BASE_SEED + 2,
+                                       device=dev)
+        o = torch.empty((T, 96, D), dtype=torch.bfloat16, device=dev)
+        Sf = torch.empty((1, 96, D, D), dtype=torch.float32, device=dev)
+        fn = lambda: kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta,
+                                     inp.cu_seqlens, None, o=o, S_final=Sf)
+        units = T
+    else:
+        B = 32 if args.small else 256
+        dinp = synthetic.decode_inputs(B, 96, torch.bfloat16, device=dev)
+        od = torch.empty((B, 96, D), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_decode_step(dinp.q, dinp.k, dinp.v, dinp.log_alpha, dinp.beta,
+                                         dinp.S, o=od)
+        units = B
+    total, per = time_launches(fn, args.steps, args.warmup, 1)
+    print(json.dumps({"only": args.only, "small": args.small, "units": units,
+                      "ms_mean": sum(per) / len(per), "ms_min": min(per)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -318,6 +344,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="profiling aid: run just this kernel (no baseline, no e2e)")
+    ap.add_argument("--small", action="store_true",
+                    help="with --only: a smaller case sized for ncu captures")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
@@ -326,6 +356,9 @@ def main():
         run_reference(args, world, rank)
         return
     world, rank, local = dist_setup()
+    if args.only:
+        run_only(args, local)
+        return
     run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist

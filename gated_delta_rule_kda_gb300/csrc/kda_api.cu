@@ -30,6 +30,10 @@ DeviceStatus device_status() {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool ok_ptr(const void *p) { return p != nullptr && aligned16(p); }
 bool ok_opt_ptr(const void *p) { return p == nullptr || aligned16(p); }
+// Per-row scalars (beta, cu_seqlens, beta_logit) need only their element alignment.
+bool ok_ptr_elem(const void *p, size_t align) {
+    return p != nullptr && (reinterpret_cast<uintptr_t>(p) & (align - 1)) == 0;
+}
 bool ok_dtype(kda_dtype d) { return d == KDA_BF16 || d == KDA_FP32; }
 
 bool overlap(const void *a, const void *b, size_t bytes) {
@@ -74,9 +78,9 @@ kda_status kda_prefill(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs
                        float *S_final, void *workspace, size_t workspace_bytes, void *stream) {
     if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
     if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
-    if (!ok_ptr(cu_seqlens)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_ptr_elem(cu_seqlens, 4)) return KDA_ERR_INVALID_ARGUMENT;
     if (total_tokens > 0) {
-        if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(log_alpha) || !ok_ptr(beta) ||
+        if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(log_alpha) || !ok_ptr_elem(beta, 4) ||
             !ok_ptr(o))
             return KDA_ERR_INVALID_ARGUMENT;
     }
@@ -105,7 +109,7 @@ kda_status kda_decode_step(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batc
                            float scale, void *o, void *stream) {
     if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
     if (batch < 1 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
-    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(log_alpha) || !ok_ptr(beta) ||
+    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(log_alpha) || !ok_ptr_elem(beta, 4) ||
         !ok_ptr(S_inout) || !ok_ptr(o))
         return KDA_ERR_INVALID_ARGUMENT;
     if ((int64_t)batch * num_heads > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
@@ -126,12 +130,12 @@ kda_status kda_frontend(int32_t num_seqs, int32_t total_tokens, int32_t num_head
                         void *stream) {
     if (!ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
     if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
-    if (!ok_ptr(cu_seqlens) || !ok_ptr(conv_w) || !ok_ptr(A) || !ok_opt_ptr(b))
+    if (!ok_ptr_elem(cu_seqlens, 4) || !ok_ptr(conv_w) || !ok_ptr_elem(A, 4) || !ok_opt_ptr(b))
         return KDA_ERR_INVALID_ARGUMENT;
     if (total_tokens > 0) {
-        if (!ok_ptr(qp) || !ok_ptr(kp) || !ok_ptr(vp) || !ok_ptr(z) || !ok_ptr(beta_logit) ||
+        if (!ok_ptr(qp) || !ok_ptr(kp) || !ok_ptr(vp) || !ok_ptr(z) || !ok_ptr_elem(beta_logit, 2) ||
             !ok_ptr(q_hat) || !ok_ptr(k_hat) || !ok_ptr(v_out) || !ok_ptr(log_alpha) ||
-            !ok_ptr(beta))
+            !ok_ptr_elem(beta, 4))
             return KDA_ERR_INVALID_ARGUMENT;
     }
     if ((int64_t)total_tokens * num_heads / 8 >= 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;

@@ -17,9 +17,11 @@
  * Conventions shared by every entry point
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
  *     library never allocates, frees or retains them beyond the call.
- *   - Every tensor pointer must be 16-byte aligned; tensors are dense and
- *     row-major.  Token tensors are token-major [t][h][i] with i (the 128
- *     channels) contiguous; states are [n][h][j][c].
+ *   - Every tensor pointer must be 16-byte aligned, except per-row scalars
+ *     (beta, beta_logit, A, cu_seqlens), which need only their element's
+ *     alignment.  Tensors are dense and row-major.  Token tensors are
+ *     token-major [t][h][i] with i (the 128 channels) contiguous; states are
+ *     [n][h][j][c].
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Calls are asynchronous on that stream.
  *   - Argument errors are detected on the host before any launch and return

@@ -61,7 +61,9 @@ def test_edge_cases(kda, case):
     elif case == "beta_one":
         inp.beta.fill_(1.0)
     elif case == "beta_zero":
+        # no writes: the state only decays; slow decay keeps it inside fp32 range
         inp.beta.zero_()
+        inp.log_alpha.mul_(0.02)
     check(kda, inp, TOL_BF16, torch.float32)
 
 
