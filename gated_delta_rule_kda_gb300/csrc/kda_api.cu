@@ -100,6 +100,9 @@ kda_status kda_prefill(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs
     a.cu_seqlens = cu_seqlens; a.scale = scale; a.o = o; a.S_final = S_final;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
     a.status = device_status();
+    // bf16 inputs: chunked tensor-core kernel; fp32 inputs: full-precision recurrent kernel.
+    if (in_dtype == KDA_BF16)
+        return from_cuda(launch_prefill_tc(a, static_cast<cudaStream_t>(stream)));
     return from_cuda(launch_prefill_recurrent(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -113,6 +113,7 @@ struct GateArgs {
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_recurrent(const PrefillArgs &a, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 cudaError_t launch_frontend(const FrontendArgs &a, cudaStream_t stream);
 cudaError_t launch_output_gate(const GateArgs &a, cudaStream_t stream);
 
