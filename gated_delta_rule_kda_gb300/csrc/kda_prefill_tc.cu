@@ -28,7 +28,8 @@
 // The state is held TRANSPOSED (TMEM lane = value channel c, column = key
 // channel j), so every product is an M = 128 tcgen05.mma:
 //   M1  G = [k E ; q E] . (k E^-1)^T                  (lanes 0-31 -> A, 32-63 -> P)
-//   M2  W^T = (k Gamma)^T . Tb^T,   U~^T = V^T . Tb^T  (A read MN-major)
+//   M2  U~^T = V^T . Tb^T                            (V read MN-major from its staged tile)
+//   M2b W = Tb . (k Gamma)       (rows r in lanes 0-31; B read MN-major)
 //   M3  [ (W S0)^T | (Q~ S0)^T ] = S0^T . [W ; Q~]^T   (A = S0^T from TMEM)
 //   M4  (Q~ S0 + P U)^T += U^T . P^T
 //   M5  S^T += U^T . K^        (S^T scaled by Gamma_C along j first; B read MN-major)
@@ -72,8 +73,8 @@ constexpr int kLd = 33;  // padded row stride of A and T
 // ---- TMEM column map (512 columns) -----------------------------------------
 constexpr uint32_t TM_ST = 0;    // S^T fp32 [c][j]
 constexpr uint32_t TM_D1 = 128;  // [(W S0)^T | (Q~ S0 + P U)^T] (32 + 32); Gram result during M1
-constexpr uint32_t TM_DW = 192;  // [W^T | U~^T] (32 + 32)
-constexpr uint32_t TM_OPG = 256; // M1's A operand: hi (64) | lo (64)
+constexpr uint32_t TM_DW = 192;  // [unused | U~^T] (32 + 32)
+constexpr uint32_t TM_OPG = 256; // M1's A operand: hi (64) | lo (64); then W (lanes 0-31, 128 cols)
 constexpr uint32_t TM_OPS = 384; // M3's A operand S^T hi (64) | lo (64); then U^T hi (16) | lo (16)
 
 // Swizzled [32 rows][128 bf16] tile: two 64-column blocks of 32 x 128 bytes,
@@ -120,13 +121,19 @@ __device__ __forceinline__ void store_split_chunk(unsigned char *hi, unsigned ch
     *reinterpret_cast<uint4 *>(lo) = l;
 }
 
+// One thread waits for the tensor core (bounded); the CTA barrier then orders
+// every other thread after the completed MMAs.
 __device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, DeviceStatus st,
                                          uint32_t where) {
-    const bool ok = mbar_wait_bounded(bar, phase & 1u, kWaitNs);
+    bool ok = true;
+    if (threadIdx.x == 0) {
+        ok = mbar_wait_bounded(bar, phase & 1u, kWaitNs);
+        if (!ok) record_status(st, KDA_ERR_DEVICE_TIMEOUT, where);
+    }
     ++phase;
-    if (!ok) record_status(st, KDA_ERR_DEVICE_TIMEOUT, where);
+    ok = __syncthreads_and(ok) != 0;
     fence_after_sync();
-    return __syncthreads_and(ok) != 0;
+    return ok;
 }
 
 // Operand writes (generic-proxy smem stores and tcgen05.st) -> visible to the MMA.
@@ -235,38 +242,40 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
             issue_loads(p, sm + ((chunk + 1) & 1) * IB_SIZE, t0 + kC, min(kC, t_end - t0 - kC), h,
                         tid);
 
-        // ---- F2: decay factors D = gamma - gamma_15, E = e^D, E^-1 = e^-D ----
+        // ---- F2: decay factors in log2 units: D = (gamma - gamma_15) log2(e),
+        //      E = 2^D, E^-1 = 2^-D ----
         {
             const int c = tid & 127;
             const float *la = reinterpret_cast<const float *>(buf + IB_LA);
+            const float kL2E = 1.4426950408889634f;
+            const uint32_t cq = (uint32_t)(c >> 2), cb = (uint32_t)((c & 3) << 2);
             float acc = 0.f;
             if (half == 0) {  // rows 15..0: D_r = -(sum of log alpha over rows r+1..15)
 #pragma unroll
                 for (int r = 15; r >= 0; --r) {
-                    const float d = -acc;
-                    const uint32_t off = e_chunk(r, c >> 2) + ((c & 3) << 2);
-                    *reinterpret_cast<float *>(sm + W_E + off) = expf(d);
-                    *reinterpret_cast<float *>(sm + W_EI + off) = expf(-d);
-                    acc += la[r * kD + c];
+                    const uint32_t off = (uint32_t)(r * 512) + ((cq ^ (uint32_t)r) << 4) + cb;
+                    *reinterpret_cast<float *>(sm + W_E + off) = ex2_approx(-acc);
+                    *reinterpret_cast<float *>(sm + W_EI + off) = ex2_approx(acc);
+                    acc = fmaf(la[r * kD + c], kL2E, acc);
                 }
-                vec[V_M + c] = acc;  // gamma_15
-                vec[V_EM + c] = expf(acc);
+                vec[V_M + c] = acc;  // gamma_15 log2(e)
+                vec[V_EM + c] = ex2_approx(acc);
             } else {  // rows 16..31: D_r = sum of log alpha over rows 16..r
 #pragma unroll
                 for (int r = 16; r < 32; ++r) {
-                    acc += la[r * kD + c];
-                    const uint32_t off = e_chunk(r, c >> 2) + ((c & 3) << 2);
-                    *reinterpret_cast<float *>(sm + W_E + off) = expf(acc);
-                    *reinterpret_cast<float *>(sm + W_EI + off) = expf(-acc);
+                    acc = fmaf(la[r * kD + c], kL2E, acc);
+                    const uint32_t off = (uint32_t)(r * 512) + ((cq ^ (uint32_t)r) << 4) + cb;
+                    *reinterpret_cast<float *>(sm + W_E + off) = ex2_approx(acc);
+                    *reinterpret_cast<float *>(sm + W_EI + off) = ex2_approx(-acc);
                 }
                 vec[V_D31 + c] = acc;
-                vec[V_E31 + c] = expf(acc);
+                vec[V_E31 + c] = ex2_approx(acc);
             }
         }
         __syncthreads();
 
         // ---- F3: operands that do not depend on the state ----
-        if (tid < kD) vec[V_GC + tid] = expf(vec[V_M + tid] + vec[V_D31 + tid]);  // Gamma_C
+        if (tid < kD) vec[V_GC + tid] = ex2_approx(vec[V_M + tid] + vec[V_D31 + tid]);  // Gamma_C
         if (trow < 64) {  // M1's A operand into TMEM: rows 0..31 k E, rows 32..63 q E
             const int r = trow & 31;
             const unsigned char *src = buf + (trow < 32 ? IB_K : IB_Q);
@@ -287,42 +296,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
             tmem_st32(tl + TM_OPG + 32 * half, hw);
             tmem_st32(tl + TM_OPG + 64 + 32 * half, lw);
         }
-        // 16-byte-chunk jobs: R = k E^-1 (M1 B), k Gamma (M2 A), K^ (M5 B), Q~ (M3 B rows 32..63)
-#pragma unroll 2
+        // 16-byte-chunk jobs: R = k E^-1 (M1 B), k Gamma (M2b B), K^ (M5 B), Q~ (M3 B rows 32..63)
+#pragma unroll
         for (int m = 0; m < 8; ++m) {
-            const int e = tid + kThreads * m;  // 2048 jobs
-            const int job = e >> 9, rem = e & 511;
+            const int job = m >> 1;
+            const int rem = tid + kThreads * (m & 1);
             const int i = rem >> 4, cc = rem & 15;
             float x[8];
             bf16x8_to_f32(*reinterpret_cast<const uint4 *>(buf + (job == 3 ? IB_Q : IB_K) +
                                                            tile_chunk(i, cc)),
                           x);
             const uint32_t fsrc = (job == 0 || job == 2) ? W_EI : W_E;
-            const float4 f0 = *reinterpret_cast<const float4 *>(sm + fsrc + e_chunk(i, 2 * cc));
-            const float4 f1 =
-                *reinterpret_cast<const float4 *>(sm + fsrc + e_chunk(i, 2 * cc + 1));
-            x[0] *= f0.x; x[1] *= f0.y; x[2] *= f0.z; x[3] *= f0.w;
-            x[4] *= f1.x; x[5] *= f1.y; x[6] *= f1.z; x[7] *= f1.w;
+            float4 f0 = *reinterpret_cast<const float4 *>(sm + fsrc + e_chunk(i, 2 * cc));
+            float4 f1 = *reinterpret_cast<const float4 *>(sm + fsrc + e_chunk(i, 2 * cc + 1));
             if (job != 0) {  // channel factor: e^m (k Gamma, Q~) or E_31 (K^)
                 const float *cf = vec + (job == 2 ? V_E31 : V_EM) + 8 * cc;
-#pragma unroll
-                for (int t = 0; t < 8; ++t) x[t] *= cf[t];
+                const float4 c0 = *reinterpret_cast<const float4 *>(cf);
+                const float4 c1 = *reinterpret_cast<const float4 *>(cf + 4);
+                f0.x *= c0.x; f0.y *= c0.y; f0.z *= c0.z; f0.w *= c0.w;
+                f1.x *= c1.x; f1.y *= c1.y; f1.z *= c1.z; f1.w *= c1.w;
             }
-            unsigned char *hi, *lo;
+            const float2 p0 = mul2(make_float2(x[0], x[1]), make_float2(f0.x, f0.y));
+            const float2 p1 = mul2(make_float2(x[2], x[3]), make_float2(f0.z, f0.w));
+            const float2 p2 = mul2(make_float2(x[4], x[5]), make_float2(f1.x, f1.y));
+            const float2 p3 = mul2(make_float2(x[6], x[7]), make_float2(f1.z, f1.w));
+            const float y[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
+            unsigned char *hi;
+            uint32_t lo_off;
             if (job == 0) {
                 hi = sm + W_R + tile_chunk(i, cc);
-                lo = hi + 8192;
+                lo_off = 8192;
             } else if (job == 1) {
                 hi = sm + W_KT + tile_chunk(i, cc);
-                lo = hi + 8192;
+                lo_off = 8192;
             } else if (job == 2) {
                 hi = sm + W_KH + tile_chunk(i, cc);
-                lo = hi + 8192;
+                lo_off = 8192;
             } else {
                 hi = sm + W_WQ + sw128_chunk_offset(64, 32 + i, cc);
-                lo = hi + 16384;
+                lo_off = 16384;
             }
-            store_split_chunk(hi, lo, x);
+            store_split_chunk(hi, hi + lo_off, y);
         }
         publish_operands();
         if (tid == 0) {  // M1: Gram
@@ -351,7 +365,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
 #pragma unroll
             for (int pp = 0; pp < 16; ++pp) split2(sv[2 * pp], sv[2 * pp + 1], hw[pp], lw[pp]);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) sc[jj] = __float_as_uint(sv[jj] * vec[V_GC + j0 + jj]);
+            for (int jj = 0; jj < 32; jj += 4) {
+                const float4 g4 = *reinterpret_cast<const float4 *>(vec + V_GC + j0 + jj);
+                const float2 a = mul2(make_float2(sv[jj], sv[jj + 1]), make_float2(g4.x, g4.y));
+                const float2 b = mul2(make_float2(sv[jj + 2], sv[jj + 3]), make_float2(g4.z, g4.w));
+                sc[jj] = __float_as_uint(a.x);
+                sc[jj + 1] = __float_as_uint(a.y);
+                sc[jj + 2] = __float_as_uint(b.x);
+                sc[jj + 3] = __float_as_uint(b.y);
+            }
             tmem_st16u(tl + TM_OPS + (j0 >> 1), hw);
             tmem_st16u(tl + TM_OPS + 64 + (j0 >> 1), lw);
             tmem_st32(tl + TM_ST + j0, sc);
@@ -419,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
             sT[(16 + r) * kLd + i] = -y;
         }
         __syncthreads();
-        if (tid < 128) {  // Tb -> M2's B operand (32 rows x 32 K)
+        if (tid < 128) {  // Tb -> M2's B operand and M2b's A operand (32 rows x 32 K)
             const int r = tid >> 2, cc = tid & 3;
             float x[8];
 #pragma unroll
@@ -431,49 +453,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
                               sm + W_R + 4096 + sw128_chunk_offset(32, r, cc), x);
         }
         publish_operands();
-        if (tid == 0) {  // M2: W^T = (k Gamma)^T Tb^T,  U~^T = V^T Tb^T
-            const uint32_t id = idesc_bf16_f32(128, 32) | kIdescAMN;
+        if (tid == 0) {
             const uint32_t th = smem_u32(sm + W_R), tlo = th + 4096;
-            const uint32_t kh = smem_u32(sm + W_KT), kl = kh + 8192;
+            // M2: U~^T = V^T Tb^T  (V exact in bf16, read MN-major from the staged tile)
+            const uint32_t idv = idesc_bf16_f32(128, 32) | kIdescAMN;
             const uint32_t va = smem_u32(buf + IB_V);
 #pragma unroll
             for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_DW, sw128_desc_mn(kh + 2048 * s, 4096), sw128_desc_k(th, 32, s),
-                         id, s > 0);
-#pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_DW, sw128_desc_mn(kh + 2048 * s, 4096), sw128_desc_k(tlo, 32, s),
-                         id, 1);
-#pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_DW, sw128_desc_mn(kl + 2048 * s, 4096), sw128_desc_k(th, 32, s),
-                         id, 1);
+                mma_bf16(tb + TM_DW + 32, sw128_desc_mn(va + 2048 * s, 4096),
+                         sw128_desc_k(th, 32, s), idv, s > 0);
 #pragma unroll
             for (int s = 0; s < 2; ++s)
                 mma_bf16(tb + TM_DW + 32, sw128_desc_mn(va + 2048 * s, 4096),
-                         sw128_desc_k(th, 32, s), id, s > 0);
+                         sw128_desc_k(tlo, 32, s), idv, 1);
+            // M2b: W = Tb (k Gamma): A = Tb (rows r; lanes >= 32 unused), B = (k Gamma) MN-major
+            const uint32_t idw = idesc_bf16_f32(128, 128) | kIdescBMN;
+            const uint32_t kh = smem_u32(sm + W_KT), kl = kh + 8192;
 #pragma unroll
             for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_DW + 32, sw128_desc_mn(va + 2048 * s, 4096),
-                         sw128_desc_k(tlo, 32, s), id, 1);
+                mma_bf16(tb + TM_OPG, sw128_desc_k(th, 128, s), sw128_desc_mn(kh + 2048 * s, 4096),
+                         idw, s > 0);
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+                mma_bf16(tb + TM_OPG, sw128_desc_k(th, 128, s), sw128_desc_mn(kl + 2048 * s, 4096),
+                         idw, 1);
+#pragma unroll
+            for (int s = 0; s < 2; ++s)
+                mma_bf16(tb + TM_OPG, sw128_desc_k(tlo, 128, s), sw128_desc_mn(kh + 2048 * s, 4096),
+                         idw, 1);
             mma_commit(bar);
         }
         alive = wait_mma(bar, phase, p.status, 2);
         if (!alive) break;
 
-        // ---- F7: W rows of M3's B operand (lane j holds W[r][j]) ----
-        {
-            const int j = trow;
-            float w[16];
-            tmem_ld16(tl + TM_DW + 16 * half, w);
+        // ---- F7: W rows (TMEM lanes 0..31) -> rows 0..31 of M3's B operand ----
+        if (quarter == 0) {
+            const int r = lane;
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int r = 16 * half + e;
-                const __nv_bfloat16 hb = __float2bfloat16_rn(w[e]);
-                const __nv_bfloat16 lb = __float2bfloat16_rn(w[e] - __bfloat162float(hb));
-                const uint32_t off = sw128_offset(64, r, j);
-                *reinterpret_cast<__nv_bfloat16 *>(sm + W_WQ + off) = hb;
-                *reinterpret_cast<__nv_bfloat16 *>(sm + W_WQ + 16384 + off) = lb;
+            for (int part = 0; part < 2; ++part) {
+                const int j0 = 64 * half + 32 * part;
+                float w[32];
+                tmem_ld32(tl + TM_OPG + j0, w);
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    const float x[8] = {w[8 * q8], w[8 * q8 + 1], w[8 * q8 + 2], w[8 * q8 + 3],
+                                        w[8 * q8 + 4], w[8 * q8 + 5], w[8 * q8 + 6], w[8 * q8 + 7]};
+                    const int cc = (j0 >> 3) + q8;
+                    unsigned char *hi = sm + W_WQ + sw128_chunk_offset(64, r, cc);
+                    store_split_chunk(hi, hi + 16384, x);
+                }
             }
         }
         publish_operands();

@@ -290,10 +290,29 @@ __device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-    float2 hf = __bfloat1622float2(h);
-    __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
     hi = *reinterpret_cast<uint32_t *>(&h);
+    // residuals a - bf16(a), b - bf16(b) with one packed fp32x2 subtraction
+    const uint64_t x = ((uint64_t)__float_as_uint(b) << 32) | __float_as_uint(a);
+    const uint64_t hx = ((uint64_t)(hi & 0xFFFF0000u) << 32) | (uint64_t)(hi << 16);
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(hx));
+    __nv_bfloat162 l = __floats2bfloat162_rn(__uint_as_float((uint32_t)r),
+                                             __uint_as_float((uint32_t)(r >> 32)));
     lo = *reinterpret_cast<uint32_t *>(&l);
+}
+// Packed fp32x2 multiply: (a0, a1) * (b0, b1).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t x = ((uint64_t)__float_as_uint(a.y) << 32) | __float_as_uint(a.x);
+    uint64_t y = ((uint64_t)__float_as_uint(b.y) << 32) | __float_as_uint(b.x);
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
+    return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+// 2^x on the SFU (max relative error about 2^-22).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 }  // namespace tc
