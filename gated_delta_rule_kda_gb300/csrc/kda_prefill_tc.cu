@@ -29,16 +29,21 @@
 // channel j), so every product is an M = 128 tcgen05.mma:
 //   M1  G = [k E ; q E] . (k E^-1)^T                  (lanes 0-31 -> A, 32-63 -> P)
 //   M2  U~^T = V^T . Tb^T                            (V read MN-major from its staged tile)
-//   M2b W = Tb . (k Gamma)       (rows r in lanes 0-31; B read MN-major)
+//   M2b W' = Tb . (k E)          (Tb repeated in all four lane quarters; B read MN-major)
 //   M3  [ (W S0)^T | (Q~ S0)^T ] = S0^T . [W ; Q~]^T   (A = S0^T from TMEM)
 //   M4  (Q~ S0 + P U)^T += U^T . P^T
-//   M5  S^T += U^T . K^        (S^T scaled by Gamma_C along j first; B read MN-major)
+//   M5  X^T += U^T . (k E^-1)    (the state kept as X = S / e31; B read MN-major)
 //
 // Precision: an fp32 quantity x enters an MMA as x = hi + lo (two bf16,
 // round-to-nearest), and a product X.Y is formed as hi.hi + hi.lo + lo.hi
 // (fp32 accumulation); V is exact in bf16 and enters once.
 //
-// Inputs of chunk c+1 are staged with cp.async while chunk c is processed.
+// Inputs of chunk c+1 are staged with TMA (q, k, v, log_alpha) and cp.async (beta)
+// while chunk c is processed.
+#include <cuda.h>
+#include <cstring>
+#include <cudaTypedefs.h>
+
 #include "kda_common.cuh"
 #include "tc_primitives.cuh"
 
@@ -52,37 +57,40 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // bound on every wait for the tens
 
 // ---- shared memory map (bytes from a 1024-aligned base) --------------------
 // Two input buffers, each: q, k, v tiles (bf16 [32][128] in the swizzled tile
-// layout below), log_alpha (fp32 [32][128] natural), beta [32].
+// layout below, written by TMA with 128-byte swizzle), log_alpha (fp32, four
+// [32 rows][32 channels] boxes of 4096 bytes), beta [32].
 constexpr uint32_t IB_Q = 0, IB_K = 8192, IB_V = 16384, IB_LA = 24576, IB_BETA = 40960;
 constexpr uint32_t IB_SIZE = 43008;
-constexpr uint32_t W_E = 2 * IB_SIZE;     // fp32 [32][128]  e^{D}
-constexpr uint32_t W_EI = W_E + 16384;    // fp32 [32][128]  e^{-D}
-constexpr uint32_t W_R = W_EI + 16384;    // R hi|lo (M1 B); then Tb hi|lo, P hi|lo (4 KB each)
-constexpr uint32_t W_KT = W_R + 16384;    // (k Gamma) hi|lo, MN-major A of M2
-constexpr uint32_t W_KH = W_KT + 16384;   // K^ hi|lo, MN-major B of M5
-constexpr uint32_t W_WQ = W_KH + 16384;   // [W ; Q~] hi (16 KB) | lo (16 KB), B of M3
-constexpr uint32_t W_A = W_WQ + 32768;    // fp32 [32][33]
-constexpr uint32_t W_T = W_A + 4224;      // fp32 [32][33]
-constexpr uint32_t W_VEC = W_T + 4224;    // per-channel vectors (below)
-constexpr uint32_t W_BAR = W_VEC + 5 * 512;
-constexpr uint32_t W_TSLOT = W_BAR + 8;
+constexpr uint32_t W_E = 2 * IB_SIZE;    // fp32 [32][128] 2^D, then (solve) Tb x4 hi (16 KB)
+constexpr uint32_t W_EI = W_E + 16384;   // fp32 [32][128] 2^-D, then Tb x4 lo (16 KB)
+constexpr uint32_t W_X = W_EI + 16384;   // [k E ; q E] hi (16 KB) | lo (16 KB), 64 rows x 128 K
+constexpr uint32_t W_R = W_X + 32768;    // R = k E^-1 hi (8 KB) | lo (8 KB), 32 rows x 128 K
+constexpr uint32_t W_WQ = W_R + 16384;   // [W ; Q~] hi (16 KB) | lo (16 KB), 64 rows x 128 K
+constexpr uint32_t W_P = W_WQ + 32768;   // P hi (4 KB) | lo (4 KB), 32 rows x 32 K
+constexpr uint32_t W_A = W_P + 8192;     // fp32 [32][33]
+constexpr uint32_t W_T = W_A + 4224;     // fp32 [32][33]
+constexpr uint32_t W_VEC = W_T + 4224;   // em[2][128], e31[2][128] (by chunk parity)
+constexpr uint32_t W_BAR = W_VEC + 4 * 512;   // two MMA mbarriers, then two TMA mbarriers
+constexpr uint32_t W_TSLOT = W_BAR + 32;
+constexpr uint32_t kTmaBytes = 10 * 4096;        // 6 bf16 boxes (q, k, v) + 4 fp32 boxes
 constexpr uint32_t SM_DYN = W_TSLOT + 8 + 1024;  // + alignment slack
-constexpr int V_M = 0, V_EM = 128, V_D31 = 256, V_E31 = 384, V_GC = 512;  // float offsets
 constexpr int kLd = 33;  // padded row stride of A and T
 
 // ---- TMEM column map (512 columns) -----------------------------------------
-constexpr uint32_t TM_ST = 0;    // S^T fp32 [c][j]
-constexpr uint32_t TM_D1 = 128;  // [(W S0)^T | (Q~ S0 + P U)^T] (32 + 32); Gram result during M1
-constexpr uint32_t TM_DW = 192;  // [unused | U~^T] (32 + 32)
-constexpr uint32_t TM_OPG = 256; // M1's A operand: hi (64) | lo (64); then W (lanes 0-31, 128 cols)
-constexpr uint32_t TM_OPS = 384; // M3's A operand S^T hi (64) | lo (64); then U^T hi (16) | lo (16)
+constexpr uint32_t TM_ST = 0;    // state, stored as S^T / e31 (lane c, column j), fp32
+constexpr uint32_t TM_D1 = 128;  // [(W S0)^T | (Q~ S0 + P U)^T] (32 + 32)
+constexpr uint32_t TM_DG = 192;  // Gram result, K steps 0-3 (lanes 0-31 k rows, 32-63 q rows)
+constexpr uint32_t TM_DU = 224;  // Gram result, K steps 4-7; then U~^T (32 columns)
+constexpr uint32_t TM_WT = 256;  // W' = Tb (k E) (rows r repeated in every lane quarter), 128
+                                 // columns; then the K steps 4-7 half of M3 (64 columns)
+constexpr uint32_t TM_OPS = 384; // M3's A operand S0^T hi (64) | lo (64); then U^T hi (16) | lo (16)
 
-// Swizzled [32 rows][128 bf16] tile: two 64-column blocks of 32 x 128 bytes,
-// 16-byte chunk j of row i at chunk position j ^ (i % 8).  Read as a K-major
-// operand it has 32 rows and K = 128; read MN-major it has K = 32 rows and
-// MN = 128 (64-element blocks 4096 bytes apart).
-__device__ __forceinline__ uint32_t tile_chunk(int i, int cc) {
-    return (uint32_t)((cc >> 3) * 4096 + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
+// Swizzled [rows][128 bf16] operand tile with `rows` rows: two 64-column blocks
+// of rows x 128 bytes, 16-byte chunk j of row i at chunk position j ^ (i % 8).
+// Read K-major it has `rows` rows and K = 128; read MN-major (K = the rows) its
+// 64-element MN blocks are rows * 128 bytes apart.
+__device__ __forceinline__ uint32_t tile_chunk(int rows, int i, int cc) {
+    return (uint32_t)((cc >> 3) * rows * 128 + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
 }
 // fp32 [32][128] with 16-byte chunks swizzled by row.
 __device__ __forceinline__ uint32_t e_chunk(int r, int q) {  // q = 4-float chunk 0..31
@@ -90,6 +98,7 @@ __device__ __forceinline__ uint32_t e_chunk(int r, int q) {  // q = 4-float chun
 }
 
 struct Params {
+    CUtensorMap tm_q, tm_k, tm_v, tm_la;  // [T][H*128] with boxes of 32 tokens
     const __nv_bfloat16 *q, *k, *v;
     const float *log_alpha, *beta, *S0;
     const int32_t *cu_seqlens;
@@ -121,13 +130,24 @@ __device__ __forceinline__ void store_split_chunk(unsigned char *hi, unsigned ch
     *reinterpret_cast<uint4 *>(lo) = l;
 }
 
-// One thread waits for the tensor core (bounded); the CTA barrier then orders
-// every other thread after the completed MMAs.
+__device__ __forceinline__ void mul8(float (&x)[8], const float4 &a, const float4 &b) {
+    const float2 p0 = mul2(make_float2(x[0], x[1]), make_float2(a.x, a.y));
+    const float2 p1 = mul2(make_float2(x[2], x[3]), make_float2(a.z, a.w));
+    const float2 p2 = mul2(make_float2(x[4], x[5]), make_float2(b.x, b.y));
+    const float2 p3 = mul2(make_float2(x[6], x[7]), make_float2(b.z, b.w));
+    x[0] = p0.x; x[1] = p0.y; x[2] = p1.x; x[3] = p1.y;
+    x[4] = p2.x; x[5] = p2.y; x[6] = p3.x; x[7] = p3.y;
+}
+
+// MMAs are issued by two threads (lane 0 of warps 0 and 1), each tracking its
+// own work on its own mbarrier.  Those two threads wait (bounded) for their
+// barrier; the CTA barrier then orders every other thread after both.
+constexpr int kIssuerA = 0, kIssuerB = 32;
 __device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, DeviceStatus st,
                                          uint32_t where) {
     bool ok = true;
-    if (threadIdx.x == 0) {
-        ok = mbar_wait_bounded(bar, phase & 1u, kWaitNs);
+    if (threadIdx.x == kIssuerA || threadIdx.x == kIssuerB) {
+        ok = mbar_wait_bounded(bar + (threadIdx.x == kIssuerB), phase & 1u, kWaitNs);
         if (!ok) record_status(st, KDA_ERR_DEVICE_TIMEOUT, where);
     }
     ++phase;
@@ -145,43 +165,50 @@ __device__ __forceinline__ void publish_operands() {
     fence_after_sync();
 }
 
-// Stage chunk [t0, t0 + nrow) of this head into input buffer `buf` (zero rows past nrow).
-__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *buf, int t0, int nrow,
-                                            int h, int tid) {
-    const int H = p.H;
-    const __nv_bfloat16 *src[3] = {p.q, p.k, p.v};
-    const uint32_t dst[3] = {IB_Q, IB_K, IB_V};
+// Stage chunk [t0, t0 + 32) of this head into input buffer `buf`: one thread
+// issues the TMA boxes, threads 0..31 fetch beta (zero past nrow).  Rows past the
+// sequence end are not masked here: log_alpha and beta are masked where they are
+// used, which keeps those rows out of every product (see the kernel).
+constexpr int kTmaThread = 64;
+__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *buf, uint64_t *tbar,
+                                            int t0, int nrow, int h, int tid) {
+    if (tid == kTmaThread) {
+        fence_proxy_async_smem();  // earlier generic accesses to this buffer come first
+        mbar_arrive_expect_tx(tbar, kTmaBytes);
+        const CUtensorMap *maps[3] = {&p.tm_q, &p.tm_k, &p.tm_v};
+        const uint32_t dst[3] = {IB_Q, IB_K, IB_V};
 #pragma unroll
-    for (int m = 0; m < 6; ++m) {
-        const int e = tid + kThreads * m;  // 1536 chunks of 16 bytes
-        const int a = e >> 9, rem = e & 511;
-        const int i = rem >> 4, cc = rem & 15;
-        const bool ok = i < nrow;
-        const __nv_bfloat16 *s = ok ? src[a] + ((size_t)(t0 + i) * H + h) * kD + 8 * cc : src[a];
-        cp_async16(smem_u32(buf + dst[a] + tile_chunk(i, cc)), s, ok ? 16u : 0u);
-    }
+        for (int a = 0; a < 3; ++a)
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int e = tid + kThreads * m;  // 1024 chunks of 4 floats
-        const int i = e >> 5, qq = e & 31;
-        const bool ok = i < nrow;
-        const float *s = ok ? p.log_alpha + ((size_t)(t0 + i) * H + h) * kD + 4 * qq : p.log_alpha;
-        cp_async16(smem_u32(buf + IB_LA + i * 512 + qq * 16), s, ok ? 16u : 0u);
+            for (int b = 0; b < 2; ++b)
+                tma_load_2d(smem_u32(buf + dst[a] + 4096 * b), maps[a], h * kD + 64 * b, t0, tbar);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            tma_load_2d(smem_u32(buf + IB_LA + 4096 * b), &p.tm_la, h * kD + 32 * b, t0, tbar);
     }
     if (tid < kC) {
         const bool ok = tid < nrow;
-        const float *s = ok ? p.beta + (size_t)(t0 + tid) * H + h : p.beta;
+        const float *s = ok ? p.beta + (size_t)(t0 + tid) * p.H + h : p.beta;
         cp_async4(smem_u32(buf + IB_BETA + 4 * tid), s, ok ? 4u : 0u);
+        cp_async_commit();
     }
-    cp_async_commit();
 }
 
+// Algebra per chunk (log2 units, D_r = (gamma_r - gamma_15) log2 e, E = 2^D,
+// em = e^{gamma_15}, e31 = 2^{D_31}, so Gamma_r = em E_r and Gamma_C = em e31):
+//   Gram:  G = [k E ; q E] (k E^-1)^T  ->  A = beta_r G_k (i < r), P = G_q (i <= r)
+//   W = Tb (k Gamma) = (Tb (k E)) diag(em),   Q~ = (q E) diag(em),   U~ = Tb V
+//   K^ = (k E^-1) diag(e31)  =>  S_C = Diag(e31) [ Diag(em) S0 + (k E^-1)^T U ]
+// The state is kept in TMEM as X = S / e31 (per key channel), so the update is
+// X <- Diag(em) S0 + (k E^-1)^T U with the Gram's own R = k E^-1 tile as M5's
+// B operand, and S0 = Diag(e31_prev) X is formed once per chunk in the pass that
+// also builds M3's A operand.
 template <typename Tout>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float *vec = reinterpret_cast<float *>(sm + W_VEC);
+    float *vec = reinterpret_cast<float *>(sm + W_VEC);  // em[2][128] | e31[2][128]
     float *sA = reinterpret_cast<float *>(sm + W_A);
     float *sT = reinterpret_cast<float *>(sm + W_T);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + W_BAR);
@@ -199,11 +226,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
         tmem_alloc(tslot, 512);
         tmem_relinquish();
     }
-    if (tid == 0) {
+    uint64_t *tbar = bar + 2;  // TMA barriers, one per input buffer
+    if (tid == kTmaThread) {
         mbar_init(bar, 1);
+        mbar_init(bar + 1, 1);
+        mbar_init(tbar, 1);
+        mbar_init(tbar + 1, 1);
         fence_mbar_init();
     }
-    if (t_begin < t_end) issue_loads(p, sm, t_begin, min(kC, t_end - t_begin), h, tid);
+    if (tid < kD) vec[2 * kD + kD + tid] = 1.f;  // e31 of "chunk -1": the entering state is exact
+    __syncthreads();
+    if (t_begin < t_end) issue_loads(p, sm, tbar, t_begin, min(kC, t_end - t_begin), h, tid);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -230,132 +263,111 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
     int chunk = 0;
     for (int t0 = t_begin; t0 < t_end && alive; t0 += kC, ++chunk) {
         const int nrow = min(kC, t_end - t0);
-        unsigned char *buf = sm + (chunk & 1) * IB_SIZE;
+        const int par = chunk & 1;
+        unsigned char *buf = sm + par * IB_SIZE;
         const float *beta_s = reinterpret_cast<const float *>(buf + IB_BETA);
+        float *em = vec + par * kD;
+        float *e31 = vec + 2 * kD + par * kD;
+        const float *e31_prev = vec + 2 * kD + (par ^ 1) * kD;
 
         // ---- F1: this chunk's inputs have landed; stage the next chunk ----
-        cp_async_wait_all();
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
+        {
+            bool ok = true;
+            if (tid == kTmaThread) {
+                ok = mbar_wait_bounded(tbar + par, (uint32_t)(chunk >> 1) & 1u, kWaitNs);
+                if (!ok) record_status(p.status, KDA_ERR_DEVICE_TIMEOUT, 0);
+            }
+            if (tid < kC) cp_async_wait_all();
+            if (!__syncthreads_and(ok)) {
+                alive = false;
+                break;
+            }
+            fence_after_sync();
+        }
         if (t0 + kC < t_end)
-            issue_loads(p, sm + ((chunk + 1) & 1) * IB_SIZE, t0 + kC, min(kC, t_end - t0 - kC), h,
-                        tid);
+            issue_loads(p, sm + (par ^ 1) * IB_SIZE, tbar + (par ^ 1), t0 + kC,
+                        min(kC, t_end - t0 - kC), h, tid);
 
-        // ---- F2: decay factors in log2 units: D = (gamma - gamma_15) log2(e),
-        //      E = 2^D, E^-1 = 2^-D ----
+        // ---- F2: decay factors; threads c and c + 128 share key channel c ----
         {
             const int c = tid & 127;
             const float *la = reinterpret_cast<const float *>(buf + IB_LA);
             const float kL2E = 1.4426950408889634f;
             const uint32_t cq = (uint32_t)(c >> 2), cb = (uint32_t)((c & 3) << 2);
+            float pre[16];
             float acc = 0.f;
-            if (half == 0) {  // rows 15..0: D_r = -(sum of log alpha over rows r+1..15)
+            const int r0 = 16 * half;
 #pragma unroll
-                for (int r = 15; r >= 0; --r) {
-                    const uint32_t off = (uint32_t)(r * 512) + ((cq ^ (uint32_t)r) << 4) + cb;
-                    *reinterpret_cast<float *>(sm + W_E + off) = ex2_approx(-acc);
-                    *reinterpret_cast<float *>(sm + W_EI + off) = ex2_approx(acc);
-                    acc = fmaf(la[r * kD + c], kL2E, acc);
-                }
-                vec[V_M + c] = acc;  // gamma_15 log2(e)
-                vec[V_EM + c] = ex2_approx(acc);
-            } else {  // rows 16..31: D_r = sum of log alpha over rows 16..r
-#pragma unroll
-                for (int r = 16; r < 32; ++r) {
-                    acc = fmaf(la[r * kD + c], kL2E, acc);
-                    const uint32_t off = (uint32_t)(r * 512) + ((cq ^ (uint32_t)r) << 4) + cb;
-                    *reinterpret_cast<float *>(sm + W_E + off) = ex2_approx(acc);
-                    *reinterpret_cast<float *>(sm + W_EI + off) = ex2_approx(-acc);
-                }
-                vec[V_D31 + c] = acc;
-                vec[V_E31 + c] = ex2_approx(acc);
+            const float *lac = la + (c >> 5) * 1024 + (c & 31);  // box c/32, row stride 32
+            for (int r = 0; r < 16; ++r) {
+                const float x = (r0 + r) < nrow ? lac[(r0 + r) * 32] : 0.f;  // rows past the end
+                acc = fmaf(x, kL2E, acc);
+                pre[r] = acc;
             }
+            // rows 0..15: D = prefix - prefix_15;  rows 16..31: D = sum of rows 16..r
+            const float sub = half == 0 ? pre[15] : 0.f;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const float d = pre[r] - sub;
+                const uint32_t off =
+                    (uint32_t)((r0 + r) * 512) + ((cq ^ (uint32_t)(r0 + r)) << 4) + cb;
+                *reinterpret_cast<float *>(sm + W_E + off) = ex2_approx(d);
+                *reinterpret_cast<float *>(sm + W_EI + off) = ex2_approx(-d);
+            }
+            if (half == 0) em[c] = ex2_approx(pre[15]);
+            else e31[c] = ex2_approx(pre[15]);
         }
         __syncthreads();
 
-        // ---- F3: operands that do not depend on the state ----
-        if (tid < kD) vec[V_GC + tid] = ex2_approx(vec[V_M + tid] + vec[V_D31 + tid]);  // Gamma_C
-        if (trow < 64) {  // M1's A operand into TMEM: rows 0..31 k E, rows 32..63 q E
-            const int r = trow & 31;
-            const unsigned char *src = buf + (trow < 32 ? IB_K : IB_Q);
-            uint32_t hw[32], lw[32];
+        // ---- F3: [k E ; q E], R = k E^-1, Q~ = q E em (one 16-byte chunk per job) ----
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) {
-                const int cc = 8 * half + q8;
-                float x[8];
-                bf16x8_to_f32(*reinterpret_cast<const uint4 *>(src + tile_chunk(r, cc)), x);
-                const float4 e0 = *reinterpret_cast<const float4 *>(sm + W_E + e_chunk(r, 2 * cc));
-                const float4 e1 =
-                    *reinterpret_cast<const float4 *>(sm + W_E + e_chunk(r, 2 * cc + 1));
-                split2(x[0] * e0.x, x[1] * e0.y, hw[4 * q8 + 0], lw[4 * q8 + 0]);
-                split2(x[2] * e0.z, x[3] * e0.w, hw[4 * q8 + 1], lw[4 * q8 + 1]);
-                split2(x[4] * e1.x, x[5] * e1.y, hw[4 * q8 + 2], lw[4 * q8 + 2]);
-                split2(x[6] * e1.z, x[7] * e1.w, hw[4 * q8 + 3], lw[4 * q8 + 3]);
-            }
-            tmem_st32(tl + TM_OPG + 32 * half, hw);
-            tmem_st32(tl + TM_OPG + 64 + 32 * half, lw);
-        }
-        // 16-byte-chunk jobs: R = k E^-1 (M1 B), k Gamma (M2b B), K^ (M5 B), Q~ (M3 B rows 32..63)
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int job = m >> 1;
-            const int rem = tid + kThreads * (m & 1);
-            const int i = rem >> 4, cc = rem & 15;
-            float x[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(buf + (job == 3 ? IB_Q : IB_K) +
-                                                           tile_chunk(i, cc)),
-                          x);
-            const uint32_t fsrc = (job == 0 || job == 2) ? W_EI : W_E;
-            float4 f0 = *reinterpret_cast<const float4 *>(sm + fsrc + e_chunk(i, 2 * cc));
-            float4 f1 = *reinterpret_cast<const float4 *>(sm + fsrc + e_chunk(i, 2 * cc + 1));
-            if (job != 0) {  // channel factor: e^m (k Gamma, Q~) or E_31 (K^)
-                const float *cf = vec + (job == 2 ? V_E31 : V_EM) + 8 * cc;
-                const float4 c0 = *reinterpret_cast<const float4 *>(cf);
-                const float4 c1 = *reinterpret_cast<const float4 *>(cf + 4);
-                f0.x *= c0.x; f0.y *= c0.y; f0.z *= c0.z; f0.w *= c0.w;
-                f1.x *= c1.x; f1.y *= c1.y; f1.z *= c1.z; f1.w *= c1.w;
-            }
-            const float2 p0 = mul2(make_float2(x[0], x[1]), make_float2(f0.x, f0.y));
-            const float2 p1 = mul2(make_float2(x[2], x[3]), make_float2(f0.z, f0.w));
-            const float2 p2 = mul2(make_float2(x[4], x[5]), make_float2(f1.x, f1.y));
-            const float2 p3 = mul2(make_float2(x[6], x[7]), make_float2(f1.z, f1.w));
-            const float y[8] = {p0.x, p0.y, p1.x, p1.y, p2.x, p2.y, p3.x, p3.y};
-            unsigned char *hi;
-            uint32_t lo_off;
-            if (job == 0) {
-                hi = sm + W_R + tile_chunk(i, cc);
-                lo_off = 8192;
-            } else if (job == 1) {
-                hi = sm + W_KT + tile_chunk(i, cc);
-                lo_off = 8192;
-            } else if (job == 2) {
-                hi = sm + W_KH + tile_chunk(i, cc);
-                lo_off = 8192;
-            } else {
-                hi = sm + W_WQ + sw128_chunk_offset(64, 32 + i, cc);
-                lo_off = 16384;
-            }
-            store_split_chunk(hi, hi + lo_off, y);
+        for (int m = 0; m < 2; ++m) {
+            const int e = tid + kThreads * m;  // 512 jobs: row i, chunk cc
+            const int i = e >> 4, cc = e & 15;
+            float xk[8], xq[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(buf + IB_K + tile_chunk(32, i, cc)), xk);
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(buf + IB_Q + tile_chunk(32, i, cc)), xq);
+            const float4 e0 = *reinterpret_cast<const float4 *>(sm + W_E + e_chunk(i, 2 * cc));
+            const float4 e1 = *reinterpret_cast<const float4 *>(sm + W_E + e_chunk(i, 2 * cc + 1));
+            const float4 f0 = *reinterpret_cast<const float4 *>(sm + W_EI + e_chunk(i, 2 * cc));
+            const float4 f1 = *reinterpret_cast<const float4 *>(sm + W_EI + e_chunk(i, 2 * cc + 1));
+            const float4 m0 = *reinterpret_cast<const float4 *>(em + 8 * cc);
+            const float4 m1 = *reinterpret_cast<const float4 *>(em + 8 * cc + 4);
+            float r8[8] = {xk[0], xk[1], xk[2], xk[3], xk[4], xk[5], xk[6], xk[7]};
+            mul8(r8, f0, f1);   // k E^-1
+            mul8(xk, e0, e1);   // k E
+            mul8(xq, e0, e1);   // q E
+            unsigned char *xh = sm + W_X + tile_chunk(64, i, cc);
+            store_split_chunk(xh, xh + 16384, xk);
+            xh = sm + W_X + tile_chunk(64, 32 + i, cc);
+            store_split_chunk(xh, xh + 16384, xq);
+            unsigned char *rh = sm + W_R + tile_chunk(32, i, cc);
+            store_split_chunk(rh, rh + 8192, r8);
+            mul8(xq, m0, m1);   // Q~ = q E em
+            unsigned char *qh = sm + W_WQ + tile_chunk(64, 32 + i, cc);
+            store_split_chunk(qh, qh + 16384, xq);
         }
         publish_operands();
-        if (tid == 0) {  // M1: Gram
+        if (tid == kIssuerA || tid == kIssuerB) {  // M1: Gram, K steps split over two issuers
+            // A = [k E ; q E] (rows 64..127 of the view are ignored), B = R
             const uint32_t id = idesc_bf16_f32(128, 32);
+            const int s0 = tid == kIssuerA ? 0 : 4;
+            const uint32_t d = tb + (tid == kIssuerA ? TM_DG : TM_DU);
+            const uint32_t xh = smem_u32(sm + W_X), xl = xh + 16384;
             const uint32_t rh = smem_u32(sm + W_R), rl = rh + 8192;
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_bf16_tmem_a(tb + TM_D1, tb + TM_OPG + 8 * s, sw128_desc_k(rh, 32, s), id, s > 0);
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(d, sw128_desc_k(xh, 64, s0 + s), sw128_desc_k(rh, 32, s0 + s), id, s > 0);
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_bf16_tmem_a(tb + TM_D1, tb + TM_OPG + 8 * s, sw128_desc_k(rl, 32, s), id, 1);
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(d, sw128_desc_k(xh, 64, s0 + s), sw128_desc_k(rl, 32, s0 + s), id, 1);
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_bf16_tmem_a(tb + TM_D1, tb + TM_OPG + 64 + 8 * s, sw128_desc_k(rh, 32, s), id,
-                                1);
-            mma_commit(bar);
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(d, sw128_desc_k(xl, 64, s0 + s), sw128_desc_k(rh, 32, s0 + s), id, 1);
+            mma_commit(bar + (tid == kIssuerB));
         }
 
-        // ---- F4 (while M1 runs): S0^T -> M3's A operand; S^T *= Gamma_C along j ----
+        // ---- F4 (while M1 runs): S0 = e31_prev X -> M3's A operand; X <- em S0 ----
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             const int j0 = 64 * half + 32 * part;
@@ -363,12 +375,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
             tmem_ld32(tl + TM_ST + j0, sv);
             uint32_t hw[16], lw[16], sc[32];
 #pragma unroll
+            for (int jj = 0; jj < 32; jj += 4) {
+                const float4 g = *reinterpret_cast<const float4 *>(e31_prev + j0 + jj);
+                const float2 a = mul2(make_float2(sv[jj], sv[jj + 1]), make_float2(g.x, g.y));
+                const float2 b = mul2(make_float2(sv[jj + 2], sv[jj + 3]), make_float2(g.z, g.w));
+                sv[jj] = a.x; sv[jj + 1] = a.y; sv[jj + 2] = b.x; sv[jj + 3] = b.y;
+            }
+#pragma unroll
             for (int pp = 0; pp < 16; ++pp) split2(sv[2 * pp], sv[2 * pp + 1], hw[pp], lw[pp]);
 #pragma unroll
             for (int jj = 0; jj < 32; jj += 4) {
-                const float4 g4 = *reinterpret_cast<const float4 *>(vec + V_GC + j0 + jj);
-                const float2 a = mul2(make_float2(sv[jj], sv[jj + 1]), make_float2(g4.x, g4.y));
-                const float2 b = mul2(make_float2(sv[jj + 2], sv[jj + 3]), make_float2(g4.z, g4.w));
+                const float4 g = *reinterpret_cast<const float4 *>(em + j0 + jj);
+                const float2 a = mul2(make_float2(sv[jj], sv[jj + 1]), make_float2(g.x, g.y));
+                const float2 b = mul2(make_float2(sv[jj + 2], sv[jj + 3]), make_float2(g.z, g.w));
                 sc[jj] = __float_as_uint(a.x);
                 sc[jj + 1] = __float_as_uint(a.y);
                 sc[jj + 2] = __float_as_uint(b.x);
@@ -383,8 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
 
         // ---- F5: A (k rows, scaled by beta, strictly lower) and P (q rows, lower) ----
         if (trow < 64) {
-            float g[16];
-            tmem_ld16(tl + TM_D1 + 16 * half, g);
+            float g[16], g2[16];
+            tmem_ld16(tl + TM_DG + 16 * half, g);
+            tmem_ld16(tl + TM_DU + 16 * half, g2);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) g[e] += g2[e];
             if (trow < 32) {
                 const int r = trow;
                 const float br = beta_s[r];
@@ -403,9 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
                         const int i = 16 * half + 8 * c2 + e;
                         x[e] = i <= r ? g[8 * c2 + e] : 0.f;
                     }
-                    const int ch = 2 * half + c2;
-                    store_split_chunk(sm + W_R + 8192 + sw128_chunk_offset(32, r, ch),
-                                      sm + W_R + 12288 + sw128_chunk_offset(32, r, ch), x);
+                    unsigned char *ph = sm + W_P + sw128_chunk_offset(32, r, 2 * half + c2);
+                    store_split_chunk(ph, ph + 4096, x);
                 }
             }
         }
@@ -441,93 +462,105 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
             sT[(16 + r) * kLd + i] = -y;
         }
         __syncthreads();
-        if (tid < 128) {  // Tb -> M2's B operand and M2b's A operand (32 rows x 32 K)
-            const int r = tid >> 2, cc = tid & 3;
+        {  // Tb (32 rows x 32 K) written 4 times: rows 32 q + r, so W' lands in every lane quarter
+            const int r = tid >> 3, cc = tid & 3, copy2 = (tid >> 2) & 1;
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int i = 8 * cc + e;
                 x[e] = i <= r ? sT[r * kLd + i] * beta_s[i] : 0.f;
             }
-            store_split_chunk(sm + W_R + sw128_chunk_offset(32, r, cc),
-                              sm + W_R + 4096 + sw128_chunk_offset(32, r, cc), x);
+#pragma unroll
+            for (int cp = 0; cp < 2; ++cp) {
+                const int row = 32 * (2 * cp + copy2) + r;
+                unsigned char *th = sm + W_E + sw128_chunk_offset(128, row, cc);
+                store_split_chunk(th, th + 16384, x);
+            }
         }
         publish_operands();
-        if (tid == 0) {
-            const uint32_t th = smem_u32(sm + W_R), tlo = th + 4096;
-            // M2: U~^T = V^T Tb^T  (V exact in bf16, read MN-major from the staged tile)
+        if (tid == kIssuerA) {  // M2: U~^T = V^T Tb^T  (V exact in bf16, read MN-major)
+            const uint32_t th = smem_u32(sm + W_E), tlo = th + 16384;
             const uint32_t idv = idesc_bf16_f32(128, 32) | kIdescAMN;
             const uint32_t va = smem_u32(buf + IB_V);
 #pragma unroll
             for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_DW + 32, sw128_desc_mn(va + 2048 * s, 4096),
-                         sw128_desc_k(th, 32, s), idv, s > 0);
+                mma_bf16(tb + TM_DU, sw128_desc_mn(va + 2048 * s, 4096), sw128_desc_k(th, 128, s),
+                         idv, s > 0);
 #pragma unroll
             for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_DW + 32, sw128_desc_mn(va + 2048 * s, 4096),
-                         sw128_desc_k(tlo, 32, s), idv, 1);
-            // M2b: W = Tb (k Gamma): A = Tb (rows r; lanes >= 32 unused), B = (k Gamma) MN-major
+                mma_bf16(tb + TM_DU, sw128_desc_mn(va + 2048 * s, 4096), sw128_desc_k(tlo, 128, s),
+                         idv, 1);
+            mma_commit(bar);
+        } else if (tid == kIssuerB) {
+            // M2b: W' = Tb (k E): A = Tb x4 (128 rows), B = rows 0..31 of [k E ; q E] MN-major
+            const uint32_t th = smem_u32(sm + W_E), tlo = th + 16384;
             const uint32_t idw = idesc_bf16_f32(128, 128) | kIdescBMN;
-            const uint32_t kh = smem_u32(sm + W_KT), kl = kh + 8192;
+            const uint32_t xh = smem_u32(sm + W_X), xl = xh + 16384;
 #pragma unroll
             for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_OPG, sw128_desc_k(th, 128, s), sw128_desc_mn(kh + 2048 * s, 4096),
+                mma_bf16(tb + TM_WT, sw128_desc_k(th, 128, s), sw128_desc_mn(xh + 2048 * s, 8192),
                          idw, s > 0);
 #pragma unroll
             for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_OPG, sw128_desc_k(th, 128, s), sw128_desc_mn(kl + 2048 * s, 4096),
+                mma_bf16(tb + TM_WT, sw128_desc_k(th, 128, s), sw128_desc_mn(xl + 2048 * s, 8192),
                          idw, 1);
 #pragma unroll
             for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_OPG, sw128_desc_k(tlo, 128, s), sw128_desc_mn(kh + 2048 * s, 4096),
+                mma_bf16(tb + TM_WT, sw128_desc_k(tlo, 128, s), sw128_desc_mn(xh + 2048 * s, 8192),
                          idw, 1);
-            mma_commit(bar);
+            mma_commit(bar + 1);
         }
         alive = wait_mma(bar, phase, p.status, 2);
         if (!alive) break;
 
-        // ---- F7: W rows (TMEM lanes 0..31) -> rows 0..31 of M3's B operand ----
-        if (quarter == 0) {
+        // ---- F7: W = W' diag(em) -> rows 0..31 of M3's B operand (all 8 warps) ----
+        {
             const int r = lane;
+            const int c0 = 16 * (2 * quarter + half);
+            float w[16];
+            tmem_ld16(tl + TM_WT + c0, w);
 #pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                const int j0 = 64 * half + 32 * part;
-                float w[32];
-                tmem_ld32(tl + TM_OPG + j0, w);
-#pragma unroll
-                for (int q8 = 0; q8 < 4; ++q8) {
-                    const float x[8] = {w[8 * q8], w[8 * q8 + 1], w[8 * q8 + 2], w[8 * q8 + 3],
-                                        w[8 * q8 + 4], w[8 * q8 + 5], w[8 * q8 + 6], w[8 * q8 + 7]};
-                    const int cc = (j0 >> 3) + q8;
-                    unsigned char *hi = sm + W_WQ + sw128_chunk_offset(64, r, cc);
-                    store_split_chunk(hi, hi + 16384, x);
-                }
+            for (int h8 = 0; h8 < 2; ++h8) {
+                float x[8] = {w[8 * h8], w[8 * h8 + 1], w[8 * h8 + 2], w[8 * h8 + 3],
+                              w[8 * h8 + 4], w[8 * h8 + 5], w[8 * h8 + 6], w[8 * h8 + 7]};
+                const float4 m0 = *reinterpret_cast<const float4 *>(em + c0 + 8 * h8);
+                const float4 m1 = *reinterpret_cast<const float4 *>(em + c0 + 8 * h8 + 4);
+                mul8(x, m0, m1);
+                unsigned char *wh = sm + W_WQ + tile_chunk(64, r, (c0 >> 3) + h8);
+                store_split_chunk(wh, wh + 16384, x);
             }
         }
         publish_operands();
-        if (tid == 0) {  // M3: [(W S0)^T | (Q~ S0)^T] = S0^T [W ; Q~]^T
+        if (tid == kIssuerA || tid == kIssuerB) {
+            // M3: [(W S0)^T | (Q~ S0)^T] = S0^T [W ; Q~]^T, K steps 0-3 -> D1, 4-7 -> WT
             const uint32_t id = idesc_bf16_f32(128, 64);
+            const int s0 = tid == kIssuerA ? 0 : 4;
+            const uint32_t d = tb + (tid == kIssuerA ? TM_D1 : TM_WT);
             const uint32_t bh = smem_u32(sm + W_WQ), bl = bh + 16384;
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_bf16_tmem_a(tb + TM_D1, tb + TM_OPS + 8 * s, sw128_desc_k(bh, 64, s), id, s > 0);
+            for (int s = 0; s < 4; ++s)
+                mma_bf16_tmem_a(d, tb + TM_OPS + 8 * (s0 + s), sw128_desc_k(bh, 64, s0 + s), id,
+                                s > 0);
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_bf16_tmem_a(tb + TM_D1, tb + TM_OPS + 8 * s, sw128_desc_k(bl, 64, s), id, 1);
+            for (int s = 0; s < 4; ++s)
+                mma_bf16_tmem_a(d, tb + TM_OPS + 8 * (s0 + s), sw128_desc_k(bl, 64, s0 + s), id, 1);
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-                mma_bf16_tmem_a(tb + TM_D1, tb + TM_OPS + 64 + 8 * s, sw128_desc_k(bh, 64, s), id,
+            for (int s = 0; s < 4; ++s)
+                mma_bf16_tmem_a(d, tb + TM_OPS + 64 + 8 * (s0 + s), sw128_desc_k(bh, 64, s0 + s), id,
                                 1);
-            mma_commit(bar);
+            mma_commit(bar + (tid == kIssuerB));
         }
         alive = wait_mma(bar, phase, p.status, 3);
         if (!alive) break;
 
         // ---- F8: U^T = U~^T - (W S0)^T -> A operand of M4 / M5 ----
         {
-            float ut[16], ws[16];
-            tmem_ld16(tl + TM_DW + 32 + 16 * half, ut);
+            float ut[16], ws[16], ws2[16];
+            tmem_ld16(tl + TM_DU + 16 * half, ut);
             tmem_ld16(tl + TM_D1 + 16 * half, ws);
+            tmem_ld16(tl + TM_WT + 16 * half, ws2);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ws[e] += ws2[e];
             uint32_t hw[8], lw[8];
 #pragma unroll
             for (int pp = 0; pp < 8; ++pp)
@@ -536,12 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
             tmem_st8u(tl + TM_OPS + 16 + 8 * half, lw);
         }
         publish_operands();
-        if (tid == 0) {
+        if (tid == kIssuerA) {  // M4: (Q~ S0 + P U)^T += U^T P^T
             const uint32_t id32 = idesc_bf16_f32(128, 32);
-            const uint32_t id128 = idesc_bf16_f32(128, 128) | kIdescBMN;
-            const uint32_t ph = smem_u32(sm + W_R + 8192), pl = ph + 4096;
-            const uint32_t kh = smem_u32(sm + W_KH), kl = kh + 8192;
-            // M4: (Q~ S0 + P U)^T += U^T P^T
+            const uint32_t ph = smem_u32(sm + W_P), pl = ph + 4096;
 #pragma unroll
             for (int s = 0; s < 2; ++s)
                 mma_bf16_tmem_a(tb + TM_D1 + 32, tb + TM_OPS + 8 * s, sw128_desc_k(ph, 32, s), id32,
@@ -554,20 +584,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
             for (int s = 0; s < 2; ++s)
                 mma_bf16_tmem_a(tb + TM_D1 + 32, tb + TM_OPS + 16 + 8 * s, sw128_desc_k(ph, 32, s),
                                 id32, 1);
-            // M5: S^T += U^T K^
+            mma_commit(bar);
+        } else if (tid == kIssuerB) {  // M5: X += U^T (k E^-1)  (the Gram's R tile, read MN-major)
+            const uint32_t id128 = idesc_bf16_f32(128, 128) | kIdescBMN;
+            const uint32_t rh = smem_u32(sm + W_R), rl = rh + 8192;
 #pragma unroll
             for (int s = 0; s < 2; ++s)
-                mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 8 * s, sw128_desc_mn(kh + 2048 * s, 4096),
+                mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 8 * s, sw128_desc_mn(rh + 2048 * s, 4096),
                                 id128, 1);
 #pragma unroll
             for (int s = 0; s < 2; ++s)
-                mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 8 * s, sw128_desc_mn(kl + 2048 * s, 4096),
+                mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 8 * s, sw128_desc_mn(rl + 2048 * s, 4096),
                                 id128, 1);
 #pragma unroll
             for (int s = 0; s < 2; ++s)
                 mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 16 + 8 * s,
-                                sw128_desc_mn(kh + 2048 * s, 4096), id128, 1);
-            mma_commit(bar);
+                                sw128_desc_mn(rh + 2048 * s, 4096), id128, 1);
+            mma_commit(bar + 1);
         }
         alive = wait_mma(bar, phase, p.status, 4);
         if (!alive) break;
@@ -575,8 +608,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
         // ---- F9: readout o[r][c] = scale (Q~ S0 + P U)^T[c][r] ----
         {
             const int c = trow;
-            float ov[16];
+            float ov[16], ov2[16];
             tmem_ld16(tl + TM_D1 + 32 + 16 * half, ov);
+            tmem_ld16(tl + TM_WT + 32 + 16 * half, ov2);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] += ov2[e];
             Tout *o = static_cast<Tout *>(p.o);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -591,9 +627,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
     }
 
     cp_async_wait_all();  // nothing may still be in flight into shared memory on exit
-    // ---- final state (lane c, column j) -> S_final[j][c] ----
+    if (tid == kTmaThread && !alive) {  // let an outstanding TMA load land before leaving
+        // loads were issued for chunks 0 .. n_issued-1; chunks 0 .. chunk-1 were consumed
+        const int n_issued = (t_end - t_begin + kC - 1) / kC < chunk + 2
+                                 ? (t_end - t_begin + kC - 1) / kC
+                                 : chunk + 2;
+        for (int c = chunk; c < n_issued; ++c)
+            mbar_wait_bounded(tbar + (c & 1), (uint32_t)(c >> 1) & 1u, kWaitNs);
+    }
+    // ---- final state S = Diag(e31_last) X (lane c, column j) -> S_final[j][c] ----
     if (alive && p.S_final != nullptr) {
         const int c = trow;
+        const float *e31_last = vec + 2 * kD + ((chunk - 1) & 1) * kD;  // chunk 0 -> slot 1 = 1
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
             const int j0 = 64 * half + 32 * part;
@@ -601,12 +646,39 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(Params p) {
             tmem_ld32(tl + TM_ST + j0, sv);
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj)
-                p.S_final[state_off + (size_t)(j0 + jj) * kD + c] = sv[jj];
+                p.S_final[state_off + (size_t)(j0 + jj) * kD + c] = sv[jj] * e31_last[j0 + jj];
         }
     }
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// [T][H*128] tensor, boxes of 32 tokens x box_cols elements.
+bool encode_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem_bytes, int T,
+                int H, int box_cols, CUtensorMapSwizzle swz) {
+    auto fn = tensor_map_encoder();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)H * kD, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * kD * elem_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kC};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <typename Tout>
@@ -615,6 +687,19 @@ cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM_DYN);
     if (e != cudaSuccess) return e;
     Params p;
+    memset(&p, 0, sizeof(p));
+    if (a.total_tokens > 0) {
+        const int T = a.total_tokens, H = a.num_heads;
+        if (!encode_map(&p.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, 64,
+                        CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_map(&p.tm_la, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T, H, 32,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
     p.k = static_cast<const __nv_bfloat16 *>(a.k);
     p.v = static_cast<const __nv_bfloat16 *>(a.v);
