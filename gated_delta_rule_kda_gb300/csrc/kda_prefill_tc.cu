@@ -259,8 +259,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tmem_wait_st();
     }
 
+    // Readout of a finished chunk: o[t0 + r][c] = scale (Q~ S0 + P U)^T[c][r], the two K
+    // halves of M3 summed.  Done by warps 4..7 (one per lane quarter): the tile is staged
+    // row-major in the (dead) E^-1 table, then written out as 16-byte row chunks.
+    Tout *o = static_cast<Tout *>(p.o);
+    auto readout = [&](int t0r, int nrowr) {
+        Tout *ot = reinterpret_cast<Tout *>(sm + W_EI);  // [32][128]
+        const int c = trow;
+#pragma unroll
+        for (int r0 = 0; r0 < 32; r0 += 16) {
+            float ov[16], ov2[16];
+            tmem_ld16(tl + TM_D1 + 32 + r0, ov);
+            tmem_ld16(tl + TM_WT + 32 + r0, ov2);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                Elem<Tout>::store(ot + (r0 + e) * kD + c, p.scale * (ov[e] + ov2[e]));
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 4..7 only
+        constexpr int kPerRow = kD * (int)sizeof(Tout) / 16;  // 16-byte chunks per row
+        const int lt = tid - 128;
+        for (int e = lt; e < kC * kPerRow; e += 128) {
+            const int r = e / kPerRow, ch = e % kPerRow;
+            if (r < nrowr)
+                *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(
+                    o + ((size_t)(t0r + r) * H + h) * kD) + 16 * ch) =
+                    *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned char *>(ot) +
+                                                     r * kD * sizeof(Tout) + 16 * ch);
+        }
+    };
+
     bool alive = true;
-    int chunk = 0;
+    int chunk = 0, t0_prev = 0, nrow_prev = 0;
     for (int t0 = t_begin; t0 < t_end && alive; t0 += kC, ++chunk) {
         const int nrow = min(kC, t_end - t0);
         const int par = chunk & 1;
@@ -432,7 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         __syncthreads();
 
-        // ---- F6: T = (I + A)^-1 on 2 x 2 tiles of 16, then Tb = T diag(beta) ----
+        // ---- F6: T = (I + A)^-1 on 2 x 2 tiles of 16, then Tb = T diag(beta); while warp 0
+        //      solves the diagonal tiles, warps 4..7 read out the previous chunk ----
+        if (half == 1 && chunk > 0) readout(t0_prev, nrow_prev);
         if (tid < 32) {  // diagonal tiles, one column per thread
             const int blk = tid >> 4, jj = tid & 15;
             float x[16];
@@ -605,27 +636,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         alive = wait_mma(bar, phase, p.status, 4);
         if (!alive) break;
 
-        // ---- F9: readout o[r][c] = scale (Q~ S0 + P U)^T[c][r] ----
-        {
-            const int c = trow;
-            float ov[16], ov2[16];
-            tmem_ld16(tl + TM_D1 + 32 + 16 * half, ov);
-            tmem_ld16(tl + TM_WT + 32 + 16 * half, ov2);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) ov[e] += ov2[e];
-            Tout *o = static_cast<Tout *>(p.o);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int r = 16 * half + e;
-                if (r < nrow)
-                    Elem<Tout>::store(o + ((size_t)(t0 + r) * H + h) * kD + c, p.scale * ov[e]);
-            }
-        }
-        fence_before_sync();
-        __syncthreads();
-        fence_after_sync();
+        t0_prev = t0;
+        nrow_prev = nrow;  // read out during the next chunk's solve (or after the loop)
     }
 
+    if (alive && chunk > 0 && half == 1) readout(t0_prev, nrow_prev);  // the last chunk
     cp_async_wait_all();  // nothing may still be in flight into shared memory on exit
     if (tid == kTmaThread && !alive) {  // let an outstanding TMA load land before leaving
         // loads were issued for chunks 0 .. n_issued-1; chunks 0 .. chunk-1 were consumed
