@@ -53,7 +53,7 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -70,7 +70,7 @@ class ClockSampler:
         self.f = open(self.path, "w")
         self.proc = subprocess.Popen(
             ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
-             "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+             "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
             stderr=subprocess.DEVNULL)
 
     def stop(self):
@@ -285,18 +285,41 @@ def run_ours(args, world, rank, local):
     del dinp, od
     torch.cuda.empty_cache()
 
+    # ---------------- fused layer core (varlen, 16 sequences) ----------------
+    layer = None
+    if not args.skip_layer_core:
+        linp = synthetic.workload(5, device=dev)
+        LT = linp.qp.shape[0]
+        ws = torch.empty(kda.kda_layer_core_workspace_size(16, LT, 96), dtype=torch.uint8,
+                         device=dev)
+        og = torch.empty((LT, 96, D), dtype=torch.bfloat16, device=dev)
+        Sl = torch.empty((16, 96, D, D), dtype=torch.float32, device=dev)
+
+        def layer_step():
+            kda.kda_layer_core(linp.qp, linp.kp, linp.vp, linp.conv_w, linp.z, linp.A, linp.b,
+                               linp.beta_logit, linp.g, linp.cu_seqlens, None, o=og, S_final=Sl,
+                               workspace=ws)
+
+        l_steps = max(1, min(args.steps, 5))
+        l_total, _ = time_launches(layer_step, l_steps, args.warmup, world)
+        l_ms = max_over_ranks(l_total / l_steps, world)
+        layer = {"tokens_per_s": world * LT / (l_ms / 1e3), "ms_per_step": l_ms,
+                 "tokens": LT, "workload": "16 sequences, lengths log-uniform in [1K, 64K], "
+                                           "96 heads, front end + recurrence + gate",
+                 "launches_per_step": 3}
+        del linp, ws, og, Sl
+        torch.cuda.empty_cache()
+
     # ---------------- CPU baseline: the oracle on a bounded sample ----------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from gated_delta_rule_kda_gb300 import synthetic as syn
-        H_sample, T_sample = 32, 2048
-        cinp = syn.prefill_inputs([T_sample], H_sample, torch.bfloat16,
-                                  seed=syn.BASE_SEED + 2, device="cpu")
-        dt, head_tokens, cores = cpu_baseline_prefill(cinp, list(range(H_sample)), T_sample)
+        cinp = syn.workload(2, device="cpu")
+        dt, head_tokens, cores = cpu_baseline_prefill(cinp, list(range(96)), 8192)
         cpu = {"value": head_tokens / dt / 96.0, "unit": UNIT, "cores": cores,
                "kind": "oracle",
-               "sample": f"{H_sample} heads x {T_sample} tokens of the prefill workload, "
-                         f"{dt:.1f} s, scaled to 96-head tokens"}
+               "sample": f"the whole prefill workload (96 heads x 8192 tokens), {dt:.1f} s wall "
+                         f"on {cores} threads"}
 
     if rank == 0:
         line = {
@@ -305,6 +328,7 @@ def run_ours(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
+            "layer_core": layer,
             "clocks": clk, "gpu_launches": args.steps,
             "kernel_ms_mean": launch_ms,
         }
@@ -340,10 +364,11 @@ def run_only(args, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-layer-core", action="store_true")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="profiling aid: run just this kernel (no baseline, no e2e)")
     ap.add_argument("--small", action="store_true",

@@ -169,6 +169,56 @@ kda_status kda_output_gate(int64_t num_rows, kda_dtype in_dtype, const void *o_t
     return from_cuda(launch_output_gate(a, static_cast<cudaStream_t>(stream)));
 }
 
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t kda_layer_core_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t num_heads) {
+    (void)num_seqs;
+    if (total_tokens < 0 || num_heads < 1) return 0;
+    const size_t rows = (size_t)total_tokens * num_heads;
+    return 3 * align256(rows * kD * 2)    /* q^, k^, v bf16 */
+           + align256(rows * kD * 4)      /* log_alpha fp32 */
+           + align256(rows * 4)           /* beta fp32 */
+           + align256(rows * kD * 4)      /* o~ fp32 */
+           + kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, KDA_BF16);
+}
+
+kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                          const void *qp, const void *kp, const void *vp, const float *conv_w,
+                          const void *z, const float *A, const float *b, const void *beta_logit,
+                          const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
+                          float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
+                          float *S_final, void *workspace, size_t workspace_bytes, void *stream) {
+    if (!ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (total_tokens > 0 && (!ok_ptr(g) || !ok_ptr(o_gated))) return KDA_ERR_INVALID_ARGUMENT;
+    const size_t need = kda_layer_core_workspace_size(num_seqs, total_tokens, num_heads);
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+        return KDA_ERR_WORKSPACE;
+    const size_t rows = (size_t)total_tokens * num_heads;
+    unsigned char *w = static_cast<unsigned char *>(workspace);
+    void *q_hat = w;
+    void *k_hat = w + align256(rows * kD * 2);
+    void *v_out = w + 2 * align256(rows * kD * 2);
+    float *log_alpha = reinterpret_cast<float *>(w + 3 * align256(rows * kD * 2));
+    float *beta = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(log_alpha) +
+                                            align256(rows * kD * 4));
+    float *o_tilde = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(beta) +
+                                               align256(rows * 4));
+    void *pre_ws = reinterpret_cast<unsigned char *>(o_tilde) + align256(rows * kD * 4);
+    const size_t pre_ws_bytes = kda_prefill_workspace_size(num_seqs, total_tokens, num_heads,
+                                                           KDA_BF16);
+    kda_status st = kda_frontend(num_seqs, total_tokens, num_heads, qp, kp, vp, conv_w, z, A, b,
+                                 beta_logit, cu_seqlens, l2_eps, KDA_BF16, q_hat, k_hat, v_out,
+                                 log_alpha, beta, stream);
+    if (st != KDA_OK) return st;
+    st = kda_prefill(KDA_BF16, KDA_FP32, num_seqs, total_tokens, num_heads, q_hat, k_hat, v_out,
+                     log_alpha, beta, S0, cu_seqlens, scale, o_tilde, S_final, pre_ws,
+                     pre_ws_bytes, stream);
+    if (st != KDA_OK) return st;
+    return kda_output_gate((int64_t)rows, KDA_FP32, o_tilde, g, rms_eps, out_dtype, o_gated,
+                           stream);
+}
+
 kda_status kda_get_device_status(void *stream, uint32_t *detail) {
     if (detail) *detail = 0;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)

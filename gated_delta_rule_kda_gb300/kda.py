@@ -42,6 +42,8 @@ EXPORTED = (
     "kda_decode_step",
     "kda_frontend",
     "kda_output_gate",
+    "kda_layer_core_workspace_size",
+    "kda_layer_core",
     "kda_get_device_status",
 )
 
@@ -76,6 +78,11 @@ def _load() -> ctypes.CDLL:
     lib.kda_frontend.restype = ctypes.c_int
     lib.kda_output_gate.argtypes = [I64, ctypes.c_int, P, P, F, ctypes.c_int, P, P]
     lib.kda_output_gate.restype = ctypes.c_int
+    lib.kda_layer_core_workspace_size.argtypes = [I32, I32, I32]
+    lib.kda_layer_core_workspace_size.restype = SZ
+    lib.kda_layer_core.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, F, F, F,
+                                   ctypes.c_int, P, P, P, SZ, P]
+    lib.kda_layer_core.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.kda_get_device_status.restype = ctypes.c_int
     return lib
@@ -196,6 +203,32 @@ def kda_output_gate(o_tilde, g, eps=1e-6, *, out_dtype=torch.bfloat16, out=None,
                               _dtype_code(out.dtype), _p(out), _stream(stream))
     _check("kda_output_gate", rc)
     return out
+
+
+def kda_layer_core_workspace_size(num_seqs: int, total_tokens: int, num_heads: int) -> int:
+    return int(_lib.kda_layer_core_workspace_size(num_seqs, total_tokens, num_heads))
+
+
+def kda_layer_core(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=None,
+                   scale=DEFAULT_SCALE, l2_eps=1e-6, rms_eps=1e-6, *, out_dtype=torch.bfloat16,
+                   o=None, S_final=None, want_state=True, workspace=None, stream=None):
+    """Front end -> recurrence -> output gate.  Returns (o_gated, S_final or None)."""
+    T, H, _ = qp.shape
+    N = cu_seqlens.shape[0] - 1
+    if o is None:
+        o = torch.empty((T, H, HEAD_DIM), dtype=out_dtype, device=qp.device)
+    if S_final is None and want_state:
+        S_final = torch.empty((N, H, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=qp.device)
+    need = kda_layer_core_workspace_size(N, T, H)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=qp.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = _lib.kda_layer_core(N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A), _p(b),
+                             _p(beta_logit), _p(g), _p(cu_seqlens), _p(S0), float(scale),
+                             float(l2_eps), float(rms_eps), _dtype_code(o.dtype), _p(o),
+                             _p(S_final), _p(workspace), wbytes, _stream(stream))
+    _check("kda_layer_core", rc)
+    return o, S_final
 
 
 def kda_get_device_status(stream=None):

@@ -178,6 +178,35 @@ kda_status kda_output_gate(int64_t num_rows, kda_dtype in_dtype, const void *o_t
                            void *stream);
 
 /*
+ * Bytes of device scratch kda_layer_core needs for these sizes.
+ */
+size_t kda_layer_core_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t num_heads);
+
+/*
+ * kda_layer_core - one KDA layer core over packed variable-length sequences:
+ * front end, recurrence and output gate ("Kimi K3 · KDA layer", KDA equation
+ * list), i.e. kda_frontend -> kda_prefill -> kda_output_gate on `stream`.
+ *
+ * The front end hands q^, k^ and v to the recurrence in bf16 (the kernel
+ * interface the pages describe takes BF16 query/key/value: "Inside Kimi K3:
+ * How KDA, AttnRes, and 896 Experts Work", section "The lower bound on decay
+ * is a hardware decision"); log_alpha and beta stay fp32 and o~ stays fp32
+ * until the gate.  These intermediates live in `workspace`, which must hold
+ * kda_layer_core_workspace_size() bytes; nothing is allocated.
+ *
+ *   qp, kp, vp, z [T][H][128] bf16; conv_w [3][H*128][4] fp32; A [H] fp32;
+ *   b [H][128] fp32 or NULL; beta_logit [T][H] bf16; g [T][H][128] bf16;
+ *   cu_seqlens [N+1] int32 (device); S0 [N][H][128][128] fp32 or NULL;
+ *   o_gated [T][H][128] out_dtype; S_final [N][H][128][128] fp32 or NULL.
+ */
+kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                          const void *qp, const void *kp, const void *vp, const float *conv_w,
+                          const void *z, const float *A, const float *b, const void *beta_logit,
+                          const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
+                          float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
+                          float *S_final, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * kda_get_device_status - synchronises `stream`, then returns and clears the
  * device status word: KDA_OK, KDA_ERR_DEVICE_TIMEOUT or KDA_ERR_DEVICE_CHECK
  * (KDA_ERR_CUDA if the synchronisation itself fails).  If detail is not

@@ -105,3 +105,14 @@ def test_frontend_and_gate_reject_bad_arguments(kda):
 
 def test_workspace_size_is_callable(kda):
     assert kda.kda_prefill_workspace_size(1, 8192, 96) >= 0
+
+
+def test_layer_core_rejects_missing_workspace(kda):
+    lib = kda.library()
+    rc = lib.kda_layer_core(1, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE,
+                            None, 0.1, 1e-6, 1e-6, 0, FAKE, None, None, 0, None)
+    assert rc == 3  # KDA_ERR_WORKSPACE
+    rc = lib.kda_layer_core(1, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE,
+                            None, 0.1, 1e-6, 1e-6, 0, FAKE, None, FAKE, 1 << 20, None)
+    assert rc == 1  # g missing
+    assert kda.kda_layer_core_workspace_size(16, 1000, 96) > 1000 * 96 * 128 * 2 * 3
