@@ -175,11 +175,11 @@ size_t kda_layer_core_workspace_size(int32_t num_seqs, int32_t total_tokens, int
     (void)num_seqs;
     if (total_tokens < 0 || num_heads < 1) return 0;
     const size_t rows = (size_t)total_tokens * num_heads;
-    return 3 * align256(rows * kD * 2)    /* q^, k^, v bf16 */
+    return 3 * align256(rows * kD * 4)    /* q^, k^, v fp32 */
            + align256(rows * kD * 4)      /* log_alpha fp32 */
            + align256(rows * 4)           /* beta fp32 */
            + align256(rows * kD * 4)      /* o~ fp32 */
-           + kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, KDA_BF16);
+           + kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, KDA_FP32);
 }
 
 kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
@@ -197,21 +197,21 @@ kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_he
     const size_t rows = (size_t)total_tokens * num_heads;
     unsigned char *w = static_cast<unsigned char *>(workspace);
     void *q_hat = w;
-    void *k_hat = w + align256(rows * kD * 2);
-    void *v_out = w + 2 * align256(rows * kD * 2);
-    float *log_alpha = reinterpret_cast<float *>(w + 3 * align256(rows * kD * 2));
+    void *k_hat = w + align256(rows * kD * 4);
+    void *v_out = w + 2 * align256(rows * kD * 4);
+    float *log_alpha = reinterpret_cast<float *>(w + 3 * align256(rows * kD * 4));
     float *beta = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(log_alpha) +
                                             align256(rows * kD * 4));
     float *o_tilde = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(beta) +
                                                align256(rows * 4));
     void *pre_ws = reinterpret_cast<unsigned char *>(o_tilde) + align256(rows * kD * 4);
     const size_t pre_ws_bytes = kda_prefill_workspace_size(num_seqs, total_tokens, num_heads,
-                                                           KDA_BF16);
+                                                           KDA_FP32);
     kda_status st = kda_frontend(num_seqs, total_tokens, num_heads, qp, kp, vp, conv_w, z, A, b,
-                                 beta_logit, cu_seqlens, l2_eps, KDA_BF16, q_hat, k_hat, v_out,
+                                 beta_logit, cu_seqlens, l2_eps, KDA_FP32, q_hat, k_hat, v_out,
                                  log_alpha, beta, stream);
     if (st != KDA_OK) return st;
-    st = kda_prefill(KDA_BF16, KDA_FP32, num_seqs, total_tokens, num_heads, q_hat, k_hat, v_out,
+    st = kda_prefill(KDA_FP32, KDA_FP32, num_seqs, total_tokens, num_heads, q_hat, k_hat, v_out,
                      log_alpha, beta, S0, cu_seqlens, scale, o_tilde, S_final, pre_ws,
                      pre_ws_bytes, stream);
     if (st != KDA_OK) return st;

@@ -187,11 +187,11 @@ size_t kda_layer_core_workspace_size(int32_t num_seqs, int32_t total_tokens, int
  * front end, recurrence and output gate ("Kimi K3 · KDA layer", KDA equation
  * list), i.e. kda_frontend -> kda_prefill -> kda_output_gate on `stream`.
  *
- * The front end hands q^, k^ and v to the recurrence in bf16 (the kernel
- * interface the pages describe takes BF16 query/key/value: "Inside Kimi K3:
- * How KDA, AttnRes, and 896 Experts Work", section "The lower bound on decay
- * is a hardware decision"); log_alpha and beta stay fp32 and o~ stays fp32
- * until the gate.  These intermediates live in `workspace`, which must hold
+ * All intermediates (q^, k^, v, log_alpha, beta, o~) stay fp32: with the
+ * front end's short-convolution smoothing, consecutive keys are close to
+ * parallel and the recurrence is ill-conditioned, so rounding q^, k^, v to
+ * bf16 between the stages moves the output by several percent.  The
+ * intermediates live in `workspace`, which must hold
  * kda_layer_core_workspace_size() bytes; nothing is allocated.
  *
  *   qp, kp, vp, z [T][H][128] bf16; conv_w [3][H*128][4] fp32; A [H] fp32;

@@ -1,9 +1,15 @@
 """GPU layer core (front end -> recurrence -> output gate) vs the fp64 oracle.
 
-The library hands q^, k^, v from the front end to the recurrence in bf16 (the
-kernel interface the pages describe takes bf16 q/k/v).  The oracle composition
-below rounds at the same point (torch's bf16 rounding of the oracle's own fp64
-front-end outputs); every other step is fp64.
+The library keeps every intermediate of the layer in fp32, and the oracle is
+the plain fp64 composition.  (Rounding q^, k^, v to bf16 between the stages
+moves the output of these inputs by ~10%: the conv-smoothed keys are close to
+parallel and the recurrence is ill-conditioned.)
+
+Tolerance of the gated output.  RMSNorm divides each (token, head) row by its
+own RMS, so an error that is 2e-3 of the tensor-wide RMS of o~ becomes
+2e-3 * rms(o~) / rms_row(o~) of that row after the gate.  The check therefore
+scales the bound per row by max(1, rms(o~) / rms_row(o~)) (o~ from the oracle);
+S_final keeps the plain 2e-3 bound.
 """
 import numpy as np
 import pytest
@@ -11,7 +17,7 @@ import torch
 
 import oracle
 from gated_delta_rule_kda_gb300 import synthetic
-from tests._parity import TOL_BF16, assert_close, to64
+from tests._parity import TOL_BF16, TOL_FP32, assert_close, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -20,10 +26,6 @@ pytestmark = pytest.mark.gpu
 def kda():
     from gated_delta_rule_kda_gb300 import kda as mod
     return mod
-
-
-def bf16_round(x):
-    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
 
 
 def oracle_layer_core(inp, heads=None):
@@ -37,9 +39,23 @@ def oracle_layer_core(inp, heads=None):
                                                to64(inp.A)[hs], to64(inp.b)[hs],
                                                to64(sel(inp.beta_logit)), cu)
     S0 = None if inp.S0 is None else to64(inp.S0)[:, hs]
-    ot, Sf = oracle.kda_prefill(bf16_round(qh), bf16_round(kh), bf16_round(vv), la, beta, cu,
-                                S0=S0)
-    return oracle.kda_output_gate(ot, to64(sel(inp.g))), Sf
+    ot, Sf = oracle.kda_prefill(qh, kh, vv, la, beta, cu, S0=S0)
+    return oracle.kda_output_gate(ot, to64(sel(inp.g))), Sf, ot
+
+
+def assert_gated_close(gpu, ref, ot_ref, out_is_bf16):
+    """|gpu - ref| <= TOL * rms(ref) * cond_row (+ bf16 half-ulp), cond_row as in the docstring."""
+    gpu = np.asarray(gpu, np.float64)
+    assert np.isfinite(gpu).all(), "o_gated: non-finite values"
+    rms_all = np.sqrt(np.mean(ot_ref ** 2))
+    rms_row = np.sqrt(np.mean(ot_ref ** 2, axis=-1, keepdims=True))
+    cond = np.maximum(1.0, rms_all / np.maximum(rms_row, 1e-300))
+    diff = np.abs(gpu - ref)
+    if out_is_bf16:
+        diff = np.maximum(diff - 2.0 ** -8 * np.abs(ref), 0.0)
+    scale = np.sqrt(np.mean(ref ** 2))
+    worst = float((diff / (scale * cond)).max())
+    assert worst <= TOL_BF16, f"o_gated: row-conditioned error {worst:.3e} > {TOL_BF16:.1e}"
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
@@ -49,8 +65,8 @@ def test_layer_core_small_varlen(kda, out_dtype):
                                 inp.beta_logit, inp.g, inp.cu_seqlens, inp.S0,
                                 out_dtype=out_dtype)
     torch.cuda.synchronize()
-    ref_o, ref_S = oracle_layer_core(inp)
-    assert_close(to64(og), ref_o, TOL_BF16, "o_gated", out_is_bf16=out_dtype == torch.bfloat16)
+    ref_o, ref_S, ref_ot = oracle_layer_core(inp)
+    assert_gated_close(to64(og), ref_o, ref_ot, out_dtype == torch.bfloat16)
     assert_close(to64(Sf), ref_S, TOL_BF16, "S_final")
 
 
@@ -61,12 +77,15 @@ def test_layer_core_matches_its_three_calls(kda):
                                 inp.beta_logit, inp.g, inp.cu_seqlens, None,
                                 out_dtype=torch.float32)
     qh, kh, vv, la, beta = kda.kda_frontend(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A,
-                                            inp.b, inp.beta_logit, inp.cu_seqlens)
+                                            inp.b, inp.beta_logit, inp.cu_seqlens,
+                                            out_dtype=torch.float32)
     ot, Sf2 = kda.kda_prefill(qh, kh, vv, la, beta, inp.cu_seqlens, None,
                               out_dtype=torch.float32)
     og2 = kda.kda_output_gate(ot, inp.g, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert torch.equal(og, og2) and torch.equal(Sf, Sf2)
+    _, _, ref_ot = oracle_layer_core(inp)
+    assert_close(to64(ot), ref_ot, TOL_FP32 * 10, "o~ (before the gate)")
 
 
 def test_layer_core_full_varlen_sampled_heads(kda):
@@ -78,8 +97,8 @@ def test_layer_core_full_varlen_sampled_heads(kda):
                                 out_dtype=torch.bfloat16)
     torch.cuda.synchronize()
     heads = [0, 47, 95]
-    ref_o, ref_S = oracle_layer_core(inp, heads)
-    assert_close(to64(og[:, heads]), ref_o, TOL_BF16, "o_gated", out_is_bf16=True)
+    ref_o, ref_S, ref_ot = oracle_layer_core(inp, heads)
+    assert_gated_close(to64(og[:, heads]), ref_o, ref_ot, True)
     assert_close(to64(Sf[:, heads]), ref_S, TOL_BF16, "S_final")
 
 
