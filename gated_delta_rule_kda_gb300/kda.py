@@ -44,8 +44,12 @@ EXPORTED = (
     "kda_output_gate",
     "kda_layer_core_workspace_size",
     "kda_layer_core",
+    "kda_layer_core_noalloc",
     "kda_get_device_status",
 )
+
+# Capacity of the fixed scratch array behind kda_layer_core_noalloc (include/kda.h).
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
 
 class KdaError(RuntimeError):
@@ -83,6 +87,9 @@ def _load() -> ctypes.CDLL:
     lib.kda_layer_core.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, F, F, F,
                                    ctypes.c_int, P, P, P, SZ, P]
     lib.kda_layer_core.restype = ctypes.c_int
+    lib.kda_layer_core_noalloc.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, F, F,
+                                           F, ctypes.c_int, P, P, P]
+    lib.kda_layer_core_noalloc.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.kda_get_device_status.restype = ctypes.c_int
     return lib
@@ -228,6 +235,23 @@ def kda_layer_core(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=No
                              float(l2_eps), float(rms_eps), _dtype_code(o.dtype), _p(o),
                              _p(S_final), _p(workspace), wbytes, _stream(stream))
     _check("kda_layer_core", rc)
+    return o, S_final
+
+
+def kda_layer_core_noalloc(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=None,
+                           scale=DEFAULT_SCALE, l2_eps=1e-6, rms_eps=1e-6, *, o, S_final=None,
+                           stream=None):
+    """kda_layer_core for callers that cannot allocate device memory: the library
+    supplies the scratch from a fixed array of NOALLOC_SCRATCH_BYTES bytes.
+    `o` (and `S_final` if wanted) must be provided by the caller; nothing is
+    allocated here.  Calls that overlap on the GPU race on the shared scratch."""
+    T, H, _ = qp.shape
+    N = cu_seqlens.shape[0] - 1
+    rc = _lib.kda_layer_core_noalloc(N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A),
+                                     _p(b), _p(beta_logit), _p(g), _p(cu_seqlens), _p(S0),
+                                     float(scale), float(l2_eps), float(rms_eps),
+                                     _dtype_code(o.dtype), _p(o), _p(S_final), _stream(stream))
+    _check("kda_layer_core_noalloc", rc)
     return o, S_final
 
 

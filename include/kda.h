@@ -207,6 +207,40 @@ kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_he
                           float *S_final, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kda_layer_core_noalloc - kda_layer_core without a caller-provided workspace.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory themselves, for example a plugin inside a host
+ * application that owns every device allocation and hands out no scratch, or a
+ * latency-critical path on which an allocation (and the synchronisation it may
+ * imply) is not acceptable.
+ *
+ * Arguments and results are those of kda_layer_core.  The scratch it needs is
+ * taken from a fixed array of KDA_NOALLOC_SCRATCH_BYTES bytes in the library's
+ * own device memory, which every GPU that loads the library holds until the
+ * process exits.  The call allocates nothing and frees nothing.
+ *   - Sizes whose scratch, kda_layer_core_workspace_size(), exceeds
+ *     KDA_NOALLOC_SCRATCH_BYTES are rejected with KDA_ERR_UNSUPPORTED before any
+ *     launch (with fp32 intermediates that is about 26,000 (token, head) rows).
+ *   - All calls share the one array, and it keeps the last call's contents.
+ *     Nothing in it has to start at zero: every stage writes its part in full
+ *     before the next stage reads it.  Calls that overlap on the GPU (two
+ *     streams, or two host threads, at once) race on the array and corrupt each
+ *     other's results, so serialise them.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+kda_status kda_layer_core_noalloc(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                  const void *qp, const void *kp, const void *vp,
+                                  const float *conv_w, const void *z, const float *A,
+                                  const float *b, const void *beta_logit, const void *g,
+                                  const int32_t *cu_seqlens, const float *S0, float scale,
+                                  float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
+                                  float *S_final, void *stream);
+
+/*
  * kda_get_device_status - synchronises `stream`, then returns and clears the
  * device status word: KDA_OK, KDA_ERR_DEVICE_TIMEOUT or KDA_ERR_DEVICE_CHECK
  * (KDA_ERR_CUDA if the synchronisation itself fails).  If detail is not
