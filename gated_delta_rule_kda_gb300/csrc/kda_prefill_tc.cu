@@ -25,21 +25,36 @@
 // causal 32 x 32 Gram block is ONE dense tensor-core product; the pairs i > r
 // that the range does not cover are masked out afterwards.
 //
+// In log2 units, D_r = (gamma_r - gamma_15) log2 e, E = 2^D, em = e^{gamma_15},
+// e31 = 2^{D_31}, so Gamma_r = em E_r and Gamma_C = em e31.  The state is kept
+// in TMEM as X = S / e31 of the chunk that produced it (per key channel):
+//   W  = (Tb (k E)) Diag(em),  Q~ = (q E) Diag(em)   (both bounded by |k|, |q|)
+//   S0 = Diag(e31_prev) X,     X_new = Diag(em) S0 + (k E^-1)^T U
+// em multiplies the q / W side of every product, never the state operand: em
+// can be as small as e^-80, and a state operand scaled by it would lose its low
+// bf16 half to the subnormal range.
+//
 // The state is held TRANSPOSED (TMEM lane = value channel c, column = key
 // channel j), so every product is an M = 128 tcgen05.mma:
 //   M1  G = [k E ; q E] . (k E^-1)^T                  (lanes 0-31 -> A, 32-63 -> P)
 //   M2  U~^T = V^T . Tb^T                            (V read MN-major from its staged tile)
-//   M2b W' = Tb . (k E)          (Tb repeated in all four lane quarters; B read MN-major)
+//   M2b W'^T = (k E)^T . Tb^T                        (k E read MN-major; lane = key channel)
 //   M3  [ (W S0)^T | (Q~ S0)^T ] = S0^T . [W ; Q~]^T   (A = S0^T from TMEM)
 //   M4  (Q~ S0 + P U)^T += U^T . P^T
-//   M5  X^T += U^T . (k E^-1)    (the state kept as X = S / e31; B read MN-major)
+//   M5  X^T = (Diag(em) S0)^T + U^T . (k E^-1)        (the Gram's B tile, read MN-major)
 //
 // Precision: an fp32 quantity x enters an MMA as x = hi + lo (two bf16,
 // round-to-nearest), and a product X.Y is formed as hi.hi + hi.lo + lo.hi
 // (fp32 accumulation); V is exact in bf16 and enters once.
 //
-// Inputs of chunk c+1 are staged with TMA (q, k, v, log_alpha) and cp.async (beta)
-// while chunk c is processed.
+// Warp roles.  Only M3 .. M5 depend on the state; everything before them
+// depends on the chunk's inputs alone.  Warps 4-7 (the prep group) therefore
+// build chunk c+1's operands (decay, [k E ; q E] and k E^-1, the Gram, the
+// triangular solve, U~ and W') while warps 0-3 (the chain group) run the
+// state-dependent products of chunk c.  The operands of a chunk live in one of
+// two slots (shared-memory tiles, U~ in TMEM); the groups hand slots over with
+// mbarriers ("full" prep -> chain, "empty" chain -> prep), and every wait is
+// bounded in time.
 #include <cuda.h>
 #include <cstring>
 #include <cudaTypedefs.h>
@@ -52,54 +67,79 @@ namespace {
 using namespace tc;
 
 constexpr int kC = 32;
-constexpr int kThreads = 256;
-constexpr uint64_t kWaitNs = 2000000000ull;  // bound on every wait for the tensor core
+constexpr int kThreads = 384;  // chain group: warps 0-3, prep group: warps 4-11
+constexpr uint64_t kWaitNs = 2000000000ull;  // bound on every wait
 
 // ---- shared memory map (bytes from a 1024-aligned base) --------------------
-// Two input buffers, each: q, k, v tiles (bf16 [32][128] in the swizzled tile
-// layout below, written by TMA with 128-byte swizzle), log_alpha (fp32, four
-// [32 rows][32 channels] boxes of 4096 bytes), beta [32].
-constexpr uint32_t IB_Q = 0, IB_K = 8192, IB_V = 16384, IB_LA = 24576, IB_BETA = 40960;
-constexpr uint32_t IB_SIZE = 43008;
-constexpr uint32_t W_E = 2 * IB_SIZE;    // fp32 [32][128] 2^D, then (solve) Tb x4 hi (16 KB)
-constexpr uint32_t W_EI = W_E + 16384;   // fp32 [32][128] 2^-D, then Tb x4 lo (16 KB)
-constexpr uint32_t W_X = W_EI + 16384;   // [k E ; q E] hi (16 KB) | lo (16 KB), 64 rows x 128 K
-constexpr uint32_t W_R = W_X + 32768;    // R = k E^-1 hi (8 KB) | lo (8 KB), 32 rows x 128 K
-constexpr uint32_t W_WQ = W_R + 16384;   // [W ; Q~] hi (16 KB) | lo (16 KB), 64 rows x 128 K
-constexpr uint32_t W_P = W_WQ + 32768;   // P hi (4 KB) | lo (4 KB), 32 rows x 32 K
-constexpr uint32_t W_A = W_P + 8192;     // fp32 [32][33]
-constexpr uint32_t W_T = W_A + 4224;     // fp32 [32][33]
-constexpr uint32_t W_VEC = W_T + 4224;   // em[2][128], e31[2][128] (by chunk parity)
-constexpr uint32_t W_BAR = W_VEC + 4 * 512;   // two MMA mbarriers, then two TMA mbarriers
-constexpr uint32_t W_TSLOT = W_BAR + 32;
-constexpr uint32_t kTmaBytes = 10 * 4096;        // 6 bf16 boxes (q, k, v) + 4 fp32 boxes
-constexpr uint32_t SM_DYN = W_TSLOT + 8 + 1024;  // + alignment slack
-constexpr int kLd = 33;  // padded row stride of A and T
+// q, k, v tiles (bf16 [32][128], two 64-column blocks with 128-byte swizzle, as
+// written by TMA) for two chunks.  log_alpha travels through registers.
+constexpr uint32_t S_QKV = 0, QKV_SIZE = 24576, QO = 0, KO = 8192, VO = 16384;
+// D (fp32 [32][128], log2 units); once F3 has read it the region holds Tb hi | lo
+// (a 32-row operand tile, K = 32), then A and T (fp32 [32][32], XOR-swizzled rows).
+constexpr uint32_t S_DT = 2 * QKV_SIZE;
+constexpr uint32_t S_TB = S_DT;
+constexpr uint32_t S_A = S_DT + 8192;
+constexpr uint32_t S_T = S_A + 4096;
+// [k E ; q E] hi | lo (64 rows), private to the prep group.
+constexpr uint32_t S_WX = S_DT + 16384;
+// Per slot: [W ; Q~] hi | lo (64 rows), R = k E^-1 hi | lo (32 rows),
+// P hi | lo (32 rows, K = 32).
+constexpr uint32_t S_WQ = S_WX + 32768, WQ_SIZE = 32768;
+constexpr uint32_t S_R = S_WQ + 2 * WQ_SIZE, R_SIZE = 16384;
+constexpr uint32_t S_P = S_R + 2 * R_SIZE, P_SIZE = 8192;
+constexpr uint32_t S_STG = S_P + 2 * P_SIZE;  // bf16 output staging [32][128]
+constexpr uint32_t S_VEC = S_STG + 8192;      // em[2][128], e31p[2][128], e31[2][128]
+constexpr uint32_t S_BETA = S_VEC + 3072;     // beta [2][32]
+constexpr uint32_t S_BAR = S_BETA + 256;
+constexpr uint32_t S_TSLOT = S_BAR + 128;
+constexpr uint32_t SM_DYN = S_TSLOT + 16 + 1024;  // + alignment slack
+static_assert(SM_DYN <= 232448, "shared memory map exceeds 227 KB");
+// M1 reads 128 rows of the 64-row [k E ; q E] tile (rows 64-127 are ignored):
+// what follows the tile must still be inside the map.
+static_assert(S_WX + 32768 + 8192 <= S_STG, "M1's A view leaves the map");
+
+// A and T: element (r, i) of a [32][32] fp32 matrix.  The column is XOR-ed
+// with r ^ (r >> 3): row-wise writes by 32 threads, the four 8 x 8 diagonal
+// blocks read in parallel, and the Tb pass all hit distinct banks.
+__device__ __forceinline__ int ati(int r, int i) { return r * 32 + ((i ^ r ^ (r >> 3)) & 31); }
+
+// mbarriers (8 bytes each, from S_BAR)
+constexpr int B_TQKV = 0;   // [2] TMA q/k/v by slot
+constexpr int B_CA = 2, B_CB = 3, B_PA = 4, B_PB = 5;  // MMA completion, one per issuer
+constexpr int B_FULL = 6;   // [2] prep -> chain: slot holds a chunk's operands
+constexpr int B_EMPTY = 8;  // [2] chain -> prep: slot consumed
+constexpr int kNumBars = 10;
 
 // ---- TMEM column map (512 columns) -----------------------------------------
-constexpr uint32_t TM_ST = 0;    // state, stored as S^T / e31 (lane c, column j), fp32
-constexpr uint32_t TM_D1 = 128;  // [(W S0)^T | (Q~ S0 + P U)^T] (32 + 32)
-constexpr uint32_t TM_DG = 192;  // Gram result, K steps 0-3 (lanes 0-31 k rows, 32-63 q rows)
-constexpr uint32_t TM_DU = 224;  // Gram result, K steps 4-7; then U~^T (32 columns)
-constexpr uint32_t TM_WT = 256;  // W' = Tb (k E) (rows r repeated in every lane quarter), 128
-                                 // columns; then the K steps 4-7 half of M3 (64 columns)
-constexpr uint32_t TM_OPS = 384; // M3's A operand S0^T hi (64) | lo (64); then U^T hi (16) | lo (16)
+constexpr uint32_t TM_ST = 0;    // state X^T (lane c, column j), fp32
+constexpr uint32_t TM_OPS = 128; // M3's A operand S0^T hi (64) | lo (64); then U^T hi (16) | lo (16)
+constexpr uint32_t TM_D3A = 256; // M3, K steps 0-3: [(W S0)^T | (Q~ S0)^T (+ M4)]
+constexpr uint32_t TM_D3B = 320; // M3, K steps 4-7
+constexpr uint32_t TM_DG = 384;  // Gram, K steps 0-3; then W'^T (lane j, column r)
+constexpr uint32_t TM_DU = 416;  // Gram, K steps 4-7
+constexpr uint32_t TM_UT = 448;  // U~^T by slot (32 columns each)
+
+// Threads with a fixed job.
+constexpr int kCA = 0, kCB = 32;            // chain-group MMA issuers
+constexpr int kPA = 128, kPB = 160;         // prep-group MMA issuers
+constexpr int kTmaThread = 192;             // prep-group TMA issuer
+constexpr int kChainBar = 1, kPrepBar = 2;  // named barriers
+constexpr int kChainThreads = 128, kPrepThreads = 256;
 
 // Swizzled [rows][128 bf16] operand tile with `rows` rows: two 64-column blocks
 // of rows x 128 bytes, 16-byte chunk j of row i at chunk position j ^ (i % 8).
-// Read K-major it has `rows` rows and K = 128; read MN-major (K = the rows) its
-// 64-element MN blocks are rows * 128 bytes apart.
 __device__ __forceinline__ uint32_t tile_chunk(int rows, int i, int cc) {
     return (uint32_t)((cc >> 3) * rows * 128 + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
 }
-// fp32 [32][128] with 16-byte chunks swizzled by row.
+// fp32 [32][128] table with 16-byte chunks permuted per row so that both the
+// row-wise writes (32 consecutive channels) and the reads of chunk pairs
+// (2cc, 2cc+1) by 8 consecutive threads hit 8 distinct bank groups.
 __device__ __forceinline__ uint32_t e_chunk(int r, int q) {  // q = 4-float chunk 0..31
-    return (uint32_t)(r * 512 + (((q ^ r) & 31) << 4));
+    return (uint32_t)(r * 512 + (((q ^ ((q >> 3) & 1) ^ r) & 31) << 4));
 }
 
 struct Params {
-    CUtensorMap tm_q, tm_k, tm_v, tm_la;  // [T][H*128] with boxes of 32 tokens
-    const __nv_bfloat16 *q, *k, *v;
+    CUtensorMap tm_q, tm_k, tm_v;  // [T][H*128] bf16 with boxes of 32 tokens x 64 channels
     const float *log_alpha, *beta, *S0;
     const int32_t *cu_seqlens;
     int H;
@@ -139,531 +179,691 @@ __device__ __forceinline__ void mul8(float (&x)[8], const float4 &a, const float
     x[4] = p2.x; x[5] = p2.y; x[6] = p3.x; x[7] = p3.y;
 }
 
-// MMAs are issued by two threads (lane 0 of warps 0 and 1), each tracking its
-// own work on its own mbarrier.  Those two threads wait (bounded) for their
-// barrier; the CTA barrier then orders every other thread after both.
-constexpr int kIssuerA = 0, kIssuerB = 32;
-__device__ __forceinline__ bool wait_mma(uint64_t *bar, uint32_t &phase, DeviceStatus st,
+// ---- group synchronisation (128-thread named barriers) ----------------------
+__device__ __forceinline__ int group_size(int id) {
+    return id == kChainBar ? kChainThreads : kPrepThreads;
+}
+__device__ __forceinline__ void group_sync(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(group_size(id)) : "memory");
+}
+// Barrier over the group that also ANDs a predicate across it.
+__device__ __forceinline__ bool group_and(int id, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(group_size(id))
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Bounded wait by one thread; a timeout is recorded with `where`.
+__device__ __forceinline__ bool wait_one(uint64_t *bar, uint32_t parity, DeviceStatus st,
                                          uint32_t where) {
-    bool ok = true;
-    if (threadIdx.x == kIssuerA || threadIdx.x == kIssuerB) {
-        ok = mbar_wait_bounded(bar + (threadIdx.x == kIssuerB), phase & 1u, kWaitNs);
-        if (!ok) record_status(st, KDA_ERR_DEVICE_TIMEOUT, where);
-    }
-    ++phase;
-    ok = __syncthreads_and(ok) != 0;
-    fence_after_sync();
+    const bool ok = mbar_wait_bounded(bar, parity, kWaitNs);
+    if (!ok) record_status(st, KDA_ERR_DEVICE_TIMEOUT, where);
     return ok;
 }
-
-// Operand writes (generic-proxy smem stores and tcgen05.st) -> visible to the MMA.
-__device__ __forceinline__ void publish_operands() {
+// Operand writes (generic-proxy smem stores and tcgen05.st) -> visible to an MMA
+// issued by a thread of the same group after this barrier.
+__device__ __forceinline__ void publish(int id) {
     tmem_wait_st();
     fence_proxy_async_smem();
     fence_before_sync();
-    __syncthreads();
+    group_sync(id);
     fence_after_sync();
 }
 
-// Stage chunk [t0, t0 + 32) of this head into input buffer `buf`: one thread
-// issues the TMA boxes, threads 0..31 fetch beta (zero past nrow).  Rows past the
-// sequence end are not masked here: log_alpha and beta are masked where they are
-// used, which keeps those rows out of every product (see the kernel).
-constexpr int kTmaThread = 64;
-__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *buf, uint64_t *tbar,
-                                            int t0, int nrow, int h, int tid) {
+// Stage chunk [t0, t0 + 32) of head h: q/k/v into slot `slot` (TMA, one
+// thread), beta by threads pt < 32 (cp.async, zero past nrow).  Rows past the
+// sequence end are not masked here: log_alpha and beta are masked where they
+// are used, which keeps those rows out of every product (see the kernel).
+__device__ __forceinline__ void issue_loads(const Params &p, unsigned char *sm, uint64_t *bar,
+                                            int slot, int t0, int nrow, int h, int tid) {
     if (tid == kTmaThread) {
-        fence_proxy_async_smem();  // earlier generic accesses to this buffer come first
-        mbar_arrive_expect_tx(tbar, kTmaBytes);
+        fence_proxy_async_smem();  // earlier generic accesses to these buffers come first
+        unsigned char *qkv = sm + S_QKV + slot * QKV_SIZE;
+        mbar_arrive_expect_tx(bar + B_TQKV + slot, 6 * 4096);
         const CUtensorMap *maps[3] = {&p.tm_q, &p.tm_k, &p.tm_v};
-        const uint32_t dst[3] = {IB_Q, IB_K, IB_V};
+        const uint32_t dst[3] = {QO, KO, VO};
 #pragma unroll
         for (int a = 0; a < 3; ++a)
 #pragma unroll
             for (int b = 0; b < 2; ++b)
-                tma_load_2d(smem_u32(buf + dst[a] + 4096 * b), maps[a], h * kD + 64 * b, t0, tbar);
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            tma_load_2d(smem_u32(buf + IB_LA + 4096 * b), &p.tm_la, h * kD + 32 * b, t0, tbar);
+                tma_load_2d(smem_u32(qkv + dst[a] + 4096 * b), maps[a], h * kD + 64 * b, t0,
+                            bar + B_TQKV + slot);
     }
-    if (tid < kC) {
-        const bool ok = tid < nrow;
-        const float *s = ok ? p.beta + (size_t)(t0 + tid) * p.H + h : p.beta;
-        cp_async4(smem_u32(buf + IB_BETA + 4 * tid), s, ok ? 4u : 0u);
+    const int pt = tid - 128;
+    if (pt >= 0 && pt < kC) {
+        const bool ok = pt < nrow;
+        const float *s = ok ? p.beta + (size_t)(t0 + pt) * p.H + h : p.beta;
+        cp_async4(smem_u32(sm + S_BETA + 128 * slot + 4 * pt), s, ok ? 4u : 0u);
         cp_async_commit();
     }
 }
 
-// Algebra per chunk (log2 units, D_r = (gamma_r - gamma_15) log2 e, E = 2^D,
-// em = e^{gamma_15}, e31 = 2^{D_31}, so Gamma_r = em E_r and Gamma_C = em e31):
-//   Gram:  G = [k E ; q E] (k E^-1)^T  ->  A = beta_r G_k (i < r), P = G_q (i <= r)
-//   W = Tb (k Gamma) = (Tb (k E)) diag(em),   Q~ = (q E) diag(em),   U~ = Tb V
-//   K^ = (k E^-1) diag(e31)  =>  S_C = Diag(e31) [ Diag(em) S0 + (k E^-1)^T U ]
-// The state is kept in TMEM as X = S / e31 (per key channel), so the update is
-// X <- Diag(em) S0 + (k E^-1)^T U with the Gram's own R = k E^-1 tile as M5's
-// B operand, and S0 = Diag(e31_prev) X is formed once per chunk in the pass that
-// also builds M3's A operand.
-template <typename Tout>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ Params p) {
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float *vec = reinterpret_cast<float *>(sm + W_VEC);  // em[2][128] | e31[2][128]
-    float *sA = reinterpret_cast<float *>(sm + W_A);
-    float *sT = reinterpret_cast<float *>(sm + W_T);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + W_BAR);
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + W_TSLOT);
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;
-    const int trow = 32 * quarter + lane;  // this thread's TMEM lane
-    const int H = p.H;
-    const int h = blockIdx.x % H, n = blockIdx.x / H;
-    const int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
-    const size_t state_off = ((size_t)n * H + h) * (size_t)(kD * kD);
-
-    if (warp == 0) {
-        tmem_alloc(tslot, 512);
-        tmem_relinquish();
+// log_alpha of chunk [t0, t0 + 32): rows 4 rg .. 4 rg + 3, channels 4 q4 .. 4 q4 + 3
+// (rows past nrow zero).
+__device__ __forceinline__ void load_log_alpha(const Params &p, int t0, int nrow, int h, int q4,
+                                               int rg, float4 (&la)[4]) {
+    const float *src = p.log_alpha + ((size_t)t0 * p.H + h) * kD + 4 * q4;
+    const size_t stride = (size_t)p.H * kD;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = 4 * rg + k;
+        la[k] = r < nrow ? __ldg(reinterpret_cast<const float4 *>(src + r * stride))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    uint64_t *tbar = bar + 2;  // TMA barriers, one per input buffer
-    if (tid == kTmaThread) {
-        mbar_init(bar, 1);
-        mbar_init(bar + 1, 1);
-        mbar_init(tbar, 1);
-        mbar_init(tbar + 1, 1);
-        fence_mbar_init();
-    }
-    if (tid < kD) vec[2 * kD + kD + tid] = 1.f;  // e31 of "chunk -1": the entering state is exact
-    __syncthreads();
-    if (t_begin < t_end) issue_loads(p, sm, tbar, t_begin, min(kC, t_end - t_begin), h, tid);
-    fence_before_sync();
-    __syncthreads();
-    fence_after_sync();
-    const uint32_t tb = *tslot;
-    const uint32_t tl = tb + ((uint32_t)(32 * quarter) << 16);  // this warp's lane quarter
-    uint32_t phase = 0;
+}
 
-    // ---- entering state -> TMEM, transposed (lane c, column j) ----
-    {
-        const int c = trow;
-        uint32_t w[32];
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const int j0 = 64 * half + 32 * part;
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-                w[jj] = p.S0 ? __float_as_uint(p.S0[state_off + (size_t)(j0 + jj) * kD + c]) : 0u;
-            tmem_st32(tl + TM_ST + j0, w);
-        }
-        tmem_wait_st();
-    }
-
-    // Readout of a finished chunk: o[t0 + r][c] = scale (Q~ S0 + P U)^T[c][r], the two K
-    // halves of M3 summed.  Done by warps 4..7 (one per lane quarter): the tile is staged
-    // row-major in the (dead) E^-1 table, then written out as 16-byte row chunks.
-    Tout *o = static_cast<Tout *>(p.o);
-    auto readout = [&](int t0r, int nrowr) {
-        Tout *ot = reinterpret_cast<Tout *>(sm + W_EI);  // [32][128]
-        const int c = trow;
-#pragma unroll
-        for (int r0 = 0; r0 < 32; r0 += 16) {
-            float ov[16], ov2[16];
-            tmem_ld16(tl + TM_D1 + 32 + r0, ov);
-            tmem_ld16(tl + TM_WT + 32 + r0, ov2);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                Elem<Tout>::store(ot + (r0 + e) * kD + c, p.scale * (ov[e] + ov2[e]));
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // warps 4..7 only
-        constexpr int kPerRow = kD * (int)sizeof(Tout) / 16;  // 16-byte chunks per row
-        const int lt = tid - 128;
-        for (int e = lt; e < kC * kPerRow; e += 128) {
-            const int r = e / kPerRow, ch = e % kPerRow;
-            if (r < nrowr)
-                *reinterpret_cast<uint4 *>(reinterpret_cast<unsigned char *>(
-                    o + ((size_t)(t0r + r) * H + h) * kD) + 16 * ch) =
-                    *reinterpret_cast<const uint4 *>(reinterpret_cast<const unsigned char *>(ot) +
-                                                     r * kD * sizeof(Tout) + 16 * ch);
-        }
-    };
-
+// ============================================================================
+// Prep group (warps 4-11, 256 threads): operands of every chunk, in order.
+// ============================================================================
+__device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, uint32_t tb,
+                                           int h, int t_begin, int t_end, int nchunks) {
+    const int tid = threadIdx.x, pt = tid - 128, lane = tid & 31;
+    const int quarter = (pt >> 5) & 3, half = pt >> 7;  // TMEM lane quarter; second warp of it
+    const uint32_t tl = tb + ((uint32_t)(32 * quarter) << 16);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);
+    float *vec = reinterpret_cast<float *>(sm + S_VEC);
+    float *sA = reinterpret_cast<float *>(sm + S_A);
+    float *sT = reinterpret_cast<float *>(sm + S_T);
+    unsigned char *wx = sm + S_WX;
+    // Decay pass layout: channels 4 q4 .. 4 q4 + 3, rows 4 rg .. 4 rg + 3; the
+    // eight row groups of a channel quad sit in lanes (lane & 3) + 4 rg of a warp.
+    const int q4 = 4 * (pt >> 5) + (lane & 3), rg = lane >> 2;
+    float4 e31_prev = make_float4(1.f, 1.f, 1.f, 1.f);  // 1: the entering state is exact
+    uint32_t ph = 0;   // MMA barrier phase (PA and PB)
+    int consumed = 0;  // chunks whose q/k/v were waited for
     bool alive = true;
-    int chunk = 0, t0_prev = 0, nrow_prev = 0;
-    for (int t0 = t_begin; t0 < t_end && alive; t0 += kC, ++chunk) {
-        const int nrow = min(kC, t_end - t0);
-        const int par = chunk & 1;
-        unsigned char *buf = sm + par * IB_SIZE;
-        const float *beta_s = reinterpret_cast<const float *>(buf + IB_BETA);
-        float *em = vec + par * kD;
-        float *e31 = vec + 2 * kD + par * kD;
-        const float *e31_prev = vec + 2 * kD + (par ^ 1) * kD;
+    float4 la[4];      // log_alpha of the next chunk (this thread's 4 rows x 4 channels)
 
-        // ---- F1: this chunk's inputs have landed; stage the next chunk ----
+    if (nchunks > 0) {
+        const int n0 = min(kC, t_end - t_begin);
+        issue_loads(p, sm, bar, 0, t_begin, n0, h, tid);
+        load_log_alpha(p, t_begin, n0, h, q4, rg, la);
+    }
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        const int t0 = t_begin + kC * c;
+        const int nrow = min(kC, t_end - t0);
+        const unsigned char *qkv = sm + S_QKV + s * QKV_SIZE;
+        const float *beta_s = reinterpret_cast<const float *>(sm + S_BETA + 128 * s);
+        unsigned char *wq = sm + S_WQ + s * WQ_SIZE;
+        unsigned char *rr = sm + S_R + s * R_SIZE;
+        unsigned char *pp = sm + S_P + s * P_SIZE;
+        float *em_s = vec + s * kD, *e31p_s = vec + 2 * kD + s * kD, *e31_s = vec + 4 * kD + s * kD;
+
+        // ---- slot s free again (chunk c-2 finished); chunk c's inputs landed ----
         {
             bool ok = true;
-            if (tid == kTmaThread) {
-                ok = mbar_wait_bounded(tbar + par, (uint32_t)(chunk >> 1) & 1u, kWaitNs);
-                if (!ok) record_status(p.status, KDA_ERR_DEVICE_TIMEOUT, 0);
-            }
-            if (tid < kC) cp_async_wait_all();
-            if (!__syncthreads_and(ok)) {
-                alive = false;
-                break;
-            }
+            if (tid == kPA && c >= 2)
+                ok = wait_one(bar + B_EMPTY + s, ((c >> 1) - 1) & 1, p.status, 10);
+            if (tid == kTmaThread) ok = wait_one(bar + B_TQKV + s, (c >> 1) & 1, p.status, 11);
+            if (pt < kC) cp_async_wait_all();
+            alive = group_and(kPrepBar, ok);
             fence_after_sync();
+            if (!alive) break;
+            consumed = c + 1;
         }
-        if (t0 + kC < t_end)
-            issue_loads(p, sm + (par ^ 1) * IB_SIZE, tbar + (par ^ 1), t0 + kC,
-                        min(kC, t_end - t0 - kC), h, tid);
 
-        // ---- F2: decay factors; threads c and c + 128 share key channel c ----
+        // ---- F2: D (log2 units); em, e31.  Rows 0..15: D = prefix - prefix_15,
+        //      rows 16..31: D = sum of rows 16..r (two scan segments of 4 row groups) ----
         {
-            const int c = tid & 127;
-            const float *la = reinterpret_cast<const float *>(buf + IB_LA);
             const float kL2E = 1.4426950408889634f;
-            const uint32_t cq = (uint32_t)(c >> 2), cb = (uint32_t)((c & 3) << 2);
-            float pre[16];
-            float acc = 0.f;
-            const int r0 = 16 * half;
+            float4 pre[4];
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            const float *lac = la + (c >> 5) * 1024 + (c & 31);  // box c/32, row stride 32
-            for (int r = 0; r < 16; ++r) {
-                const float x = (r0 + r) < nrow ? lac[(r0 + r) * 32] : 0.f;  // rows past the end
-                acc = fmaf(x, kL2E, acc);
-                pre[r] = acc;
+            for (int k = 0; k < 4; ++k) {
+                acc.x = fmaf(la[k].x, kL2E, acc.x);
+                acc.y = fmaf(la[k].y, kL2E, acc.y);
+                acc.z = fmaf(la[k].z, kL2E, acc.z);
+                acc.w = fmaf(la[k].w, kL2E, acc.w);
+                pre[k] = acc;
             }
-            // rows 0..15: D = prefix - prefix_15;  rows 16..31: D = sum of rows 16..r
-            const float sub = half == 0 ? pre[15] : 0.f;
+            float4 incl = acc;  // inclusive scan over the row groups of the segment
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const float d = pre[r] - sub;
-                const uint32_t off =
-                    (uint32_t)((r0 + r) * 512) + ((cq ^ (uint32_t)(r0 + r)) << 4) + cb;
-                *reinterpret_cast<float *>(sm + W_E + off) = ex2_approx(d);
-                *reinterpret_cast<float *>(sm + W_EI + off) = ex2_approx(-d);
+            for (int d = 1; d <= 2; d <<= 1) {
+                float4 y;
+                y.x = __shfl_up_sync(0xffffffffu, incl.x, 4 * d);
+                y.y = __shfl_up_sync(0xffffffffu, incl.y, 4 * d);
+                y.z = __shfl_up_sync(0xffffffffu, incl.z, 4 * d);
+                y.w = __shfl_up_sync(0xffffffffu, incl.w, 4 * d);
+                if ((rg & 3) >= d) {
+                    incl.x += y.x; incl.y += y.y; incl.z += y.z; incl.w += y.w;
+                }
             }
-            if (half == 0) em[c] = ex2_approx(pre[15]);
-            else e31[c] = ex2_approx(pre[15]);
+            float4 mid, last;  // prefix_15 and the sum of rows 16..31
+            mid.x = __shfl_sync(0xffffffffu, incl.x, 12 + (lane & 3));
+            mid.y = __shfl_sync(0xffffffffu, incl.y, 12 + (lane & 3));
+            mid.z = __shfl_sync(0xffffffffu, incl.z, 12 + (lane & 3));
+            mid.w = __shfl_sync(0xffffffffu, incl.w, 12 + (lane & 3));
+            last.x = __shfl_sync(0xffffffffu, incl.x, 28 + (lane & 3));
+            last.y = __shfl_sync(0xffffffffu, incl.y, 28 + (lane & 3));
+            last.z = __shfl_sync(0xffffffffu, incl.z, 28 + (lane & 3));
+            last.w = __shfl_sync(0xffffffffu, incl.w, 28 + (lane & 3));
+            // base = exclusive prefix of this row group, minus prefix_15 in the first segment
+            float4 base;
+            base.x = incl.x - acc.x - (rg < 4 ? mid.x : 0.f);
+            base.y = incl.y - acc.y - (rg < 4 ? mid.y : 0.f);
+            base.z = incl.z - acc.z - (rg < 4 ? mid.z : 0.f);
+            base.w = incl.w - acc.w - (rg < 4 ? mid.w : 0.f);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 dk = make_float4(base.x + pre[k].x, base.y + pre[k].y,
+                                              base.z + pre[k].z, base.w + pre[k].w);
+                *reinterpret_cast<float4 *>(sm + S_DT + e_chunk(4 * rg + k, q4)) = dk;
+            }
+            if (rg == 0) {
+                const float4 em = make_float4(ex2_approx(mid.x), ex2_approx(mid.y),
+                                              ex2_approx(mid.z), ex2_approx(mid.w));
+                const float4 e31 = make_float4(ex2_approx(last.x), ex2_approx(last.y),
+                                               ex2_approx(last.z), ex2_approx(last.w));
+                *reinterpret_cast<float4 *>(em_s + 4 * q4) = em;
+                *reinterpret_cast<float4 *>(e31p_s + 4 * q4) = e31_prev;
+                *reinterpret_cast<float4 *>(e31_s + 4 * q4) = e31;
+                e31_prev = e31;
+            }
         }
-        __syncthreads();
+        if (c + 1 < nchunks) {  // stage chunk c+1 (its q/k/v slot was freed by chunk c-1)
+            const int n1 = min(kC, t_end - t0 - kC);
+            load_log_alpha(p, t0 + kC, n1, h, q4, rg, la);
+            group_sync(kPrepBar);  // D and em complete
+            issue_loads(p, sm, bar, s ^ 1, t0 + kC, n1, h, tid);
+        } else {
+            group_sync(kPrepBar);  // D and em complete
+        }
 
-        // ---- F3: [k E ; q E], R = k E^-1, Q~ = q E em (one 16-byte chunk per job) ----
-#pragma unroll
+        // ---- F3: [k E ; q E] -> wx, R = k E^-1 -> rr, Q~ = q E em -> wq rows 32.. ----
+#pragma unroll 1
         for (int m = 0; m < 2; ++m) {
-            const int e = tid + kThreads * m;  // 512 jobs: row i, chunk cc
+            const int e = pt + 256 * m;  // row i, chunk cc
             const int i = e >> 4, cc = e & 15;
-            float xk[8], xq[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(buf + IB_K + tile_chunk(32, i, cc)), xk);
-            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(buf + IB_Q + tile_chunk(32, i, cc)), xq);
-            const float4 e0 = *reinterpret_cast<const float4 *>(sm + W_E + e_chunk(i, 2 * cc));
-            const float4 e1 = *reinterpret_cast<const float4 *>(sm + W_E + e_chunk(i, 2 * cc + 1));
-            const float4 f0 = *reinterpret_cast<const float4 *>(sm + W_EI + e_chunk(i, 2 * cc));
-            const float4 f1 = *reinterpret_cast<const float4 *>(sm + W_EI + e_chunk(i, 2 * cc + 1));
-            const float4 m0 = *reinterpret_cast<const float4 *>(em + 8 * cc);
-            const float4 m1 = *reinterpret_cast<const float4 *>(em + 8 * cc + 4);
-            float r8[8] = {xk[0], xk[1], xk[2], xk[3], xk[4], xk[5], xk[6], xk[7]};
-            mul8(r8, f0, f1);   // k E^-1
-            mul8(xk, e0, e1);   // k E
-            mul8(xq, e0, e1);   // q E
-            unsigned char *xh = sm + W_X + tile_chunk(64, i, cc);
+            float xk[8], xq[8], d8[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(qkv + KO + tile_chunk(32, i, cc)), xk);
+            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(qkv + QO + tile_chunk(32, i, cc)), xq);
+            {
+                const float4 d0 = *reinterpret_cast<const float4 *>(sm + S_DT + e_chunk(i, 2 * cc));
+                const float4 d1 =
+                    *reinterpret_cast<const float4 *>(sm + S_DT + e_chunk(i, 2 * cc + 1));
+                d8[0] = d0.x; d8[1] = d0.y; d8[2] = d0.z; d8[3] = d0.w;
+                d8[4] = d1.x; d8[5] = d1.y; d8[6] = d1.z; d8[7] = d1.w;
+            }
+            float r8[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const float E = ex2_approx(d8[t]), EI = ex2_approx(-d8[t]);
+                r8[t] = xk[t] * EI;  // k E^-1
+                xk[t] *= E;          // k E
+                xq[t] *= E;          // q E
+            }
+            unsigned char *xh = wx + tile_chunk(64, i, cc);
             store_split_chunk(xh, xh + 16384, xk);
-            xh = sm + W_X + tile_chunk(64, 32 + i, cc);
+            xh = wx + tile_chunk(64, 32 + i, cc);
             store_split_chunk(xh, xh + 16384, xq);
-            unsigned char *rh = sm + W_R + tile_chunk(32, i, cc);
+            unsigned char *rh = rr + tile_chunk(32, i, cc);
             store_split_chunk(rh, rh + 8192, r8);
-            mul8(xq, m0, m1);   // Q~ = q E em
-            unsigned char *qh = sm + W_WQ + tile_chunk(64, 32 + i, cc);
+            const float4 m0 = *reinterpret_cast<const float4 *>(em_s + 8 * cc);
+            const float4 m1 = *reinterpret_cast<const float4 *>(em_s + 8 * cc + 4);
+            mul8(xq, m0, m1);  // Q~ = q E em
+            unsigned char *qh = wq + tile_chunk(64, 32 + i, cc);
             store_split_chunk(qh, qh + 16384, xq);
         }
-        publish_operands();
-        if (tid == kIssuerA || tid == kIssuerB) {  // M1: Gram, K steps split over two issuers
-            // A = [k E ; q E] (rows 64..127 of the view are ignored), B = R
+        publish(kPrepBar);
+        if (tid == kPA || tid == kPB) {  // M1: Gram, K steps split over the two issuers
             const uint32_t id = idesc_bf16_f32(128, 32);
-            const int s0 = tid == kIssuerA ? 0 : 4;
-            const uint32_t d = tb + (tid == kIssuerA ? TM_DG : TM_DU);
-            const uint32_t xh = smem_u32(sm + W_X), xl = xh + 16384;
-            const uint32_t rh = smem_u32(sm + W_R), rl = rh + 8192;
+            const int s0 = tid == kPA ? 0 : 4;
+            const uint32_t d = tb + (tid == kPA ? TM_DG : TM_DU);
+            const uint32_t xh = smem_u32(wx), xl = xh + 16384;
+            const uint32_t rh = smem_u32(rr), rl = rh + 8192;
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(d, sw128_desc_k(xh, 64, s0 + s), sw128_desc_k(rh, 32, s0 + s), id, s > 0);
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(d, sw128_desc_k(xh, 64, s0 + k), sw128_desc_k(rh, 32, s0 + k), id, k > 0);
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(d, sw128_desc_k(xh, 64, s0 + s), sw128_desc_k(rl, 32, s0 + s), id, 1);
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(d, sw128_desc_k(xh, 64, s0 + k), sw128_desc_k(rl, 32, s0 + k), id, 1);
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(d, sw128_desc_k(xl, 64, s0 + s), sw128_desc_k(rh, 32, s0 + s), id, 1);
-            mma_commit(bar + (tid == kIssuerB));
+            for (int k = 0; k < 4; ++k)
+                mma_bf16(d, sw128_desc_k(xl, 64, s0 + k), sw128_desc_k(rh, 32, s0 + k), id, 1);
+            mma_commit(bar + (tid == kPA ? B_PA : B_PB));
+        }
+        {
+            bool ok = true;
+            if (tid == kPA || tid == kPB)
+                ok = wait_one(bar + (tid == kPA ? B_PA : B_PB), ph & 1, p.status, 13);
+            ++ph;
+            alive = group_and(kPrepBar, ok);
+            fence_after_sync();
+            if (!alive) break;
         }
 
-        // ---- F4 (while M1 runs): S0 = e31_prev X -> M3's A operand; X <- em S0 ----
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const int j0 = 64 * half + 32 * part;
-            float sv[32];
-            tmem_ld32(tl + TM_ST + j0, sv);
-            uint32_t hw[16], lw[16], sc[32];
-#pragma unroll
-            for (int jj = 0; jj < 32; jj += 4) {
-                const float4 g = *reinterpret_cast<const float4 *>(e31_prev + j0 + jj);
-                const float2 a = mul2(make_float2(sv[jj], sv[jj + 1]), make_float2(g.x, g.y));
-                const float2 b = mul2(make_float2(sv[jj + 2], sv[jj + 3]), make_float2(g.z, g.w));
-                sv[jj] = a.x; sv[jj + 1] = a.y; sv[jj + 2] = b.x; sv[jj + 3] = b.y;
-            }
-#pragma unroll
-            for (int pp = 0; pp < 16; ++pp) split2(sv[2 * pp], sv[2 * pp + 1], hw[pp], lw[pp]);
-#pragma unroll
-            for (int jj = 0; jj < 32; jj += 4) {
-                const float4 g = *reinterpret_cast<const float4 *>(em + j0 + jj);
-                const float2 a = mul2(make_float2(sv[jj], sv[jj + 1]), make_float2(g.x, g.y));
-                const float2 b = mul2(make_float2(sv[jj + 2], sv[jj + 3]), make_float2(g.z, g.w));
-                sc[jj] = __float_as_uint(a.x);
-                sc[jj + 1] = __float_as_uint(a.y);
-                sc[jj + 2] = __float_as_uint(b.x);
-                sc[jj + 3] = __float_as_uint(b.y);
-            }
-            tmem_st16u(tl + TM_OPS + (j0 >> 1), hw);
-            tmem_st16u(tl + TM_OPS + 64 + (j0 >> 1), lw);
-            tmem_st32(tl + TM_ST + j0, sc);
-        }
-        alive = wait_mma(bar, phase, p.status, 1);
-        if (!alive) break;
-
-        // ---- F5: A (k rows, scaled by beta, strictly lower) and P (q rows, lower) ----
-        if (trow < 64) {
+        // ---- F5: A (k rows, scaled by beta, strictly lower) and P (q rows, lower);
+        //      lanes 0-63, each of the two warps of a lane quarter takes 16 columns ----
+        if (quarter < 2) {
             float g[16], g2[16];
             tmem_ld16(tl + TM_DG + 16 * half, g);
             tmem_ld16(tl + TM_DU + 16 * half, g2);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) g[e] += g2[e];
-            if (trow < 32) {
-                const int r = trow;
+            const int r = lane;
+            if (quarter == 0) {
                 const float br = beta_s[r];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int i = 16 * half + e;
-                    sA[r * kLd + i] = i < r ? br * g[e] : 0.f;
+                    sA[ati(r, i)] = i < r ? br * (g[e] + g2[e]) : 0.f;
                 }
             } else {
-                const int r = trow - 32;
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int i = 16 * half + 8 * c2 + e;
-                        x[e] = i <= r ? g[8 * c2 + e] : 0.f;
+                        x[e] = i <= r ? g[8 * c2 + e] + g2[8 * c2 + e] : 0.f;
                     }
-                    unsigned char *ph = sm + W_P + sw128_chunk_offset(32, r, 2 * half + c2);
-                    store_split_chunk(ph, ph + 4096, x);
+                    unsigned char *ph2 = pp + sw128_chunk_offset(32, r, 2 * half + c2);
+                    store_split_chunk(ph2, ph2 + 4096, x);
                 }
             }
         }
-        __syncthreads();
+        group_sync(kPrepBar);
 
-        // ---- F6: T = (I + A)^-1 on 2 x 2 tiles of 16, then Tb = T diag(beta); while warp 0
-        //      solves the diagonal tiles, warps 4..7 read out the previous chunk ----
-        if (half == 1 && chunk > 0) readout(t0_prev, nrow_prev);
-        if (tid < 32) {  // diagonal tiles, one column per thread
-            const int blk = tid >> 4, jj = tid & 15;
-            float x[16];
+        // ---- F6: T = (I + A)^-1 by 8 x 8 diagonal blocks, then 16 x 16, then 32 x 32;
+        //      Tb = T diag(beta) ----
+        if (pt < 32) {  // the four 8 x 8 diagonal blocks, one column per thread
+            const int o = 8 * (pt >> 3), jj = pt & 7;
+            float x[8];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) x[m] = m == jj ? 1.f : 0.f;
+            for (int m = 0; m < 8; ++m) x[m] = m == jj ? 1.f : 0.f;
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < 8; ++i)
 #pragma unroll
-                for (int m = i + 1; m < 16; ++m)
-                    x[m] = fmaf(-sA[(16 * blk + m) * kLd + 16 * blk + i], x[i], x[m]);
+                for (int m = i + 1; m < 8; ++m) x[m] = fmaf(-sA[ati(o + m, o + i)], x[i], x[m]);
 #pragma unroll
-            for (int m = 0; m < 16; ++m) sT[(16 * blk + m) * kLd + 16 * blk + jj] = x[m];
+            for (int m = 0; m < 8; ++m) sT[ati(o + m, o + jj)] = x[m];
         }
-        __syncthreads();
-        {  // T_10 = -T_11 (A_10 T_00)
-            const int r = tid >> 4, i = tid & 15;
-            float acc = 0.f;
+        group_sync(kPrepBar);
+        {  // 16 x 16 diagonal blocks: T_10 = -T_11 (A_10 T_00) on 8 x 8 sub-blocks
+            const bool act = pt < 128;
+            const int o = 16 * ((pt >> 6) & 1), r = (pt >> 3) & 7, i = pt & 7;
+            float x = 0.f;
+            if (act) {
 #pragma unroll
-            for (int m = 0; m < 16; ++m) acc = fmaf(sA[(16 + r) * kLd + m], sT[m * kLd + i], acc);
-            sT[(16 + r) * kLd + i] = acc;  // X = A_10 T_00 in the T_10 slot
-            __syncthreads();
+                for (int m = 0; m < 8; ++m)
+                    x = fmaf(sA[ati(o + 8 + r, o + m)], sT[ati(o + m, o + i)], x);
+            }
+            if (act) sT[ati(o + r, o + 8 + i)] = 0.f;  // upper block, read by the 32 x 32 step
+            group_sync(kPrepBar);
+            if (act) sT[ati(o + 8 + r, o + i)] = x;  // X = A_10 T_00 in the T_10 slot
+            group_sync(kPrepBar);
+            float y = 0.f;
+            if (act) {
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    y = fmaf(sT[ati(o + 8 + r, o + 8 + m)], sT[ati(o + 8 + m, o + i)], y);
+            }
+            group_sync(kPrepBar);
+            if (act) sT[ati(o + 8 + r, o + i)] = -y;
+        }
+        group_sync(kPrepBar);
+        {  // 32 x 32: T_10 = -T_11 (A_10 T_00) on 16 x 16 blocks, one entry per thread
+            const int r = pt >> 4, i = pt & 15;
+            float x = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) x = fmaf(sA[ati(16 + r, m)], sT[ati(m, i)], x);
+            sT[ati(16 + r, i)] = x;  // the T_10 block was never written before
+            group_sync(kPrepBar);
             float y = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                y = fmaf(sT[(16 + r) * kLd + 16 + m], sT[(16 + m) * kLd + i], y);
-            __syncthreads();
-            sT[(16 + r) * kLd + i] = -y;
+            for (int m = 0; m < 16; ++m) y = fmaf(sT[ati(16 + r, 16 + m)], sT[ati(16 + m, i)], y);
+            group_sync(kPrepBar);
+            sT[ati(16 + r, i)] = -y;
         }
-        __syncthreads();
-        {  // Tb (32 rows x 32 K) written 4 times: rows 32 q + r, so W' lands in every lane quarter
-            const int r = tid >> 3, cc = tid & 3, copy2 = (tid >> 2) & 1;
+        group_sync(kPrepBar);
+        if (pt < 128) {  // Tb (32 rows x K 32): one 16-byte chunk per thread
+            const int r = pt >> 2, cc = pt & 3;
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int i = 8 * cc + e;
-                x[e] = i <= r ? sT[r * kLd + i] * beta_s[i] : 0.f;
+                x[e] = i <= r ? sT[ati(r, i)] * beta_s[i] : 0.f;
             }
-#pragma unroll
-            for (int cp = 0; cp < 2; ++cp) {
-                const int row = 32 * (2 * cp + copy2) + r;
-                unsigned char *th = sm + W_E + sw128_chunk_offset(128, row, cc);
-                store_split_chunk(th, th + 16384, x);
-            }
+            unsigned char *th = sm + S_TB + sw128_chunk_offset(32, r, cc);
+            store_split_chunk(th, th + 4096, x);
         }
-        publish_operands();
-        if (tid == kIssuerA) {  // M2: U~^T = V^T Tb^T  (V exact in bf16, read MN-major)
-            const uint32_t th = smem_u32(sm + W_E), tlo = th + 16384;
+        publish(kPrepBar);
+        if (tid == kPA) {  // M2: U~^T = V^T Tb^T  (V exact in bf16, read MN-major) -> slot s
+            const uint32_t th = smem_u32(sm + S_TB), tlo = th + 4096;
             const uint32_t idv = idesc_bf16_f32(128, 32) | kIdescAMN;
-            const uint32_t va = smem_u32(buf + IB_V);
+            const uint32_t va = smem_u32(qkv + VO);
+            const uint32_t d = tb + TM_UT + 32 * s;
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_DU, sw128_desc_mn(va + 2048 * s, 4096), sw128_desc_k(th, 128, s),
-                         idv, s > 0);
+            for (int k = 0; k < 2; ++k)
+                mma_bf16(d, sw128_desc_mn(va + 2048 * k, 4096), sw128_desc_k(th, 32, k), idv, k > 0);
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_DU, sw128_desc_mn(va + 2048 * s, 4096), sw128_desc_k(tlo, 128, s),
-                         idv, 1);
-            mma_commit(bar);
-        } else if (tid == kIssuerB) {
-            // M2b: W' = Tb (k E): A = Tb x4 (128 rows), B = rows 0..31 of [k E ; q E] MN-major
-            const uint32_t th = smem_u32(sm + W_E), tlo = th + 16384;
-            const uint32_t idw = idesc_bf16_f32(128, 128) | kIdescBMN;
-            const uint32_t xh = smem_u32(sm + W_X), xl = xh + 16384;
+            for (int k = 0; k < 2; ++k)
+                mma_bf16(d, sw128_desc_mn(va + 2048 * k, 4096), sw128_desc_k(tlo, 32, k), idv, 1);
+            mma_commit(bar + B_PA);
+        } else if (tid == kPB) {  // M2b: W'^T = (k E)^T Tb^T, k E read MN-major -> DG
+            const uint32_t th = smem_u32(sm + S_TB), tlo = th + 4096;
+            const uint32_t idw = idesc_bf16_f32(128, 32) | kIdescAMN;
+            const uint32_t xh = smem_u32(wx), xl = xh + 16384;
+            const uint32_t d = tb + TM_DG;
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_WT, sw128_desc_k(th, 128, s), sw128_desc_mn(xh + 2048 * s, 8192),
-                         idw, s > 0);
+            for (int k = 0; k < 2; ++k)
+                mma_bf16(d, sw128_desc_mn(xh + 2048 * k, 8192), sw128_desc_k(th, 32, k), idw, k > 0);
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_WT, sw128_desc_k(th, 128, s), sw128_desc_mn(xl + 2048 * s, 8192),
-                         idw, 1);
+            for (int k = 0; k < 2; ++k)
+                mma_bf16(d, sw128_desc_mn(xh + 2048 * k, 8192), sw128_desc_k(tlo, 32, k), idw, 1);
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16(tb + TM_WT, sw128_desc_k(tlo, 128, s), sw128_desc_mn(xh + 2048 * s, 8192),
-                         idw, 1);
-            mma_commit(bar + 1);
+            for (int k = 0; k < 2; ++k)
+                mma_bf16(d, sw128_desc_mn(xl + 2048 * k, 8192), sw128_desc_k(th, 32, k), idw, 1);
+            mma_commit(bar + B_PB);
         }
-        alive = wait_mma(bar, phase, p.status, 2);
-        if (!alive) break;
-
-        // ---- F7: W = W' diag(em) -> rows 0..31 of M3's B operand (all 8 warps) ----
         {
-            const int r = lane;
-            const int c0 = 16 * (2 * quarter + half);
+            bool ok = true;
+            if (tid == kPA || tid == kPB)
+                ok = wait_one(bar + (tid == kPA ? B_PA : B_PB), ph & 1, p.status, 14);
+            ++ph;
+            alive = group_and(kPrepBar, ok);
+            fence_after_sync();
+            if (!alive) break;
+        }
+
+        // ---- F7: W = W' Diag(em) -> rows 0..31 of wq; thread = key channel j, 16 rows ----
+        {
+            const int j = pt & 127, r0 = 16 * half;
             float w[16];
-            tmem_ld16(tl + TM_WT + c0, w);
+            tmem_ld16(tl + TM_DG + r0, w);
+            const float emj = em_s[j];
+            const uint32_t cbase = (uint32_t)((j >> 6) * 64 * 128 + ((j & 7) << 1));
+            const int jc = (j & 63) >> 3;
 #pragma unroll
-            for (int h8 = 0; h8 < 2; ++h8) {
-                float x[8] = {w[8 * h8], w[8 * h8 + 1], w[8 * h8 + 2], w[8 * h8 + 3],
-                              w[8 * h8 + 4], w[8 * h8 + 5], w[8 * h8 + 6], w[8 * h8 + 7]};
-                const float4 m0 = *reinterpret_cast<const float4 *>(em + c0 + 8 * h8);
-                const float4 m1 = *reinterpret_cast<const float4 *>(em + c0 + 8 * h8 + 4);
-                mul8(x, m0, m1);
-                unsigned char *wh = sm + W_WQ + tile_chunk(64, r, (c0 >> 3) + h8);
-                store_split_chunk(wh, wh + 16384, x);
+            for (int rr2 = 0; rr2 < 16; rr2 += 2) {
+                const int r = r0 + rr2;
+                uint32_t hw, lw;
+                split2(w[rr2] * emj, w[rr2 + 1] * emj, hw, lw);
+                const uint32_t o0 = cbase + r * 128 + ((jc ^ (r & 7)) << 4);
+                const uint32_t o1 = cbase + (r + 1) * 128 + ((jc ^ ((r + 1) & 7)) << 4);
+                *reinterpret_cast<uint16_t *>(wq + o0) = (uint16_t)(hw & 0xFFFFu);
+                *reinterpret_cast<uint16_t *>(wq + o1) = (uint16_t)(hw >> 16);
+                *reinterpret_cast<uint16_t *>(wq + 16384 + o0) = (uint16_t)(lw & 0xFFFFu);
+                *reinterpret_cast<uint16_t *>(wq + 16384 + o1) = (uint16_t)(lw >> 16);
             }
         }
-        publish_operands();
-        if (tid == kIssuerA || tid == kIssuerB) {
-            // M3: [(W S0)^T | (Q~ S0)^T] = S0^T [W ; Q~]^T, K steps 0-3 -> D1, 4-7 -> WT
-            const uint32_t id = idesc_bf16_f32(128, 64);
-            const int s0 = tid == kIssuerA ? 0 : 4;
-            const uint32_t d = tb + (tid == kIssuerA ? TM_D1 : TM_WT);
-            const uint32_t bh = smem_u32(sm + W_WQ), bl = bh + 16384;
+        publish(kPrepBar);  // also orders M2's U~ (TMEM) before the hand-over
+        if (tid == kPA) mbar_arrive(bar + B_FULL + s);
+    }
+
+    if (pt < kC) cp_async_wait_all();  // nothing may still be in flight into shared memory
+    if (!alive && tid == kTmaThread) {  // let outstanding TMA loads land before leaving
+        const int issued = min(nchunks, consumed + 1);
+        for (int c = consumed; c < issued; ++c)
+            mbar_wait_bounded(bar + B_TQKV + (c & 1), (c >> 1) & 1, kWaitNs);
+    }
+}
+
+// ============================================================================
+// Chain group (warps 0-3): the state-dependent products, chunk by chunk.
+// ============================================================================
+template <typename Tout>
+__device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, uint32_t tb,
+                                            int h, int n, int t_begin, int t_end, int nchunks) {
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int c_lane = tid;  // TMEM lane = value channel
+    const uint32_t tl = tb + ((uint32_t)(32 * warp) << 16);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);
+    const float *vec = reinterpret_cast<const float *>(sm + S_VEC);
+    const int H = p.H;
+    const size_t state_off = ((size_t)n * H + h) * (size_t)(kD * kD);
+    Tout *o = static_cast<Tout *>(p.o);
+    uint32_t ph = 0;  // MMA barrier phase (CA and CB)
+    bool alive = true;
+
+    // ---- entering state -> TMEM, transposed (lane c, column j) ----
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16_tmem_a(d, tb + TM_OPS + 8 * (s0 + s), sw128_desc_k(bh, 64, s0 + s), id,
-                                s > 0);
+    for (int part = 0; part < 4; ++part) {
+        uint32_t w[32];
+        const int j0 = 32 * part;
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16_tmem_a(d, tb + TM_OPS + 8 * (s0 + s), sw128_desc_k(bl, 64, s0 + s), id, 1);
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16_tmem_a(d, tb + TM_OPS + 64 + 8 * (s0 + s), sw128_desc_k(bh, 64, s0 + s), id,
-                                1);
-            mma_commit(bar + (tid == kIssuerB));
+        for (int jj = 0; jj < 32; ++jj)
+            w[jj] = p.S0 ? __float_as_uint(p.S0[state_off + (size_t)(j0 + jj) * kD + c_lane]) : 0u;
+        tmem_st32(tl + TM_ST + j0, w);
+    }
+    tmem_wait_st();
+
+    // bf16 output: a finished chunk is staged row-major in shared memory and
+    // copied out with 16-byte stores while the next chunk's M3 runs.
+    __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + S_STG);
+    int pend_t0 = 0, pend_rows = 0;
+    auto copy_out = [&]() {  // warps 2-3 (warps 0-1 issue M3 meanwhile)
+        if (tid < 64) return;
+        for (int e = tid - 64; e < kC * 16; e += 64) {
+            const int r = e >> 4, chn = e & 15;
+            if (r < pend_rows)
+                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(o) +
+                                           ((size_t)(pend_t0 + r) * H + h) * kD + 8 * chn) =
+                    *reinterpret_cast<const uint4 *>(stg + r * kD + 8 * chn);
         }
-        alive = wait_mma(bar, phase, p.status, 3);
-        if (!alive) break;
+        pend_rows = 0;
+    };
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        const int t0 = t_begin + kC * c;
+        const int nrow = min(kC, t_end - t0);
+        const unsigned char *wq = sm + S_WQ + s * WQ_SIZE;
+        const unsigned char *rr = sm + S_R + s * R_SIZE;
+        const unsigned char *pp = sm + S_P + s * P_SIZE;
+
+        // ---- the prep group has filled slot s ----
+        {
+            bool ok = true;
+            if (tid == 0) ok = wait_one(bar + B_FULL + s, (c >> 1) & 1, p.status, 20);
+            alive = group_and(kChainBar, ok);
+            fence_after_sync();
+            if (!alive) break;
+        }
+
+        // ---- F4: S0 = Diag(e31_prev) X -> M3's A operand (hi | lo); X <- Diag(em) S0 ----
+        {
+            const float *em = vec + s * kD, *e31p = vec + 2 * kD + s * kD;
+#pragma unroll
+            for (int part = 0; part < 4; ++part) {
+                const int j0 = 32 * part;
+                float sv[32];
+                tmem_ld32(tl + TM_ST + j0, sv);
+                uint32_t hw[16], lw[16], yv[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 4) {
+                    const float4 ep = *reinterpret_cast<const float4 *>(e31p + j0 + jj);
+                    const float4 mm = *reinterpret_cast<const float4 *>(em + j0 + jj);
+                    const float2 a = mul2(make_float2(sv[jj], sv[jj + 1]), make_float2(ep.x, ep.y));
+                    const float2 b =
+                        mul2(make_float2(sv[jj + 2], sv[jj + 3]), make_float2(ep.z, ep.w));
+                    split2(a.x, a.y, hw[jj >> 1], lw[jj >> 1]);
+                    split2(b.x, b.y, hw[(jj >> 1) + 1], lw[(jj >> 1) + 1]);
+                    const float2 ya = mul2(a, make_float2(mm.x, mm.y));
+                    const float2 yb = mul2(b, make_float2(mm.z, mm.w));
+                    yv[jj] = __float_as_uint(ya.x);
+                    yv[jj + 1] = __float_as_uint(ya.y);
+                    yv[jj + 2] = __float_as_uint(yb.x);
+                    yv[jj + 3] = __float_as_uint(yb.y);
+                }
+                tmem_st16u(tl + TM_OPS + (j0 >> 1), hw);
+                tmem_st16u(tl + TM_OPS + 64 + (j0 >> 1), lw);
+                tmem_st32(tl + TM_ST + j0, yv);
+            }
+        }
+        publish(kChainBar);
+        if (tid == kCA || tid == kCB) {
+            // M3: [(W S0)^T | (Q~ S0)^T] = S0^T [W ; Q~]^T, K steps 0-3 -> D3A, 4-7 -> D3B
+            const uint32_t id = idesc_bf16_f32(128, 64);
+            const int s0 = tid == kCA ? 0 : 4;
+            const uint32_t d = tb + (tid == kCA ? TM_D3A : TM_D3B);
+            const uint32_t bh = smem_u32(wq), bl = bh + 16384;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16_tmem_a(d, tb + TM_OPS + 8 * (s0 + k), sw128_desc_k(bh, 64, s0 + k), id,
+                                k > 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16_tmem_a(d, tb + TM_OPS + 8 * (s0 + k), sw128_desc_k(bl, 64, s0 + k), id, 1);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16_tmem_a(d, tb + TM_OPS + 64 + 8 * (s0 + k), sw128_desc_k(bh, 64, s0 + k),
+                                id, 1);
+            mma_commit(bar + (tid == kCA ? B_CA : B_CB));
+        }
+        if constexpr (sizeof(Tout) == 2) copy_out();  // previous chunk, while M3 runs
+        {
+            bool ok = true;
+            if (tid == kCA || tid == kCB)
+                ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p.status, 21);
+            ++ph;
+            alive = group_and(kChainBar, ok);
+            fence_after_sync();
+            if (!alive) break;
+        }
 
         // ---- F8: U^T = U~^T - (W S0)^T -> A operand of M4 / M5 ----
         {
-            float ut[16], ws[16], ws2[16];
-            tmem_ld16(tl + TM_DU + 16 * half, ut);
-            tmem_ld16(tl + TM_D1 + 16 * half, ws);
-            tmem_ld16(tl + TM_WT + 16 * half, ws2);
+            float ut[32], a[32], b[32];
+            tmem_ld32(tl + TM_UT + 32 * s, ut);
+            tmem_ld32(tl + TM_D3A, a);
+            tmem_ld32(tl + TM_D3B, b);
+            uint32_t hw[16], lw[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) ws[e] += ws2[e];
-            uint32_t hw[8], lw[8];
-#pragma unroll
-            for (int pp = 0; pp < 8; ++pp)
-                split2(ut[2 * pp] - ws[2 * pp], ut[2 * pp + 1] - ws[2 * pp + 1], hw[pp], lw[pp]);
-            tmem_st8u(tl + TM_OPS + 8 * half, hw);
-            tmem_st8u(tl + TM_OPS + 16 + 8 * half, lw);
+            for (int q = 0; q < 16; ++q)
+                split2(ut[2 * q] - (a[2 * q] + b[2 * q]), ut[2 * q + 1] - (a[2 * q + 1] + b[2 * q + 1]),
+                       hw[q], lw[q]);
+            tmem_st16u(tl + TM_OPS, hw);
+            tmem_st16u(tl + TM_OPS + 16, lw);
         }
-        publish_operands();
-        if (tid == kIssuerA) {  // M4: (Q~ S0 + P U)^T += U^T P^T
+        publish(kChainBar);
+        if (tid == kCA) {  // M4: (Q~ S0 + P U)^T += U^T P^T
             const uint32_t id32 = idesc_bf16_f32(128, 32);
-            const uint32_t ph = smem_u32(sm + W_P), pl = ph + 4096;
+            const uint32_t ph2 = smem_u32(pp), pl = ph2 + 4096;
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16_tmem_a(tb + TM_D1 + 32, tb + TM_OPS + 8 * s, sw128_desc_k(ph, 32, s), id32,
-                                1);
+            for (int k = 0; k < 2; ++k)
+                mma_bf16_tmem_a(tb + TM_D3A + 32, tb + TM_OPS + 8 * k, sw128_desc_k(ph2, 32, k), id32, 1);
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16_tmem_a(tb + TM_D1 + 32, tb + TM_OPS + 8 * s, sw128_desc_k(pl, 32, s), id32,
-                                1);
+            for (int k = 0; k < 2; ++k)
+                mma_bf16_tmem_a(tb + TM_D3A + 32, tb + TM_OPS + 8 * k, sw128_desc_k(pl, 32, k), id32, 1);
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16_tmem_a(tb + TM_D1 + 32, tb + TM_OPS + 16 + 8 * s, sw128_desc_k(ph, 32, s),
+            for (int k = 0; k < 2; ++k)
+                mma_bf16_tmem_a(tb + TM_D3A + 32, tb + TM_OPS + 16 + 8 * k, sw128_desc_k(ph2, 32, k),
                                 id32, 1);
-            mma_commit(bar);
-        } else if (tid == kIssuerB) {  // M5: X += U^T (k E^-1)  (the Gram's R tile, read MN-major)
+            mma_commit(bar + B_CA);
+        } else if (tid == kCB) {  // M5: X += U^T (k E^-1)  (R read MN-major)
             const uint32_t id128 = idesc_bf16_f32(128, 128) | kIdescBMN;
-            const uint32_t rh = smem_u32(sm + W_R), rl = rh + 8192;
+            const uint32_t rh = smem_u32(rr), rl = rh + 8192;
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 8 * s, sw128_desc_mn(rh + 2048 * s, 4096),
+            for (int k = 0; k < 2; ++k)
+                mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 8 * k, sw128_desc_mn(rh + 2048 * k, 4096),
                                 id128, 1);
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 8 * s, sw128_desc_mn(rl + 2048 * s, 4096),
+            for (int k = 0; k < 2; ++k)
+                mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 8 * k, sw128_desc_mn(rl + 2048 * k, 4096),
                                 id128, 1);
 #pragma unroll
-            for (int s = 0; s < 2; ++s)
-                mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 16 + 8 * s,
-                                sw128_desc_mn(rh + 2048 * s, 4096), id128, 1);
-            mma_commit(bar + 1);
+            for (int k = 0; k < 2; ++k)
+                mma_bf16_tmem_a(tb + TM_ST, tb + TM_OPS + 16 + 8 * k,
+                                sw128_desc_mn(rh + 2048 * k, 4096), id128, 1);
+            mma_commit(bar + B_CB);
         }
-        alive = wait_mma(bar, phase, p.status, 4);
-        if (!alive) break;
-
-        t0_prev = t0;
-        nrow_prev = nrow;  // read out during the next chunk's solve (or after the loop)
+        // ---- M4 done: read out o = scale (D3A + D3B)[:, 32:64] ----
+        {
+            bool ok = true;
+            if (tid == kCA) ok = wait_one(bar + B_CA, ph & 1, p.status, 22);
+            alive = group_and(kChainBar, ok);
+            fence_after_sync();
+            if (!alive) break;
+        }
+        {
+            float a[32], b[32];
+            tmem_ld32(tl + TM_D3A + 32, a);
+            tmem_ld32(tl + TM_D3B + 32, b);
+            if constexpr (sizeof(Tout) == 2) {
+#pragma unroll
+                for (int r = 0; r < 32; ++r)
+                    stg[r * kD + c_lane] = __float2bfloat16_rn(p.scale * (a[r] + b[r]));
+                pend_t0 = t0;
+                pend_rows = nrow;
+            } else {
+#pragma unroll
+                for (int r = 0; r < 32; ++r)
+                    if (r < nrow) o[((size_t)(t0 + r) * H + h) * kD + c_lane] = p.scale * (a[r] + b[r]);
+            }
+        }
+        // ---- M5 done: slot s can be refilled ----
+        {
+            bool ok = true;
+            if (tid == kCB) ok = wait_one(bar + B_CB, ph & 1, p.status, 23);
+            ++ph;
+            fence_before_sync();
+            alive = group_and(kChainBar, ok);
+            fence_after_sync();
+            if (!alive) break;
+            if (tid == 0) mbar_arrive(bar + B_EMPTY + s);
+        }
+    }
+    if constexpr (sizeof(Tout) == 2) {
+        if (alive) copy_out();
     }
 
-    if (alive && chunk > 0 && half == 1) readout(t0_prev, nrow_prev);  // the last chunk
-    cp_async_wait_all();  // nothing may still be in flight into shared memory on exit
-    if (tid == kTmaThread && !alive) {  // let an outstanding TMA load land before leaving
-        // loads were issued for chunks 0 .. n_issued-1; chunks 0 .. chunk-1 were consumed
-        const int n_issued = (t_end - t_begin + kC - 1) / kC < chunk + 2
-                                 ? (t_end - t_begin + kC - 1) / kC
-                                 : chunk + 2;
-        for (int c = chunk; c < n_issued; ++c)
-            mbar_wait_bounded(tbar + (c & 1), (uint32_t)(c >> 1) & 1u, kWaitNs);
-    }
     // ---- final state S = Diag(e31_last) X (lane c, column j) -> S_final[j][c] ----
     if (alive && p.S_final != nullptr) {
-        const int c = trow;
-        const float *e31_last = vec + 2 * kD + ((chunk - 1) & 1) * kD;  // chunk 0 -> slot 1 = 1
+        const float *e31_last = vec + 4 * kD + ((nchunks - 1) & 1) * kD;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            const int j0 = 64 * half + 32 * part;
+        for (int part = 0; part < 4; ++part) {
+            const int j0 = 32 * part;
             float sv[32];
             tmem_ld32(tl + TM_ST + j0, sv);
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj)
-                p.S_final[state_off + (size_t)(j0 + jj) * kD + c] = sv[jj] * e31_last[j0 + jj];
+                p.S_final[state_off + (size_t)(j0 + jj) * kD + c_lane] =
+                    nchunks > 0 ? sv[jj] * e31_last[j0 + jj] : sv[jj];
         }
     }
+}
+
+template <typename Tout>
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ Params p) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S_TSLOT);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int H = p.H;
+    const int h = blockIdx.x % H, n = blockIdx.x / H;
+    const int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
+    const int nchunks = t_end > t_begin ? (t_end - t_begin + kC - 1) / kC : 0;
+
+    if (warp == 0) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+    }
+    if (tid == kTmaThread) {
+        for (int i = 0; i < kNumBars; ++i) mbar_init(bar + i, 1);
+        fence_mbar_init();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tb = *tslot;
+
+    if (warp >= 4)
+        prep_group(p, sm, tb, h, t_begin, t_end, nchunks);
+    else
+        chain_group<Tout>(p, sm, tb, h, n, t_begin, t_end, nchunks);
+
     fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tb, 512);
@@ -710,14 +910,9 @@ cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
             !encode_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, 64,
                         CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&p.tm_la, a.log_alpha, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T, H, 32,
-                        CU_TENSOR_MAP_SWIZZLE_NONE))
+                        CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
-    p.q = static_cast<const __nv_bfloat16 *>(a.q);
-    p.k = static_cast<const __nv_bfloat16 *>(a.k);
-    p.v = static_cast<const __nv_bfloat16 *>(a.v);
     p.log_alpha = a.log_alpha;
     p.beta = a.beta;
     p.S0 = a.S0;
