@@ -48,9 +48,9 @@
 // (fp32 accumulation); V is exact in bf16 and enters once.
 //
 // Warp roles.  Only M3 .. M5 depend on the state; everything before them
-// depends on the chunk's inputs alone.  Warps 4-7 (the prep group) therefore
-// build chunk c+1's operands (decay, [k E ; q E] and k E^-1, the Gram, the
-// triangular solve, U~ and W') while warps 0-3 (the chain group) run the
+// depends on the chunk's inputs alone.  Warps 4-11 (the prep group) therefore
+// build chunk c+1's operands (decay, [k E ; q E], k E^-1 and Q~, the Gram, the
+// triangular solve, U~ and W) while warps 0-3 (the chain group) run the
 // state-dependent products of chunk c.  The operands of a chunk live in one of
 // two slots (shared-memory tiles, U~ in TMEM); the groups hand slots over with
 // mbarriers ("full" prep -> chain, "empty" chain -> prep), and every wait is
@@ -74,12 +74,13 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // bound on every wait
 // q, k, v tiles (bf16 [32][128], two 64-column blocks with 128-byte swizzle, as
 // written by TMA) for two chunks.  log_alpha travels through registers.
 constexpr uint32_t S_QKV = 0, QKV_SIZE = 24576, QO = 0, KO = 8192, VO = 16384;
-// D (fp32 [32][128], log2 units); once F3 has read it the region holds Tb hi | lo
-// (a 32-row operand tile, K = 32), then A and T (fp32 [32][32], XOR-swizzled rows).
+// Tb hi | lo (a 32-row operand tile, K = 32).  A (fp32 [32][32], column-major)
+// shares Tb's hi half: it is dead once Tb is written.  Then T (fp32 [32][33]).
 constexpr uint32_t S_DT = 2 * QKV_SIZE;
 constexpr uint32_t S_TB = S_DT;
-constexpr uint32_t S_A = S_DT + 8192;
-constexpr uint32_t S_T = S_A + 4096;
+constexpr uint32_t S_A = S_DT;
+constexpr uint32_t S_T = S_DT + 8192;
+constexpr int kLdT = 33;
 // [k E ; q E] hi | lo (64 rows), private to the prep group.
 constexpr uint32_t S_WX = S_DT + 16384;
 // Per slot: [W ; Q~] hi | lo (64 rows), R = k E^-1 hi | lo (32 rows),
@@ -97,11 +98,6 @@ static_assert(SM_DYN <= 232448, "shared memory map exceeds 227 KB");
 // M1 reads 128 rows of the 64-row [k E ; q E] tile (rows 64-127 are ignored):
 // what follows the tile must still be inside the map.
 static_assert(S_WX + 32768 + 8192 <= S_STG, "M1's A view leaves the map");
-
-// A and T: element (r, i) of a [32][32] fp32 matrix.  The column is XOR-ed
-// with r ^ (r >> 3): row-wise writes by 32 threads, the four 8 x 8 diagonal
-// blocks read in parallel, and the Tb pass all hit distinct banks.
-__device__ __forceinline__ int ati(int r, int i) { return r * 32 + ((i ^ r ^ (r >> 3)) & 31); }
 
 // mbarriers (8 bytes each, from S_BAR)
 constexpr int B_TQKV = 0;   // [2] TMA q/k/v by slot
@@ -131,13 +127,6 @@ constexpr int kChainThreads = 128, kPrepThreads = 256;
 __device__ __forceinline__ uint32_t tile_chunk(int rows, int i, int cc) {
     return (uint32_t)((cc >> 3) * rows * 128 + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
 }
-// fp32 [32][128] table with 16-byte chunks permuted per row so that both the
-// row-wise writes (32 consecutive channels) and the reads of chunk pairs
-// (2cc, 2cc+1) by 8 consecutive threads hit 8 distinct bank groups.
-__device__ __forceinline__ uint32_t e_chunk(int r, int q) {  // q = 4-float chunk 0..31
-    return (uint32_t)(r * 512 + (((q ^ ((q >> 3) & 1) ^ r) & 31) << 4));
-}
-
 struct Params {
     CUtensorMap tm_q, tm_k, tm_v;  // [T][H*128] bf16 with boxes of 32 tokens x 64 channels
     const float *log_alpha, *beta, *S0;
@@ -149,15 +138,6 @@ struct Params {
     DeviceStatus status;
 };
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&x)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __uint_as_float(w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-}
-
 // Store 8 fp32 values as a hi 16-byte chunk and a lo 16-byte chunk.
 __device__ __forceinline__ void store_split_chunk(unsigned char *hi, unsigned char *lo,
                                                   const float (&x)[8]) {
@@ -168,15 +148,6 @@ __device__ __forceinline__ void store_split_chunk(unsigned char *hi, unsigned ch
     split2(x[6], x[7], h.w, l.w);
     *reinterpret_cast<uint4 *>(hi) = h;
     *reinterpret_cast<uint4 *>(lo) = l;
-}
-
-__device__ __forceinline__ void mul8(float (&x)[8], const float4 &a, const float4 &b) {
-    const float2 p0 = mul2(make_float2(x[0], x[1]), make_float2(a.x, a.y));
-    const float2 p1 = mul2(make_float2(x[2], x[3]), make_float2(a.z, a.w));
-    const float2 p2 = mul2(make_float2(x[4], x[5]), make_float2(b.x, b.y));
-    const float2 p3 = mul2(make_float2(x[6], x[7]), make_float2(b.z, b.w));
-    x[0] = p0.x; x[1] = p0.y; x[2] = p1.x; x[3] = p1.y;
-    x[4] = p2.x; x[5] = p2.y; x[6] = p3.x; x[7] = p3.y;
 }
 
 // ---- group synchronisation (128-thread named barriers) ----------------------
@@ -271,7 +242,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
     const uint32_t tl = tb + ((uint32_t)(32 * quarter) << 16);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);
     float *vec = reinterpret_cast<float *>(sm + S_VEC);
-    float *sA = reinterpret_cast<float *>(sm + S_A);
+    float *sAt = reinterpret_cast<float *>(sm + S_A);  // A^T: sAt[i * 32 + r] = A[r][i]
     float *sT = reinterpret_cast<float *>(sm + S_T);
     unsigned char *wx = sm + S_WX;
     // Decay pass layout: channels 4 q4 .. 4 q4 + 3, rows 4 rg .. 4 rg + 3; the
@@ -313,8 +284,13 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             consumed = c + 1;
         }
 
-        // ---- F2: D (log2 units); em, e31.  Rows 0..15: D = prefix - prefix_15,
-        //      rows 16..31: D = sum of rows 16..r (two scan segments of 4 row groups) ----
+        if (c + 1 < nchunks)  // stage chunk c+1 into slot s^1 (freed by chunk c-1)
+            issue_loads(p, sm, bar, s ^ 1, t0 + kC, min(kC, t_end - t0 - kC), h, tid);
+
+        // ---- F2/F3: decay and operands, thread = 4 rows x 4 channels (4 q4 .. 4 q4 + 3).
+        //      D (log2 units): rows 0..15 prefix - prefix_15, rows 16..31 the sum of rows
+        //      16..r (two scan segments of 4 row groups).  Then [k E ; q E] -> wx,
+        //      R = k E^-1 -> rr, Q~ = q E em -> wq rows 32.. ----
         {
             const float kL2E = 1.4426950408889634f;
             float4 pre[4];
@@ -354,67 +330,65 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             base.y = incl.y - acc.y - (rg < 4 ? mid.y : 0.f);
             base.z = incl.z - acc.z - (rg < 4 ? mid.z : 0.f);
             base.w = incl.w - acc.w - (rg < 4 ? mid.w : 0.f);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 dk = make_float4(base.x + pre[k].x, base.y + pre[k].y,
-                                              base.z + pre[k].z, base.w + pre[k].w);
-                *reinterpret_cast<float4 *>(sm + S_DT + e_chunk(4 * rg + k, q4)) = dk;
-            }
+            const float em4[4] = {ex2_approx(mid.x), ex2_approx(mid.y), ex2_approx(mid.z),
+                                  ex2_approx(mid.w)};
             if (rg == 0) {
-                const float4 em = make_float4(ex2_approx(mid.x), ex2_approx(mid.y),
-                                              ex2_approx(mid.z), ex2_approx(mid.w));
                 const float4 e31 = make_float4(ex2_approx(last.x), ex2_approx(last.y),
                                                ex2_approx(last.z), ex2_approx(last.w));
-                *reinterpret_cast<float4 *>(em_s + 4 * q4) = em;
+                *reinterpret_cast<float4 *>(em_s + 4 * q4) =
+                    make_float4(em4[0], em4[1], em4[2], em4[3]);
                 *reinterpret_cast<float4 *>(e31p_s + 4 * q4) = e31_prev;
                 *reinterpret_cast<float4 *>(e31_s + 4 * q4) = e31;
                 e31_prev = e31;
             }
-        }
-        if (c + 1 < nchunks) {  // stage chunk c+1 (its q/k/v slot was freed by chunk c-1)
-            const int n1 = min(kC, t_end - t0 - kC);
-            load_log_alpha(p, t0 + kC, n1, h, q4, rg, la);
-            group_sync(kPrepBar);  // D and em complete
-            issue_loads(p, sm, bar, s ^ 1, t0 + kC, n1, h, tid);
-        } else {
-            group_sync(kPrepBar);  // D and em complete
-        }
-
-        // ---- F3: [k E ; q E] -> wx, R = k E^-1 -> rr, Q~ = q E em -> wq rows 32.. ----
-#pragma unroll 1
-        for (int m = 0; m < 2; ++m) {
-            const int e = pt + 256 * m;  // row i, chunk cc
-            const int i = e >> 4, cc = e & 15;
-            float xk[8], xq[8], d8[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(qkv + KO + tile_chunk(32, i, cc)), xk);
-            bf16x8_to_f32(*reinterpret_cast<const uint4 *>(qkv + QO + tile_chunk(32, i, cc)), xq);
-            {
-                const float4 d0 = *reinterpret_cast<const float4 *>(sm + S_DT + e_chunk(i, 2 * cc));
-                const float4 d1 =
-                    *reinterpret_cast<const float4 *>(sm + S_DT + e_chunk(i, 2 * cc + 1));
-                d8[0] = d0.x; d8[1] = d0.y; d8[2] = d0.z; d8[3] = d0.w;
-                d8[4] = d1.x; d8[5] = d1.y; d8[6] = d1.z; d8[7] = d1.w;
-            }
-            float r8[8];
+            // Row order rotated by rg >> 1 so that the 8 rows a warp stores at once sit
+            // in 8 distinct swizzle positions.
+            const int cc = q4 >> 1, hb = (q4 & 1) * 8;
 #pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const float E = ex2_approx(d8[t]), EI = ex2_approx(-d8[t]);
-                r8[t] = xk[t] * EI;  // k E^-1
-                xk[t] *= E;          // k E
-                xq[t] *= E;          // q E
+            for (int k = 0; k < 4; ++k) {
+                const int kk = (k + (rg >> 1)) & 3;
+                const int r = 4 * rg + kk;
+                const float4 pk = kk == 0 ? pre[0] : kk == 1 ? pre[1] : kk == 2 ? pre[2] : pre[3];
+                const float dv[4] = {base.x + pk.x, base.y + pk.y, base.z + pk.z, base.w + pk.w};
+                const uint2 kw = *reinterpret_cast<const uint2 *>(qkv + KO + tile_chunk(32, r, cc) + hb);
+                const uint2 qw = *reinterpret_cast<const uint2 *>(qkv + QO + tile_chunk(32, r, cc) + hb);
+                const float kv[4] = {__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
+                                     __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u)};
+                const float qv[4] = {__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u),
+                                     __uint_as_float(qw.y << 16), __uint_as_float(qw.y & 0xFFFF0000u)};
+                float xk[4], xq[4], xr[4], xt[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float E = ex2_approx(dv[t]), EI = ex2_approx(-dv[t]);
+                    xk[t] = kv[t] * E;    // k E
+                    xq[t] = qv[t] * E;    // q E
+                    xr[t] = kv[t] * EI;   // k E^-1
+                    xt[t] = xq[t] * em4[t];  // Q~ = q E em
+                }
+                uint2 h2, l2;
+                split2(xk[0], xk[1], h2.x, l2.x);
+                split2(xk[2], xk[3], h2.y, l2.y);
+                unsigned char *dst = wx + tile_chunk(64, r, cc) + hb;
+                *reinterpret_cast<uint2 *>(dst) = h2;
+                *reinterpret_cast<uint2 *>(dst + 16384) = l2;
+                split2(xq[0], xq[1], h2.x, l2.x);
+                split2(xq[2], xq[3], h2.y, l2.y);
+                dst = wx + tile_chunk(64, 32 + r, cc) + hb;
+                *reinterpret_cast<uint2 *>(dst) = h2;
+                *reinterpret_cast<uint2 *>(dst + 16384) = l2;
+                split2(xr[0], xr[1], h2.x, l2.x);
+                split2(xr[2], xr[3], h2.y, l2.y);
+                dst = rr + tile_chunk(32, r, cc) + hb;
+                *reinterpret_cast<uint2 *>(dst) = h2;
+                *reinterpret_cast<uint2 *>(dst + 8192) = l2;
+                split2(xt[0], xt[1], h2.x, l2.x);
+                split2(xt[2], xt[3], h2.y, l2.y);
+                dst = wq + tile_chunk(64, 32 + r, cc) + hb;
+                *reinterpret_cast<uint2 *>(dst) = h2;
+                *reinterpret_cast<uint2 *>(dst + 16384) = l2;
             }
-            unsigned char *xh = wx + tile_chunk(64, i, cc);
-            store_split_chunk(xh, xh + 16384, xk);
-            xh = wx + tile_chunk(64, 32 + i, cc);
-            store_split_chunk(xh, xh + 16384, xq);
-            unsigned char *rh = rr + tile_chunk(32, i, cc);
-            store_split_chunk(rh, rh + 8192, r8);
-            const float4 m0 = *reinterpret_cast<const float4 *>(em_s + 8 * cc);
-            const float4 m1 = *reinterpret_cast<const float4 *>(em_s + 8 * cc + 4);
-            mul8(xq, m0, m1);  // Q~ = q E em
-            unsigned char *qh = wq + tile_chunk(64, 32 + i, cc);
-            store_split_chunk(qh, qh + 16384, xq);
         }
+        if (c + 1 < nchunks) load_log_alpha(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, la);
         publish(kPrepBar);
         if (tid == kPA || tid == kPB) {  // M1: Gram, K steps split over the two issuers
             const uint32_t id = idesc_bf16_f32(128, 32);
@@ -443,8 +417,9 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             if (!alive) break;
         }
 
-        // ---- F5: A (k rows, scaled by beta, strictly lower) and P (q rows, lower);
-        //      lanes 0-63, each of the two warps of a lane quarter takes 16 columns ----
+        // ---- F5: A (k rows, scaled by beta, strictly lower; stored column-major) and
+        //      P (q rows, lower); lanes 0-63, each of the two warps of a lane quarter
+        //      takes 16 columns ----
         if (quarter < 2) {
             float g[16], g2[16];
             tmem_ld16(tl + TM_DG + 16 * half, g);
@@ -455,7 +430,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int i = 16 * half + e;
-                    sA[ati(r, i)] = i < r ? br * (g[e] + g2[e]) : 0.f;
+                    sAt[i * 32 + r] = i < r ? br * (g[e] + g2[e]) : 0.f;
                 }
             } else {
 #pragma unroll
@@ -473,56 +448,48 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         }
         group_sync(kPrepBar);
 
-        // ---- F6: T = (I + A)^-1 by 8 x 8 diagonal blocks, then 16 x 16, then 32 x 32;
+        // ---- F6: T = (I + A)^-1.  One warp inverts both 16 x 16 diagonal blocks by
+        //      forward substitution (lane = column: lanes 0-15 the upper block, 16-31 the
+        //      lower), then T_10 = -T_11 (A_10 T_00) with one entry per thread, then
         //      Tb = T diag(beta) ----
-        if (pt < 32) {  // the four 8 x 8 diagonal blocks, one column per thread
-            const int o = 8 * (pt >> 3), jj = pt & 7;
-            float x[8];
+        if (pt < 32) {
+            const int o = 16 * (lane >> 4), j = lane & 15;
+            float x[16];
 #pragma unroll
-            for (int m = 0; m < 8; ++m) x[m] = m == jj ? 1.f : 0.f;
+            for (int m = 0; m < 16; ++m) x[m] = m == j ? 1.f : 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 15; ++i) {
+                float a[16];  // column o + i of A, rows o .. o + 15
 #pragma unroll
-                for (int m = i + 1; m < 8; ++m) x[m] = fmaf(-sA[ati(o + m, o + i)], x[i], x[m]);
+                for (int q = (i + 1) >> 2; q < 4; ++q) {
+                    const float4 v = *reinterpret_cast<const float4 *>(sAt + (o + i) * 32 + o + 4 * q);
+                    a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+                }
 #pragma unroll
-            for (int m = 0; m < 8; ++m) sT[ati(o + m, o + jj)] = x[m];
+                for (int m = i + 1; m < 16; ++m) x[m] = fmaf(-a[m], x[i], x[m]);
+            }
+#pragma unroll
+            for (int m = 0; m < 16; ++m) sT[(o + m) * kLdT + o + j] = x[m];
         }
         group_sync(kPrepBar);
-        {  // 16 x 16 diagonal blocks: T_10 = -T_11 (A_10 T_00) on 8 x 8 sub-blocks
-            const bool act = pt < 128;
-            const int o = 16 * ((pt >> 6) & 1), r = (pt >> 3) & 7, i = pt & 7;
-            float x = 0.f;
-            if (act) {
-#pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    x = fmaf(sA[ati(o + 8 + r, o + m)], sT[ati(o + m, o + i)], x);
-            }
-            if (act) sT[ati(o + r, o + 8 + i)] = 0.f;  // upper block, read by the 32 x 32 step
-            group_sync(kPrepBar);
-            if (act) sT[ati(o + 8 + r, o + i)] = x;  // X = A_10 T_00 in the T_10 slot
-            group_sync(kPrepBar);
-            float y = 0.f;
-            if (act) {
-#pragma unroll
-                for (int m = 0; m < 8; ++m)
-                    y = fmaf(sT[ati(o + 8 + r, o + 8 + m)], sT[ati(o + 8 + m, o + i)], y);
-            }
-            group_sync(kPrepBar);
-            if (act) sT[ati(o + 8 + r, o + i)] = -y;
-        }
-        group_sync(kPrepBar);
-        {  // 32 x 32: T_10 = -T_11 (A_10 T_00) on 16 x 16 blocks, one entry per thread
+        {  // 32 x 32: T_10 = -T_11 (A_10 T_00), one entry per thread (row 16 + r, column i)
             const int r = pt >> 4, i = pt & 15;
-            float x = 0.f;
+            float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) x = fmaf(sA[ati(16 + r, m)], sT[ati(m, i)], x);
-            sT[ati(16 + r, i)] = x;  // the T_10 block was never written before
+            for (int m = 0; m < 16; m += 2) {
+                x0 = fmaf(sAt[m * 32 + 16 + r], sT[m * kLdT + i], x0);
+                x1 = fmaf(sAt[(m + 1) * 32 + 16 + r], sT[(m + 1) * kLdT + i], x1);
+            }
+            sT[(16 + r) * kLdT + i] = x0 + x1;  // X = A_10 T_00 in the T_10 slot
             group_sync(kPrepBar);
-            float y = 0.f;
+            float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) y = fmaf(sT[ati(16 + r, 16 + m)], sT[ati(16 + m, i)], y);
+            for (int m = 0; m < 16; m += 2) {
+                y0 = fmaf(sT[(16 + r) * kLdT + 16 + m], sT[(16 + m) * kLdT + i], y0);
+                y1 = fmaf(sT[(16 + r) * kLdT + 17 + m], sT[(17 + m) * kLdT + i], y1);
+            }
             group_sync(kPrepBar);
-            sT[ati(16 + r, i)] = -y;
+            sT[(16 + r) * kLdT + i] = -(y0 + y1);
         }
         group_sync(kPrepBar);
         if (pt < 128) {  // Tb (32 rows x K 32): one 16-byte chunk per thread
@@ -531,7 +498,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const int i = 8 * cc + e;
-                x[e] = i <= r ? sT[ati(r, i)] * beta_s[i] : 0.f;
+                x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
             }
             unsigned char *th = sm + S_TB + sw128_chunk_offset(32, r, cc);
             store_split_chunk(th, th + 4096, x);
@@ -777,13 +744,17 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                                 sw128_desc_mn(rh + 2048 * k, 4096), id128, 1);
             mma_commit(bar + B_CB);
         }
-        // ---- M4 done: read out o = scale (D3A + D3B)[:, 32:64] ----
+        // ---- M4 and M5 done: hand slot s back, then read out o = scale (D3A + D3B)[:, 32:64] ----
         {
             bool ok = true;
-            if (tid == kCA) ok = wait_one(bar + B_CA, ph & 1, p.status, 22);
+            if (tid == kCA || tid == kCB)
+                ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p.status, 22);
+            ++ph;
+            fence_before_sync();
             alive = group_and(kChainBar, ok);
             fence_after_sync();
             if (!alive) break;
+            if (tid == 0) mbar_arrive(bar + B_EMPTY + s);
         }
         {
             float a[32], b[32];
@@ -800,17 +771,6 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                 for (int r = 0; r < 32; ++r)
                     if (r < nrow) o[((size_t)(t0 + r) * H + h) * kD + c_lane] = p.scale * (a[r] + b[r]);
             }
-        }
-        // ---- M5 done: slot s can be refilled ----
-        {
-            bool ok = true;
-            if (tid == kCB) ok = wait_one(bar + B_CB, ph & 1, p.status, 23);
-            ++ph;
-            fence_before_sync();
-            alive = group_and(kChainBar, ok);
-            fence_after_sync();
-            if (!alive) break;
-            if (tid == 0) mbar_arrive(bar + B_EMPTY + s);
         }
     }
     if constexpr (sizeof(Tout) == 2) {
