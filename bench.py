@@ -32,13 +32,40 @@ import torch  # noqa: E402
 METRIC = "KDA prefill tokens/s (% bf16 TC peak); decode tokens/s (% HBM GB/s)"
 UNIT = "tokens/s"
 D = 128
-# Algorithmic cost per (token, head) at chunk 64, d = 128 (bf16 q/k/v/o, fp32 log_alpha, beta):
+# Algorithmic cost per (token, head), d = 128 (bf16 q/k/v/o, fp32 log_alpha, beta); the FLOP
+# count is the chunked form's at chunk 64 (the figure the roofline targets are quoted at):
 PREFILL_BYTES_PER_TOKEN_HEAD = 3 * D * 2 + D * 4 + 4 + D * 2          # 1540 B
 PREFILL_FLOP_PER_TOKEN_HEAD = 2 * (3 * D * D + 2.5 * 64 * D)          # 139,264 FLOP
 STATE_BYTES = D * D * 4                                               # 64 KiB per (seq, head)
 # Decode, per (request, head): state read + write, q/k/v bf16, log_alpha fp32, beta, o bf16
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * D * 2 + D * 4 + 4 + D * 2  # 132,612 B
 DECODE_FLOP_PER_UNIT = 2 * 4 * D * D
+
+
+# DRAM traffic per unit (token-head for the prefill, request-head for decode) from the
+# committed ncu captures (profiles/prefill_tc_kernel_T2048_H96.md, profiles/decode_kernel_B32_H96.md),
+# taken on a smaller case and scaled by units.  Valid only for the kernel source the capture
+# was taken on: a changed kernel reports traffic null until it is captured again.
+TRAFFIC = {
+    "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
+                "13d81302384eda6d23b6768243c093f1de5ee19aaf41f4412476cdf437a8c986",
+                (252.565504e6 + 37.732608e6) / (2048 * 96)),
+    "decode": ("gated_delta_rule_kda_gb300/csrc/kda_decode.cu",
+               "1bf0e4585307540aec99de0bebe444ea914f399db22eb7540d6128919bfb40b0",
+               (205.3e6 + 142.4e6) / (32 * 96)),
+}
+
+
+def traffic_bytes(kind, units):
+    import hashlib
+    path, digest, per_unit = TRAFFIC[kind]
+    try:
+        with open(os.path.join(ROOT, path), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    except OSError:
+        return None
+    return per_unit * units
 
 
 def peaks():
@@ -200,7 +227,8 @@ def run_reference(args, world, rank):
 
 
 def workload_config(n):
-    return {"workload": "KDA prefill B=1 H=96 T=8192 d=128 bf16 (chunk 64), S0=0, "
+    return {"workload": "KDA prefill B=1 H=96 T=8192 d=128 bf16 (kernel chunk 32; the result "
+                        "does not depend on the chunk size), S0=0, "
                         "bf16 o + fp32 S_final", "global_batch": n, "seq_len": 8192,
             "heads": 96, "head_dim": 128, "parallelism": f"replicas x{n}",
             "l2": "inputs larger than L2 (1.2 GB per step), no flush",
@@ -235,7 +263,8 @@ def run_ours(args, world, rank, local):
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
     tflops = alg_flop / (launch_ms / 1e3) / 1e12
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None, "peak_kind": peak_kind,
+                "frac": achieved / hbm, "traffic": traffic_bytes("prefill", T * H),
+                "peak_kind": peak_kind,
                 "kernel": "kda_prefill", "tc_achieved_tflops": tflops, "tc_peak_tflops": tc,
                 "tc_frac": tflops / tc,
                 "binding_roofline_frac": max(alg_bytes / (hbm * 1e9),
@@ -280,7 +309,8 @@ def run_ours(args, world, rank, local):
     d_ach = d_bytes / (d_launch / 1e3) / 1e9
     decode = {"tokens_per_s": world * 256 / (d_ms / 1e3), "ms_per_step": d_ms,
               "roofline": {"bound": "hbm", "achieved": d_ach, "peak": hbm, "unit": "GB/s",
-                           "frac": d_ach / hbm, "traffic": None, "peak_kind": peak_kind,
+                           "frac": d_ach / hbm, "traffic": traffic_bytes("decode", units),
+                           "peak_kind": peak_kind,
                            "kernel": "kda_decode_step"}}
     del dinp, od
     torch.cuda.empty_cache()
