@@ -74,17 +74,19 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // bound on every wait
 // q, k, v tiles (bf16 [32][128], two 64-column blocks with 128-byte swizzle, as
 // written by TMA) for two chunks.  log_alpha travels through registers.
 constexpr uint32_t S_QKV = 0, QKV_SIZE = 24576, QO = 0, KO = 8192, VO = 16384;
-// Tb hi | lo (a 32-row operand tile, K = 32).  A (fp32 [32][32], column-major)
-// shares Tb's hi half: it is dead once Tb is written.  Then T (fp32 [32][33]).
+// Tb hi | lo (a 32-row operand tile, K = 32), built and used by the chain group;
+// A (fp32 [32][32], column-major) for the prep group's solve; T by slot
+// (fp32 [32][33]), written by the solve and read by the chain group.
 constexpr uint32_t S_DT = 2 * QKV_SIZE;
 constexpr uint32_t S_TB = S_DT;
-constexpr uint32_t S_A = S_DT;
-constexpr uint32_t S_T = S_DT + 8192;
+constexpr uint32_t S_A = S_DT + 8192;
+constexpr uint32_t S_TS = S_DT + 12288;
 constexpr int kLdT = 33;
+constexpr uint32_t T_SIZE = 32 * kLdT * 4;
 // [k E ; q E] hi | lo (64 rows), private to the prep group.
-constexpr uint32_t S_WX = S_DT + 16384;
-// Per slot: [W ; Q~] hi | lo (64 rows), R = k E^-1 hi | lo (32 rows),
-// P hi | lo (32 rows, K = 32).
+constexpr uint32_t S_WX = (S_TS + 2 * T_SIZE + 1023) & ~1023u;
+// Per slot: [W ; Q~] hi | lo (64 rows; rows 0-31 hold k E until W replaces it),
+// R = k E^-1 hi | lo (32 rows), P hi | lo (32 rows, K = 32).
 constexpr uint32_t S_WQ = S_WX + 32768, WQ_SIZE = 32768;
 constexpr uint32_t S_R = S_WQ + 2 * WQ_SIZE, R_SIZE = 16384;
 constexpr uint32_t S_P = S_R + 2 * R_SIZE, P_SIZE = 8192;
@@ -104,16 +106,18 @@ constexpr int B_TQKV = 0;   // [2] TMA q/k/v by slot
 constexpr int B_CA = 2, B_CB = 3, B_PA = 4, B_PB = 5;  // MMA completion, one per issuer
 constexpr int B_FULL = 6;   // [2] prep -> chain: slot holds a chunk's operands
 constexpr int B_EMPTY = 8;  // [2] chain -> prep: slot consumed
-constexpr int kNumBars = 10;
+constexpr int B_VFREE = 10; // [2] chain -> prep: the slot's v tile and beta were consumed (M2, Tb)
+constexpr int kNumBars = 12;
 
 // ---- TMEM column map (512 columns) -----------------------------------------
 constexpr uint32_t TM_ST = 0;    // state X^T (lane c, column j), fp32
 constexpr uint32_t TM_OPS = 128; // M3's A operand S0^T hi (64) | lo (64); then U^T hi (16) | lo (16)
 constexpr uint32_t TM_D3A = 256; // M3, K steps 0-3: [(W S0)^T | (Q~ S0)^T (+ M4)]
 constexpr uint32_t TM_D3B = 320; // M3, K steps 4-7
-constexpr uint32_t TM_DG = 384;  // Gram, K steps 0-3; then W'^T (lane j, column r)
+constexpr uint32_t TM_DG = 384;  // Gram, K steps 0-3
 constexpr uint32_t TM_DU = 416;  // Gram, K steps 4-7
-constexpr uint32_t TM_UT = 448;  // U~^T by slot (32 columns each)
+constexpr uint32_t TM_UT = 448;  // U~^T (32 columns)
+constexpr uint32_t TM_WT = 480;  // W'^T (lane = key channel j, column = row r)
 
 // Threads with a fixed job.
 constexpr int kCA = 0, kCB = 32;            // chain-group MMA issuers
@@ -243,7 +247,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);
     float *vec = reinterpret_cast<float *>(sm + S_VEC);
     float *sAt = reinterpret_cast<float *>(sm + S_A);  // A^T: sAt[i * 32 + r] = A[r][i]
-    float *sT = reinterpret_cast<float *>(sm + S_T);
+    float *sT_base = reinterpret_cast<float *>(sm + S_TS);
     unsigned char *wx = sm + S_WX;
     // Decay pass layout: channels 4 q4 .. 4 q4 + 3, rows 4 rg .. 4 rg + 3; the
     // eight row groups of a channel quad sit in lanes (lane & 3) + 4 rg of a warp.
@@ -251,12 +255,14 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
     float4 e31_prev = make_float4(1.f, 1.f, 1.f, 1.f);  // 1: the entering state is exact
     uint32_t ph = 0;   // MMA barrier phase (PA and PB)
     int consumed = 0;  // chunks whose q/k/v were waited for
+    int issued = 0;    // chunks whose q/k/v loads were issued
     bool alive = true;
     float4 la[4];      // log_alpha of the next chunk (this thread's 4 rows x 4 channels)
 
     if (nchunks > 0) {
         const int n0 = min(kC, t_end - t_begin);
         issue_loads(p, sm, bar, 0, t_begin, n0, h, tid);
+        issued = 1;
         load_log_alpha(p, t_begin, n0, h, q4, rg, la);
     }
 
@@ -270,6 +276,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         unsigned char *rr = sm + S_R + s * R_SIZE;
         unsigned char *pp = sm + S_P + s * P_SIZE;
         float *em_s = vec + s * kD, *e31p_s = vec + 2 * kD + s * kD, *e31_s = vec + 4 * kD + s * kD;
+        float *sT = sT_base + s * (32 * kLdT);
 
         // ---- slot s free again (chunk c-2 finished); chunk c's inputs landed ----
         {
@@ -284,13 +291,10 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             consumed = c + 1;
         }
 
-        if (c + 1 < nchunks)  // stage chunk c+1 into slot s^1 (freed by chunk c-1)
-            issue_loads(p, sm, bar, s ^ 1, t0 + kC, min(kC, t_end - t0 - kC), h, tid);
-
         // ---- F2/F3: decay and operands, thread = 4 rows x 4 channels (4 q4 .. 4 q4 + 3).
         //      D (log2 units): rows 0..15 prefix - prefix_15, rows 16..31 the sum of rows
         //      16..r (two scan segments of 4 row groups).  Then [k E ; q E] -> wx,
-        //      R = k E^-1 -> rr, Q~ = q E em -> wq rows 32.. ----
+        //      (and wq rows 0..31), R = k E^-1 -> rr, Q~ = q E em -> wq rows 32.. ----
         {
             const float kL2E = 1.4426950408889634f;
             float4 pre[4];
@@ -371,6 +375,9 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 unsigned char *dst = wx + tile_chunk(64, r, cc) + hb;
                 *reinterpret_cast<uint2 *>(dst) = h2;
                 *reinterpret_cast<uint2 *>(dst + 16384) = l2;
+                dst = wq + tile_chunk(64, r, cc) + hb;  // k E for M2b, until W replaces it
+                *reinterpret_cast<uint2 *>(dst) = h2;
+                *reinterpret_cast<uint2 *>(dst + 16384) = l2;
                 split2(xq[0], xq[1], h2.x, l2.x);
                 split2(xq[2], xq[3], h2.y, l2.y);
                 dst = wx + tile_chunk(64, 32 + r, cc) + hb;
@@ -390,6 +397,15 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         }
         if (c + 1 < nchunks) load_log_alpha(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, la);
         publish(kPrepBar);
+        if (c + 1 < nchunks) {  // stage chunk c+1 into slot s^1 once chunk c-1 no longer needs it
+            bool ok = true;
+            if (tid == kTmaThread && c >= 1)
+                ok = wait_one(bar + B_VFREE + (s ^ 1), ((c - 1) >> 1) & 1, p.status, 12);
+            alive = group_and(kPrepBar, ok);
+            if (!alive) break;
+            issue_loads(p, sm, bar, s ^ 1, t0 + kC, min(kC, t_end - t0 - kC), h, tid);
+            issued = c + 2;
+        }
         if (tid == kPA || tid == kPB) {  // M1: Gram, K steps split over the two issuers
             const uint32_t id = idesc_bf16_f32(128, 32);
             const int s0 = tid == kPA ? 0 : 4;
@@ -451,7 +467,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         // ---- F6: T = (I + A)^-1.  One warp inverts both 16 x 16 diagonal blocks by
         //      forward substitution (lane = column: lanes 0-15 the upper block, 16-31 the
         //      lower), then T_10 = -T_11 (A_10 T_00) with one entry per thread, then
-        //      Tb = T diag(beta) ----
+        //      T goes to slot s for the chain group ----
         if (pt < 32) {
             const int o = 16 * (lane >> 4), j = lane & 15;
             float x[16];
@@ -491,85 +507,13 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             group_sync(kPrepBar);
             sT[(16 + r) * kLdT + i] = -(y0 + y1);
         }
+        fence_proxy_async_smem();  // P (written after the last publish) is an MMA operand
         group_sync(kPrepBar);
-        if (pt < 128) {  // Tb (32 rows x K 32): one 16-byte chunk per thread
-            const int r = pt >> 2, cc = pt & 3;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = 8 * cc + e;
-                x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
-            }
-            unsigned char *th = sm + S_TB + sw128_chunk_offset(32, r, cc);
-            store_split_chunk(th, th + 4096, x);
-        }
-        publish(kPrepBar);
-        if (tid == kPA) {  // M2: U~^T = V^T Tb^T  (V exact in bf16, read MN-major) -> slot s
-            const uint32_t th = smem_u32(sm + S_TB), tlo = th + 4096;
-            const uint32_t idv = idesc_bf16_f32(128, 32) | kIdescAMN;
-            const uint32_t va = smem_u32(qkv + VO);
-            const uint32_t d = tb + TM_UT + 32 * s;
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-                mma_bf16(d, sw128_desc_mn(va + 2048 * k, 4096), sw128_desc_k(th, 32, k), idv, k > 0);
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-                mma_bf16(d, sw128_desc_mn(va + 2048 * k, 4096), sw128_desc_k(tlo, 32, k), idv, 1);
-            mma_commit(bar + B_PA);
-        } else if (tid == kPB) {  // M2b: W'^T = (k E)^T Tb^T, k E read MN-major -> DG
-            const uint32_t th = smem_u32(sm + S_TB), tlo = th + 4096;
-            const uint32_t idw = idesc_bf16_f32(128, 32) | kIdescAMN;
-            const uint32_t xh = smem_u32(wx), xl = xh + 16384;
-            const uint32_t d = tb + TM_DG;
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-                mma_bf16(d, sw128_desc_mn(xh + 2048 * k, 8192), sw128_desc_k(th, 32, k), idw, k > 0);
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-                mma_bf16(d, sw128_desc_mn(xh + 2048 * k, 8192), sw128_desc_k(tlo, 32, k), idw, 1);
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-                mma_bf16(d, sw128_desc_mn(xl + 2048 * k, 8192), sw128_desc_k(th, 32, k), idw, 1);
-            mma_commit(bar + B_PB);
-        }
-        {
-            bool ok = true;
-            if (tid == kPA || tid == kPB)
-                ok = wait_one(bar + (tid == kPA ? B_PA : B_PB), ph & 1, p.status, 14);
-            ++ph;
-            alive = group_and(kPrepBar, ok);
-            fence_after_sync();
-            if (!alive) break;
-        }
-
-        // ---- F7: W = W' Diag(em) -> rows 0..31 of wq; thread = key channel j, 16 rows ----
-        {
-            const int j = pt & 127, r0 = 16 * half;
-            float w[16];
-            tmem_ld16(tl + TM_DG + r0, w);
-            const float emj = em_s[j];
-            const uint32_t cbase = (uint32_t)((j >> 6) * 64 * 128 + ((j & 7) << 1));
-            const int jc = (j & 63) >> 3;
-#pragma unroll
-            for (int rr2 = 0; rr2 < 16; rr2 += 2) {
-                const int r = r0 + rr2;
-                uint32_t hw, lw;
-                split2(w[rr2] * emj, w[rr2 + 1] * emj, hw, lw);
-                const uint32_t o0 = cbase + r * 128 + ((jc ^ (r & 7)) << 4);
-                const uint32_t o1 = cbase + (r + 1) * 128 + ((jc ^ ((r + 1) & 7)) << 4);
-                *reinterpret_cast<uint16_t *>(wq + o0) = (uint16_t)(hw & 0xFFFFu);
-                *reinterpret_cast<uint16_t *>(wq + o1) = (uint16_t)(hw >> 16);
-                *reinterpret_cast<uint16_t *>(wq + 16384 + o0) = (uint16_t)(lw & 0xFFFFu);
-                *reinterpret_cast<uint16_t *>(wq + 16384 + o1) = (uint16_t)(lw >> 16);
-            }
-        }
-        publish(kPrepBar);  // also orders M2's U~ (TMEM) before the hand-over
         if (tid == kPA) mbar_arrive(bar + B_FULL + s);
     }
 
     if (pt < kC) cp_async_wait_all();  // nothing may still be in flight into shared memory
     if (!alive && tid == kTmaThread) {  // let outstanding TMA loads land before leaving
-        const int issued = min(nchunks, consumed + 1);
         for (int c = consumed; c < issued; ++c)
             mbar_wait_bounded(bar + B_TQKV + (c & 1), (c >> 1) & 1, kWaitNs);
     }
@@ -624,9 +568,13 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
         const int s = c & 1;
         const int t0 = t_begin + kC * c;
         const int nrow = min(kC, t_end - t0);
-        const unsigned char *wq = sm + S_WQ + s * WQ_SIZE;
+        unsigned char *wq = sm + S_WQ + s * WQ_SIZE;
         const unsigned char *rr = sm + S_R + s * R_SIZE;
         const unsigned char *pp = sm + S_P + s * P_SIZE;
+        const unsigned char *qkv = sm + S_QKV + s * QKV_SIZE;
+        const float *beta_s = reinterpret_cast<const float *>(sm + S_BETA + 128 * s);
+        const float *sT = reinterpret_cast<const float *>(sm + S_TS + s * T_SIZE);
+        const float *em = vec + s * kD;
 
         // ---- the prep group has filled slot s ----
         {
@@ -637,9 +585,52 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             if (!alive) break;
         }
 
-        // ---- F4: S0 = Diag(e31_prev) X -> M3's A operand (hi | lo); X <- Diag(em) S0 ----
+        // ---- Tb = T diag(beta) (32 rows x K 32): one 16-byte chunk per thread ----
         {
-            const float *em = vec + s * kD, *e31p = vec + 2 * kD + s * kD;
+            const int r = tid >> 2, cc = tid & 3;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int i = 8 * cc + e;
+                x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
+            }
+            unsigned char *th = sm + S_TB + sw128_chunk_offset(32, r, cc);
+            store_split_chunk(th, th + 4096, x);
+        }
+        publish(kChainBar);
+        if (tid == kCA) {  // M2: U~^T = V^T Tb^T  (V exact in bf16, read MN-major)
+            const uint32_t th = smem_u32(sm + S_TB), tlo = th + 4096;
+            const uint32_t idv = idesc_bf16_f32(128, 32) | kIdescAMN;
+            const uint32_t va = smem_u32(qkv + VO);
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                mma_bf16(tb + TM_UT, sw128_desc_mn(va + 2048 * k, 4096), sw128_desc_k(th, 32, k), idv,
+                         k > 0);
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                mma_bf16(tb + TM_UT, sw128_desc_mn(va + 2048 * k, 4096), sw128_desc_k(tlo, 32, k), idv, 1);
+            mma_commit(bar + B_CA);
+        } else if (tid == kCB) {  // M2b: W'^T = (k E)^T Tb^T, k E (wq rows 0-31) read MN-major
+            const uint32_t th = smem_u32(sm + S_TB), tlo = th + 4096;
+            const uint32_t idw = idesc_bf16_f32(128, 32) | kIdescAMN;
+            const uint32_t xh = smem_u32(wq), xl = xh + 16384;
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                mma_bf16(tb + TM_WT, sw128_desc_mn(xh + 2048 * k, 8192), sw128_desc_k(th, 32, k), idw,
+                         k > 0);
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                mma_bf16(tb + TM_WT, sw128_desc_mn(xh + 2048 * k, 8192), sw128_desc_k(tlo, 32, k), idw, 1);
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                mma_bf16(tb + TM_WT, sw128_desc_mn(xl + 2048 * k, 8192), sw128_desc_k(th, 32, k), idw, 1);
+            mma_commit(bar + B_CB);
+        }
+
+        // ---- F4 (while M2 and M2b run): S0 = Diag(e31_prev) X -> M3's A operand (hi | lo);
+        //      X <- Diag(em) S0 ----
+        {
+            const float *e31p = vec + 2 * kD + s * kD;
 #pragma unroll
             for (int part = 0; part < 4; ++part) {
                 const int j0 = 32 * part;
@@ -665,6 +656,38 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                 tmem_st16u(tl + TM_OPS + (j0 >> 1), hw);
                 tmem_st16u(tl + TM_OPS + 64 + (j0 >> 1), lw);
                 tmem_st32(tl + TM_ST + j0, yv);
+            }
+        }
+        // ---- M2 and M2b done: slot s's v tile and beta are free ----
+        {
+            bool ok = true;
+            if (tid == kCA || tid == kCB)
+                ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p.status, 24);
+            ++ph;
+            alive = group_and(kChainBar, ok);
+            fence_after_sync();
+            if (!alive) break;
+            if (tid == 0) mbar_arrive(bar + B_VFREE + s);
+        }
+        // ---- F7: W = W' Diag(em) -> rows 0..31 of wq (the k E rows are dead); thread = key
+        //      channel j ----
+        {
+            const int j = tid;
+            float w[32];
+            tmem_ld32(tl + TM_WT, w);
+            const float emj = em[j];
+            const uint32_t cbase = (uint32_t)((j >> 6) * 64 * 128 + ((j & 7) << 1));
+            const int jc = (j & 63) >> 3;
+#pragma unroll
+            for (int r = 0; r < 32; r += 2) {
+                uint32_t hw, lw;
+                split2(w[r] * emj, w[r + 1] * emj, hw, lw);
+                const uint32_t o0 = cbase + r * 128 + ((jc ^ (r & 7)) << 4);
+                const uint32_t o1 = cbase + (r + 1) * 128 + ((jc ^ ((r + 1) & 7)) << 4);
+                *reinterpret_cast<uint16_t *>(wq + o0) = (uint16_t)(hw & 0xFFFFu);
+                *reinterpret_cast<uint16_t *>(wq + o1) = (uint16_t)(hw >> 16);
+                *reinterpret_cast<uint16_t *>(wq + 16384 + o0) = (uint16_t)(lw & 0xFFFFu);
+                *reinterpret_cast<uint16_t *>(wq + 16384 + o1) = (uint16_t)(lw >> 16);
             }
         }
         publish(kChainBar);
@@ -701,7 +724,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
         // ---- F8: U^T = U~^T - (W S0)^T -> A operand of M4 / M5 ----
         {
             float ut[32], a[32], b[32];
-            tmem_ld32(tl + TM_UT + 32 * s, ut);
+            tmem_ld32(tl + TM_UT, ut);
             tmem_ld32(tl + TM_D3A, a);
             tmem_ld32(tl + TM_D3B, b);
             uint32_t hw[16], lw[16];
