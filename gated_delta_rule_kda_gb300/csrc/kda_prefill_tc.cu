@@ -74,22 +74,23 @@ constexpr uint64_t kWaitNs = 2000000000ull;  // bound on every wait
 // q, k, v tiles (bf16 [32][128], two 64-column blocks with 128-byte swizzle, as
 // written by TMA) for two chunks.  log_alpha travels through registers.
 constexpr uint32_t S_QKV = 0, QKV_SIZE = 24576, QO = 0, KO = 8192, VO = 16384;
-// Tb hi | lo (a 32-row operand tile, K = 32), built and used by the chain group;
-// A (fp32 [32][32], column-major) for the prep group's solve; T by slot
-// (fp32 [32][33]), written by the solve and read by the chain group.
+// Tb (32 rows, K = 32: hi in K steps 0-1, lo in K steps 2-3 of one swizzled tile),
+// built and used by the chain group; A (fp32 [32][32], column-major) for the prep
+// group's solve; T by slot (fp32 [32][33]), written by the solve and read by the
+// chain group.
 constexpr uint32_t S_DT = 2 * QKV_SIZE;
 constexpr uint32_t S_TB = S_DT;
-constexpr uint32_t S_A = S_DT + 8192;
-constexpr uint32_t S_TS = S_DT + 12288;
+constexpr uint32_t S_A = S_DT + 4096;
+constexpr uint32_t S_TS = S_DT + 8192;
 constexpr int kLdT = 33;
 constexpr uint32_t T_SIZE = 32 * kLdT * 4;
 // [k E ; q E] hi | lo (64 rows), private to the prep group.
 constexpr uint32_t S_WX = (S_TS + 2 * T_SIZE + 1023) & ~1023u;
 // Per slot: [W ; Q~] hi | lo (64 rows; rows 0-31 hold k E until W replaces it),
-// R = k E^-1 hi | lo (32 rows), P hi | lo (32 rows, K = 32).
+// R = k E^-1 hi | lo (32 rows), P (32 rows, K = 32: hi in K steps 0-1, lo in 2-3).
 constexpr uint32_t S_WQ = S_WX + 32768, WQ_SIZE = 32768;
 constexpr uint32_t S_R = S_WQ + 2 * WQ_SIZE, R_SIZE = 16384;
-constexpr uint32_t S_P = S_R + 2 * R_SIZE, P_SIZE = 8192;
+constexpr uint32_t S_P = S_R + 2 * R_SIZE, P_SIZE = 4096;
 constexpr uint32_t S_STG = S_P + 2 * P_SIZE;  // bf16 output staging [32][128]
 constexpr uint32_t S_VEC = S_STG + 8192;      // em[2][128], e31p[2][128], e31[2][128]
 constexpr uint32_t S_BETA = S_VEC + 3072;     // beta [2][32]
@@ -457,8 +458,8 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                         const int i = 16 * half + 8 * c2 + e;
                         x[e] = i <= r ? g[8 * c2 + e] + g2[8 * c2 + e] : 0.f;
                     }
-                    unsigned char *ph2 = pp + sw128_chunk_offset(32, r, 2 * half + c2);
-                    store_split_chunk(ph2, ph2 + 4096, x);
+                    store_split_chunk(pp + sw128_chunk_offset(32, r, 2 * half + c2),
+                                      pp + sw128_chunk_offset(32, r, 4 + 2 * half + c2), x);
                 }
             }
         }
@@ -594,12 +595,12 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                 const int i = 8 * cc + e;
                 x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
             }
-            unsigned char *th = sm + S_TB + sw128_chunk_offset(32, r, cc);
-            store_split_chunk(th, th + 4096, x);
+            store_split_chunk(sm + S_TB + sw128_chunk_offset(32, r, cc),
+                              sm + S_TB + sw128_chunk_offset(32, r, 4 + cc), x);
         }
         publish(kChainBar);
         if (tid == kCA) {  // M2: U~^T = V^T Tb^T  (V exact in bf16, read MN-major)
-            const uint32_t th = smem_u32(sm + S_TB), tlo = th + 4096;
+            const uint32_t th = smem_u32(sm + S_TB);
             const uint32_t idv = idesc_bf16_f32(128, 32) | kIdescAMN;
             const uint32_t va = smem_u32(qkv + VO);
 #pragma unroll
@@ -608,10 +609,11 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                          k > 0);
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-                mma_bf16(tb + TM_UT, sw128_desc_mn(va + 2048 * k, 4096), sw128_desc_k(tlo, 32, k), idv, 1);
+                mma_bf16(tb + TM_UT, sw128_desc_mn(va + 2048 * k, 4096), sw128_desc_k(th, 32, 2 + k), idv,
+                         1);
             mma_commit(bar + B_CA);
         } else if (tid == kCB) {  // M2b: W'^T = (k E)^T Tb^T, k E (wq rows 0-31) read MN-major
-            const uint32_t th = smem_u32(sm + S_TB), tlo = th + 4096;
+            const uint32_t th = smem_u32(sm + S_TB);
             const uint32_t idw = idesc_bf16_f32(128, 32) | kIdescAMN;
             const uint32_t xh = smem_u32(wq), xl = xh + 16384;
 #pragma unroll
@@ -620,7 +622,8 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                          k > 0);
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-                mma_bf16(tb + TM_WT, sw128_desc_mn(xh + 2048 * k, 8192), sw128_desc_k(tlo, 32, k), idw, 1);
+                mma_bf16(tb + TM_WT, sw128_desc_mn(xh + 2048 * k, 8192), sw128_desc_k(th, 32, 2 + k), idw,
+                         1);
 #pragma unroll
             for (int k = 0; k < 2; ++k)
                 mma_bf16(tb + TM_WT, sw128_desc_mn(xl + 2048 * k, 8192), sw128_desc_k(th, 32, k), idw, 1);
@@ -738,13 +741,14 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
         publish(kChainBar);
         if (tid == kCA) {  // M4: (Q~ S0 + P U)^T += U^T P^T
             const uint32_t id32 = idesc_bf16_f32(128, 32);
-            const uint32_t ph2 = smem_u32(pp), pl = ph2 + 4096;
+            const uint32_t ph2 = smem_u32(pp);
 #pragma unroll
             for (int k = 0; k < 2; ++k)
                 mma_bf16_tmem_a(tb + TM_D3A + 32, tb + TM_OPS + 8 * k, sw128_desc_k(ph2, 32, k), id32, 1);
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-                mma_bf16_tmem_a(tb + TM_D3A + 32, tb + TM_OPS + 8 * k, sw128_desc_k(pl, 32, k), id32, 1);
+                mma_bf16_tmem_a(tb + TM_D3A + 32, tb + TM_OPS + 8 * k, sw128_desc_k(ph2, 32, 2 + k), id32,
+                                1);
 #pragma unroll
             for (int k = 0; k < 2; ++k)
                 mma_bf16_tmem_a(tb + TM_D3A + 32, tb + TM_OPS + 16 + 8 * k, sw128_desc_k(ph2, 32, k),
