@@ -219,6 +219,42 @@ kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_he
                            stream);
 }
 
+kda_status kda_layer_core_fused(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                const void *qp, const void *kp, const void *vp,
+                                const float *conv_w, const void *z, const float *A,
+                                const float *b, const void *beta_logit, const void *g,
+                                const int32_t *cu_seqlens, const float *S0, float scale,
+                                float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
+                                float *S_final, void *stream) {
+    if (!ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_ptr_elem(cu_seqlens, 4) || !ok_ptr(conv_w) || !ok_ptr_elem(A, 4) || !ok_opt_ptr(b))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (total_tokens > 0) {
+        if (!ok_ptr(qp) || !ok_ptr(kp) || !ok_ptr(vp) || !ok_ptr(z) || !ok_ptr_elem(beta_logit, 2) ||
+            !ok_ptr(g) || !ok_ptr(o_gated))
+            return KDA_ERR_INVALID_ARGUMENT;
+    }
+    if (!ok_opt_ptr(S0) || !ok_opt_ptr(S_final)) return KDA_ERR_INVALID_ARGUMENT;
+    const size_t state_bytes = (size_t)num_seqs * num_heads * kD * kD * sizeof(float);
+    if (S0 && S_final && S0 != S_final && overlap(S0, S_final, state_bytes))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (num_heads > 65535 || num_seqs > 65535) return KDA_ERR_UNSUPPORTED;
+    LayerArgs a;
+    a.num_seqs = num_seqs; a.total_tokens = total_tokens; a.num_heads = num_heads;
+    a.qp = static_cast<const __nv_bfloat16 *>(qp);
+    a.kp = static_cast<const __nv_bfloat16 *>(kp);
+    a.vp = static_cast<const __nv_bfloat16 *>(vp);
+    a.z = static_cast<const __nv_bfloat16 *>(z);
+    a.beta_logit = static_cast<const __nv_bfloat16 *>(beta_logit);
+    a.g = static_cast<const __nv_bfloat16 *>(g);
+    a.conv_w = conv_w; a.A = A; a.b = b; a.S0 = S0; a.cu_seqlens = cu_seqlens;
+    a.scale = scale; a.l2_eps = l2_eps; a.rms_eps = rms_eps;
+    a.out_dtype = out_dtype; a.o = o_gated; a.S_final = S_final;
+    a.status = device_status();
+    return from_cuda(launch_layer_tc(a, static_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_get_device_status(void *stream, uint32_t *detail) {
     if (detail) *detail = 0;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -111,9 +111,23 @@ struct GateArgs {
     void *out;
 };
 
+// One KDA layer core in a single tensor-core kernel (front end and gate fused).
+struct LayerArgs {
+    int32_t num_seqs, total_tokens, num_heads;
+    const __nv_bfloat16 *qp, *kp, *vp, *z, *beta_logit, *g;
+    const float *conv_w, *A, *b, *S0;
+    const int32_t *cu_seqlens;
+    float scale, l2_eps, rms_eps;
+    kda_dtype out_dtype;
+    void *o;
+    float *S_final;
+    DeviceStatus status;
+};
+
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_recurrent(const PrefillArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
+cudaError_t launch_layer_tc(const LayerArgs &a, cudaStream_t stream);
 cudaError_t launch_frontend(const FrontendArgs &a, cudaStream_t stream);
 cudaError_t launch_output_gate(const GateArgs &a, cudaStream_t stream);
 

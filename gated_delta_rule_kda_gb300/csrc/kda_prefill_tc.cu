@@ -55,6 +55,16 @@
 // two slots (shared-memory tiles, U~ in TMEM); the groups hand slots over with
 // mbarriers ("full" prep -> chain, "empty" chain -> prep), and every wait is
 // bounded in time.
+//
+// Layer mode (kLayer): the same kernel also runs one whole KDA layer core
+// ("Kimi K3 · KDA layer", KDA equation list) with nothing but the layer's inputs
+// and outputs crossing HBM.  The prep group computes the front end from the raw
+// pre-convolution q^p, k^p, v^p tiles: the width-4 causal short convolution
+// (the three previous tokens come from an 8-row TMA box; zero before the
+// sequence start), SiLU, the per-head L2 normalisation of q and k, log alpha =
+// -5 sigmoid(e^A (z + b)) and beta = sigmoid(beta_logit).  v is then fp32, so it
+// enters M2 as hi + lo like every other operand.  The chain group's readout
+// applies the output gate sigmoid(g) * RMSNorm(o~) per (token, head) row.
 #include <cuda.h>
 #include <cstring>
 #include <cudaTypedefs.h>
@@ -94,7 +104,11 @@ constexpr uint32_t S_P = S_R + 2 * R_SIZE, P_SIZE = 4096;
 constexpr uint32_t S_STG = S_P + 2 * P_SIZE;  // bf16 output staging [32][128]
 constexpr uint32_t S_VEC = S_STG + 8192;      // em[2][128], e31p[2][128], e31[2][128]
 constexpr uint32_t S_BETA = S_VEC + 3072;     // beta [2][32]
-constexpr uint32_t S_BAR = S_BETA + 256;
+// Layer mode: conv history (q^p, k^p, v^p rows t0-8 .. t0-1: three [8][128] bf16
+// swizzled tiles) and the gate's row reductions.
+constexpr uint32_t S_HIST = (S_BETA + 256 + 1023) & ~1023u;
+constexpr uint32_t S_GATE = S_HIST + 3 * 2048;  // [4 warps][32 rows] partials, then [32] 1/rms
+constexpr uint32_t S_BAR = S_GATE + 640;
 constexpr uint32_t S_TSLOT = S_BAR + 128;
 constexpr uint32_t SM_DYN = S_TSLOT + 16 + 1024;  // + alignment slack
 static_assert(SM_DYN <= 232448, "shared memory map exceeds 227 KB");
@@ -133,7 +147,8 @@ __device__ __forceinline__ uint32_t tile_chunk(int rows, int i, int cc) {
     return (uint32_t)((cc >> 3) * rows * 128 + i * 128 + (((cc & 7) ^ (i & 7)) << 4));
 }
 struct Params {
-    CUtensorMap tm_q, tm_k, tm_v;  // [T][H*128] bf16 with boxes of 32 tokens x 64 channels
+    CUtensorMap tm_q, tm_k, tm_v;     // [T][H*128] bf16 with boxes of 32 tokens x 64 channels
+    CUtensorMap tm_qh, tm_kh, tm_vh;  // layer mode: the same tensors, boxes of 8 tokens
     const float *log_alpha, *beta, *S0;
     const int32_t *cu_seqlens;
     int H;
@@ -141,7 +156,19 @@ struct Params {
     void *o;
     float *S_final;
     DeviceStatus status;
+    // layer mode (front end and output gate fused)
+    const __nv_bfloat16 *z, *beta_logit, *g;
+    const float *conv_w, *A, *b;
+    float l2_eps, rms_eps;
 };
+
+__device__ __forceinline__ float sigmoid_(float x) { return __frcp_rn(1.f + __expf(-x)); }
+__device__ __forceinline__ void bf16x4_to_f32(uint2 u, float (&x)[4]) {
+    x[0] = __uint_as_float(u.x << 16);
+    x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(u.y << 16);
+    x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+}
 
 // Store 8 fp32 values as a hi 16-byte chunk and a lo 16-byte chunk.
 __device__ __forceinline__ void store_split_chunk(unsigned char *hi, unsigned char *lo,
@@ -199,12 +226,24 @@ __device__ __forceinline__ void publish(int id) {
 // thread), beta by threads pt < 32 (cp.async, zero past nrow).  Rows past the
 // sequence end are not masked here: log_alpha and beta are masked where they
 // are used, which keeps those rows out of every product (see the kernel).
+template <bool kLayer>
 __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *sm, uint64_t *bar,
-                                            int slot, int t0, int nrow, int h, int tid) {
+                                            int slot, int t0, int nrow, int h, int tid,
+                                            bool history) {
     if (tid == kTmaThread) {
         fence_proxy_async_smem();  // earlier generic accesses to these buffers come first
         unsigned char *qkv = sm + S_QKV + slot * QKV_SIZE;
-        mbar_arrive_expect_tx(bar + B_TQKV + slot, 6 * 4096);
+        const bool hist = kLayer && history;
+        mbar_arrive_expect_tx(bar + B_TQKV + slot, 6 * 4096 + (hist ? 6 * 1024 : 0));
+        if (hist) {  // tokens t0-8 .. t0-1 (t0 - 8 >= 0: history is loaded only inside a sequence)
+            const CUtensorMap *hm[3] = {&p.tm_qh, &p.tm_kh, &p.tm_vh};
+#pragma unroll
+            for (int a = 0; a < 3; ++a)
+#pragma unroll
+                for (int b = 0; b < 2; ++b)
+                    tma_load_2d(smem_u32(sm + S_HIST + 2048 * a + 1024 * b), hm[a], h * kD + 64 * b,
+                                t0 - 8, bar + B_TQKV + slot);
+        }
         const CUtensorMap *maps[3] = {&p.tm_q, &p.tm_k, &p.tm_v};
         const uint32_t dst[3] = {QO, KO, VO};
 #pragma unroll
@@ -215,7 +254,7 @@ __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *sm, 
                             bar + B_TQKV + slot);
     }
     const int pt = tid - 128;
-    if (pt >= 0 && pt < kC) {
+    if (!kLayer && pt >= 0 && pt < kC) {
         const bool ok = pt < nrow;
         const float *s = ok ? p.beta + (size_t)(t0 + pt) * p.H + h : p.beta;
         cp_async4(smem_u32(sm + S_BETA + 128 * slot + 4 * pt), s, ok ? 4u : 0u);
@@ -237,9 +276,26 @@ __device__ __forceinline__ void load_log_alpha(const Params &p, int t0, int nrow
     }
 }
 
+// Layer mode: z of rows 4 rg .. 4 rg + 3, channels 4 q4 .. 4 q4 + 3 (zero past nrow), and
+// beta_logit of row pt for pt < 32.
+__device__ __forceinline__ void load_gate_inputs(const Params &p, int t0, int nrow, int h, int q4,
+                                                 int rg, int pt, uint2 (&z)[4], uint32_t &bl) {
+    const __nv_bfloat16 *src = p.z + ((size_t)t0 * p.H + h) * kD + 4 * q4;
+    const size_t stride = (size_t)p.H * kD;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = 4 * rg + k;
+        z[k] = r < nrow ? __ldg(reinterpret_cast<const uint2 *>(src + r * stride)) : make_uint2(0, 0);
+    }
+    bl = 0;
+    if (pt < kC && pt < nrow)
+        bl = __bfloat16_as_ushort(p.beta_logit[(size_t)(t0 + pt) * p.H + h]);
+}
+
 // ============================================================================
 // Prep group (warps 4-11, 256 threads): operands of every chunk, in order.
 // ============================================================================
+template <bool kLayer>
 __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, uint32_t tb,
                                            int h, int t_begin, int t_end, int nchunks) {
     const int tid = threadIdx.x, pt = tid - 128, lane = tid & 31;
@@ -259,12 +315,21 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
     int issued = 0;    // chunks whose q/k/v loads were issued
     bool alive = true;
     float4 la[4];      // log_alpha of the next chunk (this thread's 4 rows x 4 channels)
+    uint2 zr[4];       // layer mode: z of the next chunk (same rows and channels)
+    uint32_t bl = 0;   // layer mode: beta_logit of row pt of the next chunk (bf16 bits)
+    float eA = 0.f;    // layer mode: e^{A_h}
+    float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);  // layer mode: b[h][4 q4 ..]
+    if constexpr (kLayer) {
+        eA = expf(p.A[h]);
+        if (p.b != nullptr) bb = *reinterpret_cast<const float4 *>(p.b + (size_t)h * kD + 4 * q4);
+    }
 
     if (nchunks > 0) {
         const int n0 = min(kC, t_end - t_begin);
-        issue_loads(p, sm, bar, 0, t_begin, n0, h, tid);
+        issue_loads<kLayer>(p, sm, bar, 0, t_begin, n0, h, tid, false);
         issued = 1;
-        load_log_alpha(p, t_begin, n0, h, q4, rg, la);
+        if constexpr (kLayer) load_gate_inputs(p, t_begin, n0, h, q4, rg, pt, zr, bl);
+        else load_log_alpha(p, t_begin, n0, h, q4, rg, la);
     }
 
     for (int c = 0; c < nchunks; ++c) {
@@ -286,6 +351,11 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 ok = wait_one(bar + B_EMPTY + s, ((c >> 1) - 1) & 1, p.status, 10);
             if (tid == kTmaThread) ok = wait_one(bar + B_TQKV + s, (c >> 1) & 1, p.status, 11);
             if (pt < kC) cp_async_wait_all();
+            if constexpr (kLayer) {  // beta = sigmoid(beta_logit); rows past the end write nothing
+                if (pt < kC)
+                    const_cast<float *>(beta_s)[pt] =
+                        pt < nrow ? sigmoid_(__uint_as_float(bl << 16)) : 0.f;
+            }
             alive = group_and(kPrepBar, ok);
             fence_after_sync();
             if (!alive) break;
@@ -297,6 +367,100 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         //      16..r (two scan segments of 4 row groups).  Then [k E ; q E] -> wx,
         //      (and wq rows 0..31), R = k E^-1 -> rr, Q~ = q E em -> wq rows 32.. ----
         {
+            const int cc = q4 >> 1, hb = (q4 & 1) * 8;
+            float qh[4][4], kh[4][4];  // layer mode: q^, k^ of rows 4 rg + k
+            if constexpr (kLayer) {
+                // ---- front end: short conv + SiLU for q^p, k^p, v^p ----
+                float y[3][4][4];
+#pragma unroll
+                for (int X = 0; X < 3; ++X) {
+                    const unsigned char *tile = qkv + (X == 0 ? QO : X == 1 ? KO : VO);
+                    const unsigned char *hist = sm + S_HIST + 2048 * X;
+                    const float *wsrc = p.conv_w + (((size_t)X * p.H + h) * kD + 4 * q4) * 4;
+                    float4 w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) w4[e] = __ldg(reinterpret_cast<const float4 *>(wsrc) + e);
+                    float raw[7][4];  // rows 4 rg - 3 .. 4 rg + 3
+#pragma unroll
+                    for (int lr = 0; lr < 7; ++lr) {
+                        const int row = 4 * rg - 3 + lr;
+                        uint2 u = make_uint2(0, 0);
+                        if (row >= 0)
+                            u = *reinterpret_cast<const uint2 *>(tile + tile_chunk(32, row, cc) + hb);
+                        else if (c > 0)  // previous tokens of this sequence; zero before its start
+                            u = *reinterpret_cast<const uint2 *>(hist + tile_chunk(8, 8 + row, cc) + hb);
+                        bf16x4_to_f32(u, raw[lr]);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            // tap j multiplies token t - j (tap 0: the current token)
+                            float a = w4[e].x * raw[k + 3][e];
+                            a = fmaf(w4[e].y, raw[k + 2][e], a);
+                            a = fmaf(w4[e].z, raw[k + 1][e], a);
+                            a = fmaf(w4[e].w, raw[k][e], a);
+                            y[X][k][e] = a * sigmoid_(a);
+                        }
+                }
+                // ---- L2 norms of q and k per (token, head) row: 4 lanes, then 8 warps ----
+                float* part = sAt;  // [2][32 rows][8 warps]; A is not in use here
+                float ss[2][4];
+#pragma unroll
+                for (int X = 0; X < 2; ++X)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        float v = y[X][k][0] * y[X][k][0];
+                        v = fmaf(y[X][k][1], y[X][k][1], v);
+                        v = fmaf(y[X][k][2], y[X][k][2], v);
+                        v = fmaf(y[X][k][3], y[X][k][3], v);
+                        v += __shfl_xor_sync(0xffffffffu, v, 1);
+                        v += __shfl_xor_sync(0xffffffffu, v, 2);
+                        ss[X][k] = v;
+                    }
+                if ((lane & 3) == 0) {
+#pragma unroll
+                    for (int X = 0; X < 2; ++X)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) part[(X * 32 + 4 * rg + k) * 8 + (pt >> 5)] = ss[X][k];
+                }
+                group_sync(kPrepBar);  // partials complete; every raw tile read is done
+#pragma unroll
+                for (int X = 0; X < 2; ++X)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float4 a = *reinterpret_cast<const float4 *>(part + (X * 32 + 4 * rg + k) * 8);
+                        const float4 b = *reinterpret_cast<const float4 *>(part + (X * 32 + 4 * rg + k) * 8 + 4);
+                        const float inv = rsqrtf(((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w)) + p.l2_eps);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (X == 0) qh[k][e] = y[0][k][e] * inv;
+                            else kh[k][e] = y[1][k][e] * inv;
+                        }
+                    }
+                // ---- v (fp32) -> V hi over the v^p tile, V lo over the q^p tile ----
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 4 * rg + k;
+                    uint2 h2, l2;
+                    split2(y[2][k][0], y[2][k][1], h2.x, l2.x);
+                    split2(y[2][k][2], y[2][k][3], h2.y, l2.y);
+                    unsigned char *qkvw = const_cast<unsigned char *>(qkv);
+                    *reinterpret_cast<uint2 *>(qkvw + VO + tile_chunk(32, r, cc) + hb) = h2;
+                    *reinterpret_cast<uint2 *>(qkvw + QO + tile_chunk(32, r, cc) + hb) = l2;
+                }
+                // ---- log alpha = -5 sigmoid(e^A (z + b)) (rows past the end: 0) ----
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float zf[4];
+                    bf16x4_to_f32(zr[k], zf);
+                    const bool in = 4 * rg + k < nrow;
+                    la[k].x = in ? -5.f * sigmoid_(eA * (zf[0] + bb.x)) : 0.f;
+                    la[k].y = in ? -5.f * sigmoid_(eA * (zf[1] + bb.y)) : 0.f;
+                    la[k].z = in ? -5.f * sigmoid_(eA * (zf[2] + bb.z)) : 0.f;
+                    la[k].w = in ? -5.f * sigmoid_(eA * (zf[3] + bb.w)) : 0.f;
+                }
+            }
             const float kL2E = 1.4426950408889634f;
             float4 pre[4];
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -346,21 +510,26 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 *reinterpret_cast<float4 *>(e31_s + 4 * q4) = e31;
                 e31_prev = e31;
             }
-            // Row order rotated by rg >> 1 so that the 8 rows a warp stores at once sit
-            // in 8 distinct swizzle positions.
-            const int cc = q4 >> 1, hb = (q4 & 1) * 8;
+            // bf16 inputs: row order rotated by rg >> 1 so that the 8 rows a warp stores at
+            // once sit in 8 distinct swizzle positions (layer mode keeps q^, k^ in registers
+            // and takes the rows in order).
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int kk = (k + (rg >> 1)) & 3;
+                const int kk = kLayer ? k : (k + (rg >> 1)) & 3;
                 const int r = 4 * rg + kk;
                 const float4 pk = kk == 0 ? pre[0] : kk == 1 ? pre[1] : kk == 2 ? pre[2] : pre[3];
                 const float dv[4] = {base.x + pk.x, base.y + pk.y, base.z + pk.z, base.w + pk.w};
-                const uint2 kw = *reinterpret_cast<const uint2 *>(qkv + KO + tile_chunk(32, r, cc) + hb);
-                const uint2 qw = *reinterpret_cast<const uint2 *>(qkv + QO + tile_chunk(32, r, cc) + hb);
-                const float kv[4] = {__uint_as_float(kw.x << 16), __uint_as_float(kw.x & 0xFFFF0000u),
-                                     __uint_as_float(kw.y << 16), __uint_as_float(kw.y & 0xFFFF0000u)};
-                const float qv[4] = {__uint_as_float(qw.x << 16), __uint_as_float(qw.x & 0xFFFF0000u),
-                                     __uint_as_float(qw.y << 16), __uint_as_float(qw.y & 0xFFFF0000u)};
+                float kv[4], qv[4];
+                if constexpr (kLayer) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        kv[e] = kh[k][e];
+                        qv[e] = qh[k][e];
+                    }
+                } else {
+                    bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + KO + tile_chunk(32, r, cc) + hb), kv);
+                    bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + QO + tile_chunk(32, r, cc) + hb), qv);
+                }
                 float xk[4], xq[4], xr[4], xt[4];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
@@ -396,7 +565,10 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 *reinterpret_cast<uint2 *>(dst + 16384) = l2;
             }
         }
-        if (c + 1 < nchunks) load_log_alpha(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, la);
+        if (c + 1 < nchunks) {
+            if constexpr (kLayer) load_gate_inputs(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, pt, zr, bl);
+            else load_log_alpha(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, la);
+        }
         publish(kPrepBar);
         if (c + 1 < nchunks) {  // stage chunk c+1 into slot s^1 once chunk c-1 no longer needs it
             bool ok = true;
@@ -404,7 +576,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 ok = wait_one(bar + B_VFREE + (s ^ 1), ((c - 1) >> 1) & 1, p.status, 12);
             alive = group_and(kPrepBar, ok);
             if (!alive) break;
-            issue_loads(p, sm, bar, s ^ 1, t0 + kC, min(kC, t_end - t0 - kC), h, tid);
+            issue_loads<kLayer>(p, sm, bar, s ^ 1, t0 + kC, min(kC, t_end - t0 - kC), h, tid, true);
             issued = c + 2;
         }
         if (tid == kPA || tid == kPB) {  // M1: Gram, K steps split over the two issuers
@@ -523,7 +695,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
 // ============================================================================
 // Chain group (warps 0-3): the state-dependent products, chunk by chunk.
 // ============================================================================
-template <typename Tout>
+template <typename Tout, bool kLayer>
 __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, uint32_t tb,
                                             int h, int n, int t_begin, int t_end, int nchunks) {
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -586,6 +758,18 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             if (!alive) break;
         }
 
+        uint32_t gw[16];  // layer mode: g of rows 2i, 2i+1 for this thread's channel (bf16 pair)
+        if constexpr (kLayer) {
+            const unsigned short *gsrc =
+                reinterpret_cast<const unsigned short *>(p.g) + ((size_t)t0 * H + h) * kD + c_lane;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t lo = 2 * i < nrow ? gsrc[(size_t)(2 * i) * H * kD] : 0u;
+                const uint32_t hi = 2 * i + 1 < nrow ? gsrc[(size_t)(2 * i + 1) * H * kD] : 0u;
+                gw[i] = lo | (hi << 16);
+            }
+        }
+
         // ---- Tb = T diag(beta) (32 rows x K 32): one 16-byte chunk per thread ----
         {
             const int r = tid >> 2, cc = tid & 3;
@@ -599,7 +783,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                               sm + S_TB + sw128_chunk_offset(32, r, 4 + cc), x);
         }
         publish(kChainBar);
-        if (tid == kCA) {  // M2: U~^T = V^T Tb^T  (V exact in bf16, read MN-major)
+        if (tid == kCA) {  // M2: U~^T = V^T Tb^T  (V read MN-major: exact bf16, or hi + lo)
             const uint32_t th = smem_u32(sm + S_TB);
             const uint32_t idv = idesc_bf16_f32(128, 32) | kIdescAMN;
             const uint32_t va = smem_u32(qkv + VO);
@@ -611,6 +795,13 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             for (int k = 0; k < 2; ++k)
                 mma_bf16(tb + TM_UT, sw128_desc_mn(va + 2048 * k, 4096), sw128_desc_k(th, 32, 2 + k), idv,
                          1);
+            if constexpr (kLayer) {  // V lo (in the q^p tile's place)
+                const uint32_t vl = smem_u32(qkv + QO);
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    mma_bf16(tb + TM_UT, sw128_desc_mn(vl + 2048 * k, 4096), sw128_desc_k(th, 32, k), idv,
+                             1);
+            }
             mma_commit(bar + B_CA);
         } else if (tid == kCB) {  // M2b: W'^T = (k E)^T Tb^T, k E (wq rows 0-31) read MN-major
             const uint32_t th = smem_u32(sm + S_TB);
@@ -787,16 +978,46 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             float a[32], b[32];
             tmem_ld32(tl + TM_D3A + 32, a);
             tmem_ld32(tl + TM_D3B + 32, b);
+#pragma unroll
+            for (int r = 0; r < 32; ++r) a[r] = p.scale * (a[r] + b[r]);  // o~[t0 + r][c]
+            if constexpr (kLayer) {
+                // Output gate: o^g = sigmoid(g) o~ / sqrt(mean_c o~^2 + eps) per (token, head)
+                // row.  Sum of squares over this warp's 32 channels for all 32 rows at once:
+                // five halving steps leave lane l with row l's sum.
+#pragma unroll
+                for (int r = 0; r < 32; ++r) b[r] = a[r] * a[r];
+#pragma unroll
+                for (int o2 = 16; o2 >= 1; o2 >>= 1) {
+                    const bool up = (c_lane & o2) != 0;
+#pragma unroll
+                    for (int i = 0; i < o2; ++i) {
+                        const float keep = up ? b[i + o2] : b[i];
+                        const float send = up ? b[i] : b[i + o2];
+                        b[i] = keep + __shfl_xor_sync(0xffffffffu, send, o2);
+                    }
+                }
+                float *gate = reinterpret_cast<float *>(sm + S_GATE);
+                gate[warp * 32 + (c_lane & 31)] = b[0];
+                group_sync(kChainBar);
+                if (tid < 32)
+                    gate[128 + tid] = rsqrtf((gate[tid] + gate[32 + tid] + gate[64 + tid] + gate[96 + tid]) *
+                                                 (1.f / kD) + p.rms_eps);
+                group_sync(kChainBar);
+#pragma unroll
+                for (int r = 0; r < 32; ++r) {
+                    const uint32_t gb = (r & 1) ? (gw[r >> 1] & 0xFFFF0000u) : (gw[r >> 1] << 16);
+                    a[r] *= sigmoid_(__uint_as_float(gb)) * gate[128 + r];
+                }
+            }
             if constexpr (sizeof(Tout) == 2) {
 #pragma unroll
-                for (int r = 0; r < 32; ++r)
-                    stg[r * kD + c_lane] = __float2bfloat16_rn(p.scale * (a[r] + b[r]));
+                for (int r = 0; r < 32; ++r) stg[r * kD + c_lane] = __float2bfloat16_rn(a[r]);
                 pend_t0 = t0;
                 pend_rows = nrow;
             } else {
 #pragma unroll
                 for (int r = 0; r < 32; ++r)
-                    if (r < nrow) o[((size_t)(t0 + r) * H + h) * kD + c_lane] = p.scale * (a[r] + b[r]);
+                    if (r < nrow) o[((size_t)(t0 + r) * H + h) * kD + c_lane] = a[r];
             }
         }
     }
@@ -820,7 +1041,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
     }
 }
 
-template <typename Tout>
+template <typename Tout, bool kLayer>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -847,9 +1068,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const uint32_t tb = *tslot;
 
     if (warp >= 4)
-        prep_group(p, sm, tb, h, t_begin, t_end, nchunks);
+        prep_group<kLayer>(p, sm, tb, h, t_begin, t_end, nchunks);
     else
-        chain_group<Tout>(p, sm, tb, h, n, t_begin, t_end, nchunks);
+        chain_group<Tout, kLayer>(p, sm, tb, h, n, t_begin, t_end, nchunks);
 
     fence_before_sync();
     __syncthreads();
@@ -869,35 +1090,43 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// [T][H*128] tensor, boxes of 32 tokens x box_cols elements.
+// [T][H*128] tensor, boxes of box_rows tokens x box_cols elements.
 bool encode_map(CUtensorMap *m, const void *base, CUtensorMapDataType dt, int elem_bytes, int T,
-                int H, int box_cols, CUtensorMapSwizzle swz) {
+                int H, int box_cols, int box_rows, CUtensorMapSwizzle swz) {
     auto fn = tensor_map_encoder();
     if (fn == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)H * kD, (cuuint64_t)T};
     const cuuint64_t strides[1] = {(cuuint64_t)H * kD * elem_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)kC};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Tout>
-cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<Tout>,
+bool encode_bf16_tiles(CUtensorMap *m, const void *base, int T, int H, int box_rows) {
+    return encode_map(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, 64, box_rows,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+template <typename Tout, bool kLayer>
+cudaError_t launch_params(const Params &p, int num_seqs, int num_heads, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<Tout, kLayer>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM_DYN);
     if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)num_seqs * (unsigned)num_heads;
+    prefill_tc_kernel<Tout, kLayer><<<grid, kThreads, SM_DYN, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <typename Tout>
+cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
     Params p;
     memset(&p, 0, sizeof(p));
     if (a.total_tokens > 0) {
         const int T = a.total_tokens, H = a.num_heads;
-        if (!encode_map(&p.tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&p.tm_k, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_map(&p.tm_v, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, 64,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+        if (!encode_bf16_tiles(&p.tm_q, a.q, T, H, kC) || !encode_bf16_tiles(&p.tm_k, a.k, T, H, kC) ||
+            !encode_bf16_tiles(&p.tm_v, a.v, T, H, kC))
             return cudaErrorInvalidValue;
     }
     p.log_alpha = a.log_alpha;
@@ -909,9 +1138,36 @@ cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
     p.o = a.o;
     p.S_final = a.S_final;
     p.status = a.status;
-    const unsigned grid = (unsigned)a.num_seqs * (unsigned)a.num_heads;
-    prefill_tc_kernel<Tout><<<grid, kThreads, SM_DYN, stream>>>(p);
-    return cudaGetLastError();
+    return launch_params<Tout, false>(p, a.num_seqs, a.num_heads, stream);
+}
+
+template <typename Tout>
+cudaError_t launch_layer_typed(const LayerArgs &a, cudaStream_t stream) {
+    Params p;
+    memset(&p, 0, sizeof(p));
+    if (a.total_tokens > 0) {
+        const int T = a.total_tokens, H = a.num_heads;
+        if (!encode_bf16_tiles(&p.tm_q, a.qp, T, H, kC) || !encode_bf16_tiles(&p.tm_k, a.kp, T, H, kC) ||
+            !encode_bf16_tiles(&p.tm_v, a.vp, T, H, kC) || !encode_bf16_tiles(&p.tm_qh, a.qp, T, H, 8) ||
+            !encode_bf16_tiles(&p.tm_kh, a.kp, T, H, 8) || !encode_bf16_tiles(&p.tm_vh, a.vp, T, H, 8))
+            return cudaErrorInvalidValue;
+    }
+    p.S0 = a.S0;
+    p.cu_seqlens = a.cu_seqlens;
+    p.H = a.num_heads;
+    p.scale = a.scale;
+    p.o = a.o;
+    p.S_final = a.S_final;
+    p.status = a.status;
+    p.z = a.z;
+    p.beta_logit = a.beta_logit;
+    p.g = a.g;
+    p.conv_w = a.conv_w;
+    p.A = a.A;
+    p.b = a.b;
+    p.l2_eps = a.l2_eps;
+    p.rms_eps = a.rms_eps;
+    return launch_params<Tout, true>(p, a.num_seqs, a.num_heads, stream);
 }
 
 }  // namespace
@@ -919,6 +1175,11 @@ cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream) {
     if (a.out_dtype == KDA_BF16) return launch_typed<__nv_bfloat16>(a, stream);
     return launch_typed<float>(a, stream);
+}
+
+cudaError_t launch_layer_tc(const LayerArgs &a, cudaStream_t stream) {
+    if (a.out_dtype == KDA_BF16) return launch_layer_typed<__nv_bfloat16>(a, stream);
+    return launch_layer_typed<float>(a, stream);
 }
 
 }  // namespace kda

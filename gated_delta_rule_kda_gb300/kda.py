@@ -45,6 +45,7 @@ EXPORTED = (
     "kda_layer_core_workspace_size",
     "kda_layer_core",
     "kda_layer_core_noalloc",
+    "kda_layer_core_fused",
     "kda_get_device_status",
 )
 
@@ -90,6 +91,9 @@ def _load() -> ctypes.CDLL:
     lib.kda_layer_core_noalloc.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, F, F,
                                            F, ctypes.c_int, P, P, P]
     lib.kda_layer_core_noalloc.restype = ctypes.c_int
+    lib.kda_layer_core_fused.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, F, F,
+                                         F, ctypes.c_int, P, P, P]
+    lib.kda_layer_core_fused.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.kda_get_device_status.restype = ctypes.c_int
     return lib
@@ -252,6 +256,25 @@ def kda_layer_core_noalloc(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlen
                                      float(scale), float(l2_eps), float(rms_eps),
                                      _dtype_code(o.dtype), _p(o), _p(S_final), _stream(stream))
     _check("kda_layer_core_noalloc", rc)
+    return o, S_final
+
+
+def kda_layer_core_fused(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=None,
+                         scale=DEFAULT_SCALE, l2_eps=1e-6, rms_eps=1e-6, *,
+                         out_dtype=torch.bfloat16, o=None, S_final=None, want_state=True,
+                         stream=None):
+    """The layer core in one tensor-core kernel.  Returns (o_gated, S_final or None)."""
+    T, H, _ = qp.shape
+    N = cu_seqlens.shape[0] - 1
+    if o is None:
+        o = torch.empty((T, H, HEAD_DIM), dtype=out_dtype, device=qp.device)
+    if S_final is None and want_state:
+        S_final = torch.empty((N, H, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=qp.device)
+    rc = _lib.kda_layer_core_fused(N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A),
+                                   _p(b), _p(beta_logit), _p(g), _p(cu_seqlens), _p(S0),
+                                   float(scale), float(l2_eps), float(rms_eps),
+                                   _dtype_code(o.dtype), _p(o), _p(S_final), _stream(stream))
+    _check("kda_layer_core_fused", rc)
     return o, S_final
 
 

@@ -241,6 +241,35 @@ kda_status kda_layer_core_noalloc(int32_t num_seqs, int32_t total_tokens, int32_
                                   float *S_final, void *stream);
 
 /*
+ * kda_layer_core_fused - the same layer core as kda_layer_core in ONE
+ * tensor-core kernel: only the layer's inputs and outputs cross HBM ("Kimi K3 ·
+ * KDA layer", KDA equation list: short convolution, SiLU, L2 norm, the decay and
+ * write-strength gates, the delta-rule recurrence, the sigmoid-gated RMSNorm).
+ *
+ * Inside the kernel every intermediate (q^, k^, v, log_alpha, beta, o~) is fp32
+ * and enters each tensor-core product as a bf16 hi + lo pair, so the result
+ * matches kda_layer_core's within the 2e-3 (row-conditioned) bound; it is not
+ * bit-identical to it.  No workspace; nothing is allocated.
+ *
+ *   Arguments as kda_layer_core (without workspace).  qp, kp, vp, z, g and
+ *   o_gated must be 16-byte aligned (qp, kp, vp are read with TMA);
+ *   beta_logit needs 2-byte alignment; log_alpha's floor of -5 holds by
+ *   construction (-5 sigmoid(.)).
+ * Errors: KDA_ERR_INVALID_ARGUMENT (null/misaligned pointers, bad sizes or dtype,
+ * S0/S_final partially overlapping), KDA_ERR_UNSUPPORTED (more than 65535 heads
+ * or sequences), KDA_ERR_CUDA (launch failure); a kernel that gives up waiting
+ * on the tensor core reports KDA_ERR_DEVICE_TIMEOUT through
+ * kda_get_device_status.
+ */
+kda_status kda_layer_core_fused(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                const void *qp, const void *kp, const void *vp,
+                                const float *conv_w, const void *z, const float *A,
+                                const float *b, const void *beta_logit, const void *g,
+                                const int32_t *cu_seqlens, const float *S0, float scale,
+                                float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
+                                float *S_final, void *stream);
+
+/*
  * kda_get_device_status - synchronises `stream`, then returns and clears the
  * device status word: KDA_OK, KDA_ERR_DEVICE_TIMEOUT or KDA_ERR_DEVICE_CHECK
  * (KDA_ERR_CUDA if the synchronisation itself fails).  If detail is not

@@ -116,3 +116,25 @@ def test_layer_core_rejects_missing_workspace(kda):
                             None, 0.1, 1e-6, 1e-6, 0, FAKE, None, FAKE, 1 << 20, None)
     assert rc == 1  # g missing
     assert kda.kda_layer_core_workspace_size(16, 1000, 96) > 1000 * 96 * 128 * 2 * 3
+
+
+def _fused(lib, **kw):
+    a = dict(N=1, T=4, H=2, qp=FAKE, kp=FAKE, vp=FAKE, w=FAKE, z=FAKE, A=FAKE, b=None, bl=FAKE,
+             g=FAKE, cu=FAKE, S0=None, out_dt=0, o=FAKE, Sf=None)
+    a.update(kw)
+    return lib.kda_layer_core_fused(a["N"], a["T"], a["H"], a["qp"], a["kp"], a["vp"], a["w"],
+                                    a["z"], a["A"], a["b"], a["bl"], a["g"], a["cu"], a["S0"], 0.1,
+                                    1e-6, 1e-6, a["out_dt"], a["o"], a["Sf"], None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(out_dt=5), dict(N=0), dict(H=0), dict(T=-1), dict(qp=None), dict(kp=MIS), dict(vp=None),
+    dict(w=MIS), dict(z=None), dict(A=None), dict(b=MIS), dict(bl=None), dict(g=None),
+    dict(o=MIS), dict(cu=None), dict(S0=MIS), dict(S0=FAKE, Sf=FAKE + 64),
+])
+def test_layer_core_fused_rejects_bad_arguments(kda, bad):
+    assert _fused(kda.library(), **bad) == 1  # KDA_ERR_INVALID_ARGUMENT, before any launch
+
+
+def test_layer_core_fused_too_many_heads_unsupported(kda):
+    assert _fused(kda.library(), H=70000) == 2

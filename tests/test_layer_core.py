@@ -108,3 +108,60 @@ def test_layer_core_rejects_small_workspace(kda):
     with pytest.raises(kda.KdaError):
         kda.kda_layer_core(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b,
                            inp.beta_logit, inp.g, inp.cu_seqlens, None, workspace=ws)
+
+
+# ---------------------------------------------------------------------------
+# kda_layer_core_fused: the same layer core in one tensor-core kernel.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_fused_small_varlen(kda, out_dtype):
+    """Ragged lengths (1, 0, 33, 70, 129 tokens: partial chunks, an empty sequence,
+    conv history across chunk boundaries) with a carried state."""
+    inp = synthetic.layer_inputs([70, 1, 0, 33, 129], 4, seed=41, s0_std=0.1, device="cuda")
+    og, Sf = kda.kda_layer_core_fused(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b,
+                                      inp.beta_logit, inp.g, inp.cu_seqlens, inp.S0,
+                                      out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status()[0] == 0
+    ref_o, ref_S, ref_ot = oracle_layer_core(inp)
+    assert_gated_close(to64(og), ref_o, ref_ot, out_dtype == torch.bfloat16)
+    assert_close(to64(Sf), ref_S, TOL_BF16, "S_final")
+
+
+def test_fused_long_sequence_nonzero_bias(kda):
+    """One 3000-token sequence (94 chunks) plus a short one, with a nonzero decay bias b."""
+    inp = synthetic.layer_inputs([3000, 45], 2, seed=44, s0_std=0.1, device="cuda")
+    b = torch.randn(inp.b.shape, generator=torch.Generator().manual_seed(7)).to(inp.b.device) * 0.5
+    og, Sf = kda.kda_layer_core_fused(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, b,
+                                      inp.beta_logit, inp.g, inp.cu_seqlens, inp.S0,
+                                      out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    inp.b = b
+    ref_o, ref_S, ref_ot = oracle_layer_core(inp)
+    assert_gated_close(to64(og), ref_o, ref_ot, False)
+    assert_close(to64(Sf), ref_S, TOL_BF16, "S_final")
+
+
+def test_fused_full_varlen_sampled_heads(kda):
+    """Workload 5 (16 sequences, lengths log-uniform in [1K, 64K], 96 heads); oracle on
+    heads 0, 47, 95 over every sequence."""
+    inp = synthetic.workload(5, device="cuda")
+    og, Sf = kda.kda_layer_core_fused(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b,
+                                      inp.beta_logit, inp.g, inp.cu_seqlens, None,
+                                      out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status()[0] == 0
+    heads = [0, 47, 95]
+    ref_o, ref_S, ref_ot = oracle_layer_core(inp, heads)
+    assert_gated_close(to64(og[:, heads]), ref_o, ref_ot, True)
+    assert_close(to64(Sf[:, heads]), ref_S, TOL_BF16, "S_final")
+
+
+def test_fused_deterministic(kda):
+    inp = synthetic.layer_inputs([300, 77], 3, seed=45, device="cuda")
+    a, Sa = kda.kda_layer_core_fused(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b,
+                                     inp.beta_logit, inp.g, inp.cu_seqlens, None)
+    b, Sb = kda.kda_layer_core_fused(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b,
+                                     inp.beta_logit, inp.g, inp.cu_seqlens, None)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and torch.equal(Sa, Sb)
