@@ -40,6 +40,8 @@ STATE_BYTES = D * D * 4                                               # 64 KiB p
 # Decode, per (request, head): state read + write, q/k/v bf16, log_alpha fp32, beta, o bf16
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * D * 2 + D * 4 + 4 + D * 2  # 132,612 B
 DECODE_FLOP_PER_UNIT = 2 * 4 * D * D
+# Fused layer core, per (token, head): q^p, k^p, v^p, z, g bf16 in, o^g bf16 out, beta_logit.
+LAYER_BYTES_PER_TOKEN_HEAD = 5 * D * 2 + 2 + D * 2                      # 1,538 B
 
 
 # DRAM traffic per unit (token-head for the prefill, request-head for decode) from the
@@ -315,29 +317,42 @@ def run_ours(args, world, rank, local):
     del dinp, od
     torch.cuda.empty_cache()
 
-    # ---------------- fused layer core (varlen, 16 sequences) ----------------
+    # ---------------- layer core (varlen, 16 sequences) ----------------
     layer = None
     if not args.skip_layer_core:
         linp = synthetic.workload(5, device=dev)
         LT = linp.qp.shape[0]
-        ws = torch.empty(kda.kda_layer_core_workspace_size(16, LT, 96), dtype=torch.uint8,
-                         device=dev)
         og = torch.empty((LT, 96, D), dtype=torch.bfloat16, device=dev)
         Sl = torch.empty((16, 96, D, D), dtype=torch.float32, device=dev)
 
-        def layer_step():
-            kda.kda_layer_core(linp.qp, linp.kp, linp.vp, linp.conv_w, linp.z, linp.A, linp.b,
-                               linp.beta_logit, linp.g, linp.cu_seqlens, None, o=og, S_final=Sl,
-                               workspace=ws)
+        def fused_step():
+            kda.kda_layer_core_fused(linp.qp, linp.kp, linp.vp, linp.conv_w, linp.z, linp.A,
+                                     linp.b, linp.beta_logit, linp.g, linp.cu_seqlens, None,
+                                     o=og, S_final=Sl)
 
-        l_steps = max(1, min(args.steps, 5))
-        l_total, _ = time_launches(layer_step, l_steps, args.warmup, world)
+        l_steps = max(1, min(args.steps, 10))
+        l_total, _ = time_launches(fused_step, l_steps, args.warmup, world)
         l_ms = max_over_ranks(l_total / l_steps, world)
         layer = {"tokens_per_s": world * LT / (l_ms / 1e3), "ms_per_step": l_ms,
                  "tokens": LT, "workload": "16 sequences, lengths log-uniform in [1K, 64K], "
                                            "96 heads, front end + recurrence + gate",
-                 "launches_per_step": 3}
-        del linp, ws, og, Sl
+                 "entry_point": "kda_layer_core_fused", "launches_per_step": 1,
+                 "hbm_bytes_per_token_head": LAYER_BYTES_PER_TOKEN_HEAD}
+        if not args.skip_staged_layer_core:
+            ws = torch.empty(kda.kda_layer_core_workspace_size(16, LT, 96), dtype=torch.uint8,
+                             device=dev)
+
+            def staged_step():
+                kda.kda_layer_core(linp.qp, linp.kp, linp.vp, linp.conv_w, linp.z, linp.A,
+                                   linp.b, linp.beta_logit, linp.g, linp.cu_seqlens, None, o=og,
+                                   S_final=Sl, workspace=ws)
+
+            s_total, _ = time_launches(staged_step, 2, 1, world)
+            s_ms = max_over_ranks(s_total / 2, world)
+            layer["staged"] = {"entry_point": "kda_layer_core", "ms_per_step": s_ms,
+                               "tokens_per_s": world * LT / (s_ms / 1e3), "launches_per_step": 3}
+            del ws
+        del linp, og, Sl
         torch.cuda.empty_cache()
 
     # ---------------- CPU baseline: the oracle on a bounded sample ----------------
@@ -399,6 +414,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-layer-core", action="store_true")
+    ap.add_argument("--skip-staged-layer-core", action="store_true",
+                    help="time only the fused layer core, not the three-launch composition")
     ap.add_argument("--only", choices=["prefill", "decode"], default=None,
                     help="profiling aid: run just this kernel (no baseline, no e2e)")
     ap.add_argument("--small", action="store_true",

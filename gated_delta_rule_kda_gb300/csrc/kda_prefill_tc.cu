@@ -162,7 +162,14 @@ struct Params {
     float l2_eps, rms_eps;
 };
 
-__device__ __forceinline__ float sigmoid_(float x) { return __frcp_rn(1.f + __expf(-x)); }
+// 1 / (1 + 2^(-x log2 e)) on the SFU: ex2.approx and rcp.approx, each within about
+// 2^-22 relative; tends to 0 (not NaN) for x -> -inf.
+__device__ __forceinline__ float sigmoid_(float x) {
+    const float e = ex2_approx(-1.4426950408889634f * x);
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+    return r;
+}
 __device__ __forceinline__ void bf16x4_to_f32(uint2 u, float (&x)[4]) {
     x[0] = __uint_as_float(u.x << 16);
     x[1] = __uint_as_float(u.x & 0xFFFF0000u);

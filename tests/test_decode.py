@@ -12,6 +12,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module")
 def kda():
+    from gated_delta_rule_kda_gb300 import build
+    build.build()
     from gated_delta_rule_kda_gb300 import kda as mod
     return mod
 
