@@ -101,7 +101,7 @@ constexpr uint32_t S_WX = (S_TS + 2 * T_SIZE + 1023) & ~1023u;
 constexpr uint32_t S_WQ = S_WX + 32768, WQ_SIZE = 32768;
 constexpr uint32_t S_R = S_WQ + 2 * WQ_SIZE, R_SIZE = 16384;
 constexpr uint32_t S_P = S_R + 2 * R_SIZE, P_SIZE = 4096;
-constexpr uint32_t S_STG = S_P + 2 * P_SIZE;  // bf16 output staging [32][128]
+constexpr uint32_t S_STG = S_P + 2 * P_SIZE;  // bf16 output staging [32][128]; layer mode: g tile
 constexpr uint32_t S_VEC = S_STG + 8192;      // em[2][128], e31p[2][128], e31[2][128]
 constexpr uint32_t S_BETA = S_VEC + 3072;     // beta [2][32]
 // Layer mode: conv history (q^p, k^p, v^p rows t0-8 .. t0-1: three [8][128] bf16
@@ -122,7 +122,8 @@ constexpr int B_CA = 2, B_CB = 3, B_PA = 4, B_PB = 5;  // MMA completion, one pe
 constexpr int B_FULL = 6;   // [2] prep -> chain: slot holds a chunk's operands
 constexpr int B_EMPTY = 8;  // [2] chain -> prep: slot consumed
 constexpr int B_VFREE = 10; // [2] chain -> prep: the slot's v tile and beta were consumed (M2, Tb)
-constexpr int kNumBars = 12;
+constexpr int B_TG = 12;    // layer mode: TMA of the chunk's g tile (chain group)
+constexpr int kNumBars = 13;
 
 // ---- TMEM column map (512 columns) -----------------------------------------
 constexpr uint32_t TM_ST = 0;    // state X^T (lane c, column j), fp32
@@ -149,6 +150,7 @@ __device__ __forceinline__ uint32_t tile_chunk(int rows, int i, int cc) {
 struct Params {
     CUtensorMap tm_q, tm_k, tm_v;     // [T][H*128] bf16 with boxes of 32 tokens x 64 channels
     CUtensorMap tm_qh, tm_kh, tm_vh;  // layer mode: the same tensors, boxes of 8 tokens
+    CUtensorMap tm_g;                 // layer mode: g [T][H*128] bf16, boxes of 32 tokens x 128
     const float *log_alpha, *beta, *S0;
     const int32_t *cu_seqlens;
     int H;
@@ -728,6 +730,24 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
     }
     tmem_wait_st();
 
+    // Layer mode: the chunk's g tile arrives by TMA in the staging buffer's place
+    // (the gated output is stored directly); chunk c+1's tile is requested once
+    // chunk c's readout has read its own.
+    int g_issued = 0;
+    auto issue_g = [&](int t0g) {
+        if (tid == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar + B_TG, kC * kD * 2);
+            tma_load_2d(smem_u32(sm + S_STG), &p.tm_g, h * kD, t0g, bar + B_TG);
+        }
+    };
+    if constexpr (kLayer) {
+        if (nchunks > 0) {
+            issue_g(t_begin);
+            g_issued = 1;
+        }
+    }
+
     // bf16 output: a finished chunk is staged row-major in shared memory and
     // copied out with 16-byte stores while the next chunk's M3 runs.
     __nv_bfloat16 *stg = reinterpret_cast<__nv_bfloat16 *>(sm + S_STG);
@@ -763,18 +783,6 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             alive = group_and(kChainBar, ok);
             fence_after_sync();
             if (!alive) break;
-        }
-
-        uint32_t gw[16];  // layer mode: g of rows 2i, 2i+1 for this thread's channel (bf16 pair)
-        if constexpr (kLayer) {
-            const unsigned short *gsrc =
-                reinterpret_cast<const unsigned short *>(p.g) + ((size_t)t0 * H + h) * kD + c_lane;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint32_t lo = 2 * i < nrow ? gsrc[(size_t)(2 * i) * H * kD] : 0u;
-                const uint32_t hi = 2 * i + 1 < nrow ? gsrc[(size_t)(2 * i + 1) * H * kD] : 0u;
-                gw[i] = lo | (hi << 16);
-            }
         }
 
         // ---- Tb = T diag(beta) (32 rows x K 32): one 16-byte chunk per thread ----
@@ -911,7 +919,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                                 id, 1);
             mma_commit(bar + (tid == kCA ? B_CA : B_CB));
         }
-        if constexpr (sizeof(Tout) == 2) copy_out();  // previous chunk, while M3 runs
+        if constexpr (sizeof(Tout) == 2 && !kLayer) copy_out();  // previous chunk, while M3 runs
         {
             bool ok = true;
             if (tid == kCA || tid == kCB)
@@ -1005,18 +1013,45 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                 }
                 float *gate = reinterpret_cast<float *>(sm + S_GATE);
                 gate[warp * 32 + (c_lane & 31)] = b[0];
-                group_sync(kChainBar);
+                bool ok = true;
+                if (tid == 0) ok = wait_one(bar + B_TG, c & 1, p.status, 25);  // chunk c's g tile
+                ok = group_and(kChainBar, ok);
+                if (!ok) {
+                    alive = false;
+                    break;
+                }
                 if (tid < 32)
                     gate[128 + tid] = rsqrtf((gate[tid] + gate[32 + tid] + gate[64 + tid] + gate[96 + tid]) *
                                                  (1.f / kD) + p.rms_eps);
                 group_sync(kChainBar);
+                const unsigned short *gs = reinterpret_cast<const unsigned short *>(sm + S_STG);
 #pragma unroll
-                for (int r = 0; r < 32; ++r) {
-                    const uint32_t gb = (r & 1) ? (gw[r >> 1] & 0xFFFF0000u) : (gw[r >> 1] << 16);
-                    a[r] *= sigmoid_(__uint_as_float(gb)) * gate[128 + r];
+                for (int r = 0; r < 32; ++r)
+                    a[r] *= sigmoid_(__uint_as_float((uint32_t)gs[r * kD + c_lane] << 16)) * gate[128 + r];
+                group_sync(kChainBar);  // every read of the g tile is done
+                if constexpr (sizeof(Tout) == 2) {
+                    // stage the gated rows in the g tile's place, then 16-byte stores
+#pragma unroll
+                    for (int r = 0; r < 32; ++r) stg[r * kD + c_lane] = __float2bfloat16_rn(a[r]);
+                    group_sync(kChainBar);
+                    for (int e = tid; e < kC * 16; e += 128) {
+                        const int r = e >> 4, chn = e & 15;
+                        if (r < nrow)
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(o) +
+                                                       ((size_t)(t0 + r) * H + h) * kD + 8 * chn) =
+                                *reinterpret_cast<const uint4 *>(stg + r * kD + 8 * chn);
+                    }
+                    group_sync(kChainBar);  // the staged rows are out
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 32; ++r)
+                        if (r < nrow) o[((size_t)(t0 + r) * H + h) * kD + c_lane] = a[r];
                 }
-            }
-            if constexpr (sizeof(Tout) == 2) {
+                if (c + 1 < nchunks) {
+                    issue_g(t0 + kC);
+                    g_issued = c + 2;
+                }
+            } else if constexpr (sizeof(Tout) == 2) {
 #pragma unroll
                 for (int r = 0; r < 32; ++r) stg[r * kD + c_lane] = __float2bfloat16_rn(a[r]);
                 pend_t0 = t0;
@@ -1028,8 +1063,12 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             }
         }
     }
-    if constexpr (sizeof(Tout) == 2) {
+    if constexpr (sizeof(Tout) == 2 && !kLayer) {
         if (alive) copy_out();
+    }
+    if constexpr (kLayer) {  // a g tile still in flight (only after an early exit) must land first
+        if (tid == 0 && !alive && g_issued > 0)  // at most the last one is outstanding
+            mbar_wait_bounded(bar + B_TG, (g_issued - 1) & 1, kWaitNs);
     }
 
     // ---- final state S = Diag(e31_last) X (lane c, column j) -> S_final[j][c] ----
@@ -1156,7 +1195,9 @@ cudaError_t launch_layer_typed(const LayerArgs &a, cudaStream_t stream) {
         const int T = a.total_tokens, H = a.num_heads;
         if (!encode_bf16_tiles(&p.tm_q, a.qp, T, H, kC) || !encode_bf16_tiles(&p.tm_k, a.kp, T, H, kC) ||
             !encode_bf16_tiles(&p.tm_v, a.vp, T, H, kC) || !encode_bf16_tiles(&p.tm_qh, a.qp, T, H, 8) ||
-            !encode_bf16_tiles(&p.tm_kh, a.kp, T, H, 8) || !encode_bf16_tiles(&p.tm_vh, a.vp, T, H, 8))
+            !encode_bf16_tiles(&p.tm_kh, a.kp, T, H, 8) || !encode_bf16_tiles(&p.tm_vh, a.vp, T, H, 8) ||
+            !encode_map(&p.tm_g, a.g, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, H, kD, kC,
+                        CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
     p.S0 = a.S0;
