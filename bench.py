@@ -50,8 +50,8 @@ LAYER_BYTES_PER_TOKEN_HEAD = 5 * D * 2 + 2 + D * 2                      # 1,538 
 # was taken on: a changed kernel reports traffic null until it is captured again.
 TRAFFIC = {
     "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-                "13d81302384eda6d23b6768243c093f1de5ee19aaf41f4412476cdf437a8c986",
-                (252.565504e6 + 37.732608e6) / (2048 * 96)),
+                "50100b653639c091678c8aaf6614e1e295c9b60a9917387290fd0d011959cd1b",
+                (252.773888e6 + 38.073344e6) / (2048 * 96)),
     "decode": ("gated_delta_rule_kda_gb300/csrc/kda_decode.cu",
                "1bf0e4585307540aec99de0bebe444ea914f399db22eb7540d6128919bfb40b0",
                (205.3e6 + 142.4e6) / (32 * 96)),
@@ -394,6 +394,15 @@ def run_only(args, local):
         fn = lambda: kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta,
                                      inp.cu_seqlens, None, o=o, S_final=Sf)
         units = T
+    elif args.only == "layer":
+        lens = [2048] if args.small else synthetic.varlen_lengths(seed=synthetic.BASE_SEED + 5)
+        linp = synthetic.layer_inputs(lens, 96, seed=synthetic.BASE_SEED + 5, device=dev)
+        LT = linp.qp.shape[0]
+        og = torch.empty((LT, 96, D), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_layer_core_fused(linp.qp, linp.kp, linp.vp, linp.conv_w, linp.z,
+                                              linp.A, linp.b, linp.beta_logit, linp.g,
+                                              linp.cu_seqlens, None, o=og, want_state=False)
+        units = LT
     else:
         B = 32 if args.small else 256
         dinp = synthetic.decode_inputs(B, 96, torch.bfloat16, device=dev)
@@ -416,7 +425,7 @@ def main():
     ap.add_argument("--skip-layer-core", action="store_true")
     ap.add_argument("--skip-staged-layer-core", action="store_true",
                     help="time only the fused layer core, not the three-launch composition")
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "layer"], default=None,
                     help="profiling aid: run just this kernel (no baseline, no e2e)")
     ap.add_argument("--small", action="store_true",
                     help="with --only: a smaller case sized for ncu captures")
