@@ -149,12 +149,21 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time (every rank gets it).  The tensor lives where the
+    process group's backend expects it: on the GPU for NCCL, on the host for gloo."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_rate(units_per_rank_step: float, ms_per_step_max: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas (weak scaling): every rank processes
+    the same units per step; the job's step time is the slowest rank's."""
+    return world * units_per_rank_step / (ms_per_step_max / 1e3)
 
 
 def time_launches(fn, steps, warmup, world):
@@ -258,7 +267,7 @@ def run_ours(args, world, rank, local):
     clk = clocks.stop()
     ms_step = max_over_ranks(total_ms / args.steps, world)
     tokens_per_step = T
-    value = world * tokens_per_step / (ms_step / 1e3)
+    value = aggregate_rate(tokens_per_step, ms_step, world)
     launch_ms = sum(per) / len(per)
     alg_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
     alg_flop = T * H * PREFILL_FLOP_PER_TOKEN_HEAD
@@ -290,7 +299,7 @@ def run_ours(args, world, rank, local):
     e2e_steps = max(2, min(args.steps, 5))
     e2e_total, _ = time_launches(e2e_step, e2e_steps, 1, world)
     e2e_ms = max_over_ranks(e2e_total / e2e_steps, world)
-    e2e = {"value": world * tokens_per_step / (e2e_ms / 1e3), "unit": UNIT,
+    e2e = {"value": aggregate_rate(tokens_per_step, e2e_ms, world), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
     del host, o_host, S_host
 
@@ -309,7 +318,7 @@ def run_ours(args, world, rank, local):
     units = 256 * 96
     d_bytes = units * DECODE_BYTES_PER_UNIT
     d_ach = d_bytes / (d_launch / 1e3) / 1e9
-    decode = {"tokens_per_s": world * 256 / (d_ms / 1e3), "ms_per_step": d_ms,
+    decode = {"tokens_per_s": aggregate_rate(256, d_ms, world), "ms_per_step": d_ms,
               "roofline": {"bound": "hbm", "achieved": d_ach, "peak": hbm, "unit": "GB/s",
                            "frac": d_ach / hbm, "traffic": traffic_bytes("decode", units),
                            "peak_kind": peak_kind,
@@ -333,7 +342,7 @@ def run_ours(args, world, rank, local):
         l_steps = max(1, min(args.steps, 10))
         l_total, _ = time_launches(fused_step, l_steps, args.warmup, world)
         l_ms = max_over_ranks(l_total / l_steps, world)
-        layer = {"tokens_per_s": world * LT / (l_ms / 1e3), "ms_per_step": l_ms,
+        layer = {"tokens_per_s": aggregate_rate(LT, l_ms, world), "ms_per_step": l_ms,
                  "tokens": LT, "workload": "16 sequences, lengths log-uniform in [1K, 64K], "
                                            "96 heads, front end + recurrence + gate",
                  "entry_point": "kda_layer_core_fused", "launches_per_step": 1,
@@ -350,7 +359,8 @@ def run_ours(args, world, rank, local):
             s_total, _ = time_launches(staged_step, 2, 1, world)
             s_ms = max_over_ranks(s_total / 2, world)
             layer["staged"] = {"entry_point": "kda_layer_core", "ms_per_step": s_ms,
-                               "tokens_per_s": world * LT / (s_ms / 1e3), "launches_per_step": 3}
+                               "tokens_per_s": aggregate_rate(LT, s_ms, world),
+                               "launches_per_step": 3}
             del ws
         del linp, og, Sl
         torch.cuda.empty_cache()
