@@ -373,8 +373,8 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
 
         // ---- F2/F3: decay and operands, thread = 4 rows x 4 channels (4 q4 .. 4 q4 + 3).
         //      D (log2 units): rows 0..15 prefix - prefix_15, rows 16..31 the sum of rows
-        //      16..r (two scan segments of 4 row groups).  Then [k E ; q E] -> wx,
-        //      (and wq rows 0..31), R = k E^-1 -> rr, Q~ = q E em -> wq rows 32.. ----
+        //      16..r (two scan segments of 4 row groups).  Then [k E ; q E] -> wx and
+        //      R = k E^-1 -> rr (the Gram's operands) ----
         {
             const int cc = q4 >> 1, hb = (q4 & 1) * 8;
             float qh[4][4], kh[4][4];  // layer mode: q^, k^ of rows 4 rg + k
@@ -539,22 +539,18 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                     bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + KO + tile_chunk(32, r, cc) + hb), kv);
                     bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + QO + tile_chunk(32, r, cc) + hb), qv);
                 }
-                float xk[4], xq[4], xr[4], xt[4];
+                float xk[4], xq[4], xr[4];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const float E = ex2_approx(dv[t]), EI = ex2_approx(-dv[t]);
                     xk[t] = kv[t] * E;    // k E
                     xq[t] = qv[t] * E;    // q E
                     xr[t] = kv[t] * EI;   // k E^-1
-                    xt[t] = xq[t] * em4[t];  // Q~ = q E em
                 }
                 uint2 h2, l2;
                 split2(xk[0], xk[1], h2.x, l2.x);
                 split2(xk[2], xk[3], h2.y, l2.y);
                 unsigned char *dst = wx + tile_chunk(64, r, cc) + hb;
-                *reinterpret_cast<uint2 *>(dst) = h2;
-                *reinterpret_cast<uint2 *>(dst + 16384) = l2;
-                dst = wq + tile_chunk(64, r, cc) + hb;  // k E for M2b, until W replaces it
                 *reinterpret_cast<uint2 *>(dst) = h2;
                 *reinterpret_cast<uint2 *>(dst + 16384) = l2;
                 split2(xq[0], xq[1], h2.x, l2.x);
@@ -567,11 +563,6 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 dst = rr + tile_chunk(32, r, cc) + hb;
                 *reinterpret_cast<uint2 *>(dst) = h2;
                 *reinterpret_cast<uint2 *>(dst + 8192) = l2;
-                split2(xt[0], xt[1], h2.x, l2.x);
-                split2(xt[2], xt[3], h2.y, l2.y);
-                dst = wq + tile_chunk(64, 32 + r, cc) + hb;
-                *reinterpret_cast<uint2 *>(dst) = h2;
-                *reinterpret_cast<uint2 *>(dst + 16384) = l2;
             }
         }
         if (c + 1 < nchunks) {
@@ -604,6 +595,29 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             for (int k = 0; k < 4; ++k)
                 mma_bf16(d, sw128_desc_k(xl, 64, s0 + k), sw128_desc_k(rh, 32, s0 + k), id, 1);
             mma_commit(bar + (tid == kPA ? B_PA : B_PB));
+        }
+        // ---- while M1 runs: wq rows 32.. = Q~ = (q E) em, rebuilt from its hi + lo in wx (the
+        //      Gram only reads wx), and wq rows 0..31 = k E for M2b ----
+        {
+            const int cc = q4 >> 1, hb = (q4 & 1) * 8;
+            const float4 em4 = *reinterpret_cast<const float4 *>(em_s + 4 * q4);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int kk = kLayer ? k : (k + (rg >> 1)) & 3;
+                const int r = 4 * rg + kk;
+                const uint32_t oq = tile_chunk(64, 32 + r, cc) + hb, ok2 = tile_chunk(64, r, cc) + hb;
+                float qh4[4], ql4[4];
+                bf16x4_to_f32(*reinterpret_cast<const uint2 *>(wx + oq), qh4);
+                bf16x4_to_f32(*reinterpret_cast<const uint2 *>(wx + 16384 + oq), ql4);
+                uint2 h2, l2;
+                split2((qh4[0] + ql4[0]) * em4.x, (qh4[1] + ql4[1]) * em4.y, h2.x, l2.x);
+                split2((qh4[2] + ql4[2]) * em4.z, (qh4[3] + ql4[3]) * em4.w, h2.y, l2.y);
+                *reinterpret_cast<uint2 *>(wq + oq) = h2;
+                *reinterpret_cast<uint2 *>(wq + 16384 + oq) = l2;
+                *reinterpret_cast<uint2 *>(wq + ok2) = *reinterpret_cast<const uint2 *>(wx + ok2);
+                *reinterpret_cast<uint2 *>(wq + 16384 + ok2) =
+                    *reinterpret_cast<const uint2 *>(wx + 16384 + ok2);
+            }
         }
         {
             bool ok = true;
