@@ -580,7 +580,8 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             issued = c + 2;
         }
         if (tid == kPA || tid == kPB) {  // M1: Gram, K steps split over the two issuers
-            const uint32_t id = idesc_bf16_f32(128, 32);
+            // M = 64 ([k E ; q E] has 64 rows): D row m lands in TMEM lane 32 (m / 16) + m % 16
+            const uint32_t id = idesc_bf16_f32(64, 32);
             const int s0 = tid == kPA ? 0 : 4;
             const uint32_t d = tb + (tid == kPA ? TM_DG : TM_DU);
             const uint32_t xh = smem_u32(wx), xl = xh + 16384;
@@ -630,14 +631,17 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         }
 
         // ---- F5: A (k rows, scaled by beta, strictly lower; stored column-major) and
-        //      P (q rows, lower); lanes 0-63, each of the two warps of a lane quarter
-        //      takes 16 columns ----
-        if (quarter < 2) {
+        //      P (q rows, lower).  The M = 64 Gram holds its rows in lanes 0-15 of each lane
+        //      quarter: quarters 0-1 the k rows 0-15 / 16-31, quarters 2-3 the q rows; each of
+        //      the two warps of a quarter takes 16 columns ----
+        {
             float g[16], g2[16];
             tmem_ld16(tl + TM_DG + 16 * half, g);
             tmem_ld16(tl + TM_DU + 16 * half, g2);
-            const int r = lane;
-            if (quarter == 0) {
+            const int r = 16 * (quarter & 1) + lane;
+            if (lane >= 16) {
+                // lanes 16-31 of each quarter hold no Gram rows
+            } else if (quarter < 2) {
                 const float br = beta_s[r];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
