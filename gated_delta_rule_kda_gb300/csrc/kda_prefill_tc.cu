@@ -696,15 +696,15 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 x0 = fmaf(sAt[m * 32 + 16 + r], sT[m * kLdT + i], x0);
                 x1 = fmaf(sAt[(m + 1) * 32 + 16 + r], sT[(m + 1) * kLdT + i], x1);
             }
-            sT[(16 + r) * kLdT + i] = x0 + x1;  // X = A_10 T_00 in the T_10 slot
+            // X = A_10 T_00 (row r, column i) goes to T's upper-right block, which T never uses
+            sT[r * kLdT + 16 + i] = x0 + x1;
             group_sync(kPrepBar);
             float y0 = 0.f, y1 = 0.f;
 #pragma unroll
             for (int m = 0; m < 16; m += 2) {
-                y0 = fmaf(sT[(16 + r) * kLdT + 16 + m], sT[(16 + m) * kLdT + i], y0);
-                y1 = fmaf(sT[(16 + r) * kLdT + 17 + m], sT[(17 + m) * kLdT + i], y1);
+                y0 = fmaf(sT[(16 + r) * kLdT + 16 + m], sT[m * kLdT + 16 + i], y0);
+                y1 = fmaf(sT[(16 + r) * kLdT + 17 + m], sT[(m + 1) * kLdT + 16 + i], y1);
             }
-            group_sync(kPrepBar);
             sT[(16 + r) * kLdT + i] = -(y0 + y1);
         }
         fence_proxy_async_smem();  // P (written after the last publish) is an MMA operand
