@@ -179,16 +179,17 @@ __device__ __forceinline__ void bf16x4_to_f32(uint2 u, float (&x)[4]) {
     x[3] = __uint_as_float(u.y & 0xFFFF0000u);
 }
 
-// Store 8 fp32 values as a hi 16-byte chunk and a lo 16-byte chunk.
+// Store 8 fp32 values as a hi 16-byte chunk and a lo 16-byte chunk; with lo_first the lo
+// chunk is stored by the first of the two instructions.
 __device__ __forceinline__ void store_split_chunk(unsigned char *hi, unsigned char *lo,
-                                                  const float (&x)[8]) {
+                                                  const float (&x)[8], bool lo_first = false) {
     uint4 h, l;
     split2(x[0], x[1], h.x, l.x);
     split2(x[2], x[3], h.y, l.y);
     split2(x[4], x[5], h.z, l.z);
     split2(x[6], x[7], h.w, l.w);
-    *reinterpret_cast<uint4 *>(hi) = h;
-    *reinterpret_cast<uint4 *>(lo) = l;
+    *reinterpret_cast<uint4 *>(lo_first ? lo : hi) = lo_first ? l : h;
+    *reinterpret_cast<uint4 *>(lo_first ? hi : lo) = lo_first ? h : l;
 }
 
 // ---- group synchronisation (128-thread named barriers) ----------------------
@@ -449,11 +450,15 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                     }
                 // ---- v (fp32) -> V hi over the v^p tile, V lo over the q^p tile ----
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int r = 4 * rg + k;
+                for (int k = 0; k < 4; ++k) {  // rows in the order of F2/F3 (bank groups)
+                    const bool sw = (rg & 2) != 0;
+                    const int r = 4 * rg + (k ^ (rg & 2));
+                    float vv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) vv[e] = sw ? y[2][k ^ 2][e] : y[2][k][e];
                     uint2 h2, l2;
-                    split2(y[2][k][0], y[2][k][1], h2.x, l2.x);
-                    split2(y[2][k][2], y[2][k][3], h2.y, l2.y);
+                    split2(vv[0], vv[1], h2.x, l2.x);
+                    split2(vv[2], vv[3], h2.y, l2.y);
                     unsigned char *qkvw = const_cast<unsigned char *>(qkv);
                     *reinterpret_cast<uint2 *>(qkvw + VO + tile_chunk(32, r, cc) + hb) = h2;
                     *reinterpret_cast<uint2 *>(qkvw + QO + tile_chunk(32, r, cc) + hb) = l2;
@@ -519,21 +524,22 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 *reinterpret_cast<float4 *>(e31_s + 4 * q4) = e31;
                 e31_prev = e31;
             }
-            // bf16 inputs: row order rotated by rg >> 1 so that the 8 rows a warp stores at
-            // once sit in 8 distinct swizzle positions (layer mode keeps q^, k^ in registers
-            // and takes the rows in order).
+            // Row order: threads with bit 1 of rg set take their rows in the order 2, 3, 0, 1,
+            // so that the four rows a half-warp stores at once (8-byte accesses are served a
+            // half-warp at a time) fall in four distinct 32-byte bank groups of the swizzled tile.
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int kk = kLayer ? k : (k + (rg >> 1)) & 3;
+                const bool sw = (rg & 2) != 0;
+                const int kk = k ^ (rg & 2);
                 const int r = 4 * rg + kk;
-                const float4 pk = kk == 0 ? pre[0] : kk == 1 ? pre[1] : kk == 2 ? pre[2] : pre[3];
+                const float4 pk = sw ? pre[k ^ 2] : pre[k];
                 const float dv[4] = {base.x + pk.x, base.y + pk.y, base.z + pk.z, base.w + pk.w};
                 float kv[4], qv[4];
                 if constexpr (kLayer) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        kv[e] = kh[k][e];
-                        qv[e] = qh[k][e];
+                        kv[e] = sw ? kh[k ^ 2][e] : kh[k][e];
+                        qv[e] = sw ? qh[k ^ 2][e] : qh[k][e];
                     }
                 } else {
                     bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + KO + tile_chunk(32, r, cc) + hb), kv);
@@ -604,8 +610,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             const float4 em4 = *reinterpret_cast<const float4 *>(em_s + 4 * q4);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int kk = kLayer ? k : (k + (rg >> 1)) & 3;
-                const int r = 4 * rg + kk;
+                const int r = 4 * rg + (k ^ (rg & 2));  // the row order of F2/F3
                 const uint32_t oq = tile_chunk(64, 32 + r, cc) + hb, ok2 = tile_chunk(64, r, cc) + hb;
                 float qh4[4], ql4[4];
                 bf16x4_to_f32(*reinterpret_cast<const uint2 *>(wx + oq), qh4);
@@ -812,8 +817,10 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                 const int i = 8 * cc + e;
                 x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
             }
+            // a quarter-warp holds rows r and r + 1: odd rows store their lo chunk first, so
+            // that each instruction's 8 chunks fall in 8 distinct 16-byte bank groups
             store_split_chunk(sm + S_TB + sw128_chunk_offset(32, r, cc),
-                              sm + S_TB + sw128_chunk_offset(32, r, 4 + cc), x);
+                              sm + S_TB + sw128_chunk_offset(32, r, 4 + cc), x, (r & 1) != 0);
         }
         publish(kChainBar);
         if (tid == kCA) {  // M2: U~^T = V^T Tb^T  (V read MN-major: exact bf16, or hi + lo)
@@ -855,11 +862,19 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
         }
 
         // ---- F4 (while M2 and M2b run): S0 = Diag(e31_prev) X -> M3's A operand (hi | lo);
-        //      X <- Diag(em) S0 ----
+        //      X <- Diag(em) S0.  After the first quarter each issuer waits for its own
+        //      products, and M2's issuer releases slot s's v tile and beta (Tb read beta
+        //      before M2 was issued), so that the prep group can stage the chunk after next
+        //      early ----
+        bool m2_ok = true;
         {
             const float *e31p = vec + 2 * kD + s * kD;
 #pragma unroll
             for (int part = 0; part < 4; ++part) {
+                if (part == 1 && (tid == kCA || tid == kCB)) {
+                    m2_ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p.status, 24);
+                    if (m2_ok && tid == kCA) mbar_arrive(bar + B_VFREE + s);
+                }
                 const int j0 = 32 * part;
                 float sv[32];
                 tmem_ld32(tl + TM_ST + j0, sv);
@@ -885,16 +900,12 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                 tmem_st32(tl + TM_ST + j0, yv);
             }
         }
-        // ---- M2 and M2b done: slot s's v tile and beta are free ----
+        // ---- M2 and M2b done (W'^T is read next) ----
         {
-            bool ok = true;
-            if (tid == kCA || tid == kCB)
-                ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p.status, 24);
             ++ph;
-            alive = group_and(kChainBar, ok);
+            alive = group_and(kChainBar, m2_ok);
             fence_after_sync();
             if (!alive) break;
-            if (tid == 0) mbar_arrive(bar + B_VFREE + s);
         }
         // ---- F7: W = W' Diag(em) -> rows 0..31 of wq (the k E rows are dead); thread = key
         //      channel j ----
