@@ -127,14 +127,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+// One try: the thread may sleep until the phase completes, for at most about 100 us (the
+// suspend-time hint), so that a waiting thread takes few issue slots from working warps.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}\n"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
         : "memory");
     return ok != 0;
 }
@@ -150,7 +152,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-        for (int i = 0; i < 64; ++i)
+        for (int i = 0; i < 4; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > limit_ns) return false;
     }
