@@ -167,3 +167,33 @@ def test_fused_deterministic(kda):
                                      inp.beta_logit, inp.g, inp.cu_seqlens, None)
     torch.cuda.synchronize()
     assert torch.equal(a, b) and torch.equal(Sa, Sb)
+
+
+def test_fused_sequences_shorter_than_the_convolution(kda):
+    """Sequences of 1 to 5 tokens (shorter than or equal to the width-4 convolution, so
+    the zero history before each start matters on every row) beside 8, 9 and 40, with a
+    carried state."""
+    inp = synthetic.layer_inputs([2, 3, 1, 4, 5, 8, 9, 40], 3, seed=46, s0_std=0.1, device="cuda")
+    og, Sf = kda.kda_layer_core_fused(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b,
+                                      inp.beta_logit, inp.g, inp.cu_seqlens, inp.S0,
+                                      out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status()[0] == 0
+    ref_o, ref_S, ref_ot = oracle_layer_core(inp)
+    assert_gated_close(to64(og), ref_o, ref_ot, False)
+    assert_close(to64(Sf), ref_S, TOL_BF16, "S_final")
+
+
+def test_fused_many_heads_several_waves(kda):
+    """H=160 heads x 2 sequences = 320 CTAs (several waves of the grid), lengths 70 and 41
+    (history boxes across chunk boundaries); oracle on four heads, the last included."""
+    inp = synthetic.layer_inputs([70, 41], 160, seed=47, s0_std=0.1, device="cuda")
+    og, Sf = kda.kda_layer_core_fused(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b,
+                                      inp.beta_logit, inp.g, inp.cu_seqlens, inp.S0,
+                                      out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status()[0] == 0
+    heads = [0, 63, 152, 159]
+    ref_o, ref_S, ref_ot = oracle_layer_core(inp, heads)
+    assert_gated_close(to64(og[:, heads]), ref_o, ref_ot, True)
+    assert_close(to64(Sf[:, heads]), ref_S, TOL_BF16, "S_final")

@@ -170,3 +170,20 @@ def test_long_prefill_carried_state_sampled_heads(kda, x_mean):
     inp = synthetic.prefill_inputs([131072], 96, torch.bfloat16, seed=synthetic.BASE_SEED + 4,
                                    x_mean=x_mean, x_std=1.0, s0_std=0.1, device="cuda")
     check(kda, inp, TOL_BF16, torch.float32, heads=HEADS)
+
+
+def test_many_heads_several_waves(kda):
+    """H=200 heads x 2 sequences = 400 CTAs, more than one CTA per SM (several waves of
+    the grid); lengths 95 and 32 (a full last chunk).  Oracle on five heads spread over
+    the grid, the last head included."""
+    inp = synthetic.prefill_inputs([95, 32], 200, torch.bfloat16, seed=26, s0_std=0.1,
+                                   device="cuda")
+    check(kda, inp, TOL_BF16, torch.float32, heads=[0, 1, 99, 151, 199])
+
+
+@pytest.mark.parametrize("lens", [[31], [32], [33], [63, 64, 65]])
+def test_chunk_boundaries(kda, lens):
+    """Lengths one short of, equal to and one past a 32-token chunk (the kernel's chunk):
+    the last chunk holds 31, 32 or 1 rows."""
+    inp = synthetic.prefill_inputs(lens, 2, torch.bfloat16, seed=27, s0_std=0.1, device="cuda")
+    check(kda, inp, TOL_BF16, torch.float32)
