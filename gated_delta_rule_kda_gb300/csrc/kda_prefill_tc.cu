@@ -79,6 +79,7 @@ using namespace tc;
 constexpr int kC = 32;
 constexpr int kThreads = 384;  // chain group: warps 0-3, prep group: warps 4-11
 constexpr uint64_t kWaitNs = 2000000000ull;  // bound on every wait
+constexpr int kMaxOrderedSeqs = 64;  // longest-first CTA order for up to this many sequences
 
 // ---- shared memory map (bytes from a 1024-aligned base) --------------------
 // q, k, v tiles (bf16 [32][128], two 64-column blocks with 128-byte swizzle, as
@@ -1125,9 +1126,22 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S_TSLOT);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int H = p.H;
-    const int h = blockIdx.x % H, n = blockIdx.x / H;
-    const int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
-    const int nchunks = t_end > t_begin ? (t_end - t_begin + kC - 1) / kC : 0;
+    const int h = blockIdx.x % H, r = blockIdx.x / H;
+    // CTA r x H + h takes the r-th longest sequence (ties in index order): blocks start
+    // roughly in index order, so the longest (sequence, head) units start in the first
+    // wave and shorter ones fill in behind them.  Thread j < N ranks sequence j.
+    const int nseq = gridDim.x / H;
+    const bool ordered = nseq > 1 && nseq <= kMaxOrderedSeqs;
+    int *nslot = reinterpret_cast<int *>(sm + S_TSLOT + 4);
+    if (ordered && tid < nseq) {
+        const int len = p.cu_seqlens[tid + 1] - p.cu_seqlens[tid];
+        int rank = 0;
+        for (int j = 0; j < nseq; ++j) {
+            const int lj = p.cu_seqlens[j + 1] - p.cu_seqlens[j];
+            rank += (lj > len || (lj == len && j < tid)) ? 1 : 0;
+        }
+        if (rank == r) *nslot = tid;  // ranks are a permutation: exactly one writer
+    }
 
     if (warp == 0) {
         tmem_alloc(tslot, 512);
@@ -1141,6 +1155,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     __syncthreads();
     fence_after_sync();
     const uint32_t tb = *tslot;
+    const int n = ordered ? *nslot : r;
+    const int t_begin = p.cu_seqlens[n], t_end = p.cu_seqlens[n + 1];
+    const int nchunks = t_end > t_begin ? (t_end - t_begin + kC - 1) / kC : 0;
 
     if (warp >= 4)
         prep_group<kLayer>(p, sm, tb, h, t_begin, t_end, nchunks);
