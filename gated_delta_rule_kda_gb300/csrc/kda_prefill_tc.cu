@@ -415,7 +415,10 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                         }
                 }
                 // ---- L2 norms of q and k per (token, head) row: 4 lanes, then 8 warps ----
-                float* part = sAt;  // [2][32 rows][8 warps]; A is not in use here
+                // [2][32 rows][8 warps]; A is not in use here.  Warp w's partial of row r sits in
+                // word w ^ rg of the row, so that the eight row groups storing at once hit eight
+                // banks; a row's reader sums all eight words, in either half order.
+                float* part = sAt;
                 float ss[2][4];
 #pragma unroll
                 for (int X = 0; X < 2; ++X)
@@ -433,15 +436,17 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
 #pragma unroll
                     for (int X = 0; X < 2; ++X)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) part[(X * 32 + 4 * rg + k) * 8 + (pt >> 5)] = ss[X][k];
+                        for (int k = 0; k < 4; ++k) part[(X * 32 + 4 * rg + k) * 8 + ((pt >> 5) ^ rg)] = ss[X][k];
                 }
                 group_sync(kPrepBar);  // partials complete; every raw tile read is done
 #pragma unroll
                 for (int X = 0; X < 2; ++X)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float4 a = *reinterpret_cast<const float4 *>(part + (X * 32 + 4 * rg + k) * 8);
-                        const float4 b = *reinterpret_cast<const float4 *>(part + (X * 32 + 4 * rg + k) * 8 + 4);
+                        // odd row groups read the upper half first (rows 4 apart share banks)
+                        const float *row = part + (X * 32 + 4 * rg + k) * 8;
+                        const float4 a = *reinterpret_cast<const float4 *>(row + 4 * (rg & 1));
+                        const float4 b = *reinterpret_cast<const float4 *>(row + 4 * ((rg & 1) ^ 1));
                         const float inv = rsqrtf(((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w)) + p.l2_eps);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
