@@ -85,14 +85,13 @@ constexpr int kMaxOrderedSeqs = 64;  // longest-first CTA order for up to this m
 // q, k, v tiles (bf16 [32][128], two 64-column blocks with 128-byte swizzle, as
 // written by TMA) for two chunks.  log_alpha travels through registers.
 constexpr uint32_t S_QKV = 0, QKV_SIZE = 24576, QO = 0, KO = 8192, VO = 16384;
-// Tb (32 rows, K = 32: hi in K steps 0-1, lo in K steps 2-3 of one swizzled tile),
-// built and used by the chain group; A (fp32 [32][32], column-major) for the prep
-// group's solve; T by slot (fp32 [32][33]), written by the solve and read by the
-// chain group.
+// Tb by slot (32 rows, K = 32: hi in K steps 0-1, lo in K steps 2-3 of one swizzled
+// tile), built by the prep group and read by the chain group's M2 / M2b; A (fp32
+// [32][32], column-major) for the prep group's solve; T by slot (fp32 [32][33]).
 constexpr uint32_t S_DT = 2 * QKV_SIZE;
-constexpr uint32_t S_TB = S_DT;
-constexpr uint32_t S_A = S_DT + 4096;
-constexpr uint32_t S_TS = S_DT + 8192;
+constexpr uint32_t S_TB = S_DT, TB_SIZE = 4096;
+constexpr uint32_t S_A = S_DT + 2 * TB_SIZE;
+constexpr uint32_t S_TS = S_A + 4096;
 constexpr int kLdT = 33;
 constexpr uint32_t T_SIZE = 32 * kLdT * 4;
 // [k E ; q E] hi | lo (64 rows), private to the prep group.
@@ -718,7 +717,23 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             }
             sT[(16 + r) * kLdT + i] = -(y0 + y1);
         }
-        fence_proxy_async_smem();  // P (written after the last publish) is an MMA operand
+        group_sync(kPrepBar);
+        // ---- Tb = T diag(beta) (32 rows x K 32) -> slot s: one 16-byte chunk per thread ----
+        if (pt < 128) {
+            const int r = pt >> 2, cc = pt & 3;
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int i = 8 * cc + e;
+                x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
+            }
+            // a quarter-warp holds rows r and r + 1: odd rows store their lo chunk first, so
+            // that each instruction's 8 chunks fall in 8 distinct 16-byte bank groups
+            unsigned char *tbs = sm + S_TB + s * TB_SIZE;
+            store_split_chunk(tbs + sw128_chunk_offset(32, r, cc), tbs + sw128_chunk_offset(32, r, 4 + cc),
+                              x, (r & 1) != 0);
+        }
+        fence_proxy_async_smem();  // wq, P and Tb are MMA operands of the chain group
         group_sync(kPrepBar);
         if (tid == kPA) mbar_arrive(bar + B_FULL + s);
     }
@@ -801,8 +816,6 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
         const unsigned char *rr = sm + S_R + s * R_SIZE;
         const unsigned char *pp = sm + S_P + s * P_SIZE;
         const unsigned char *qkv = sm + S_QKV + s * QKV_SIZE;
-        const float *beta_s = reinterpret_cast<const float *>(sm + S_BETA + 128 * s);
-        const float *sT = reinterpret_cast<const float *>(sm + S_TS + s * T_SIZE);
         const float *em = vec + s * kD;
 
         // ---- the prep group has filled slot s ----
@@ -814,23 +827,9 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             if (!alive) break;
         }
 
-        // ---- Tb = T diag(beta) (32 rows x K 32): one 16-byte chunk per thread ----
-        {
-            const int r = tid >> 2, cc = tid & 3;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = 8 * cc + e;
-                x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
-            }
-            // a quarter-warp holds rows r and r + 1: odd rows store their lo chunk first, so
-            // that each instruction's 8 chunks fall in 8 distinct 16-byte bank groups
-            store_split_chunk(sm + S_TB + sw128_chunk_offset(32, r, cc),
-                              sm + S_TB + sw128_chunk_offset(32, r, 4 + cc), x, (r & 1) != 0);
-        }
-        publish(kChainBar);
+        // (Tb, W's k E and Q~ came with the slot: the prep group published them)
         if (tid == kCA) {  // M2: U~^T = V^T Tb^T  (V read MN-major: exact bf16, or hi + lo)
-            const uint32_t th = smem_u32(sm + S_TB);
+            const uint32_t th = smem_u32(sm + S_TB + s * TB_SIZE);
             const uint32_t idv = idesc_bf16_f32(128, 32) | kIdescAMN;
             const uint32_t va = smem_u32(qkv + VO);
 #pragma unroll
@@ -850,7 +849,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             }
             mma_commit(bar + B_CA);
         } else if (tid == kCB) {  // M2b: W'^T = (k E)^T Tb^T, k E (wq rows 0-31) read MN-major
-            const uint32_t th = smem_u32(sm + S_TB);
+            const uint32_t th = smem_u32(sm + S_TB + s * TB_SIZE);
             const uint32_t idw = idesc_bf16_f32(128, 32) | kIdescAMN;
             const uint32_t xh = smem_u32(wq), xl = xh + 16384;
 #pragma unroll
