@@ -96,7 +96,9 @@ constexpr int kLdT = 33;
 constexpr uint32_t T_SIZE = 32 * kLdT * 4;
 // [k E ; q E] hi | lo (64 rows), private to the prep group.
 constexpr uint32_t S_WX = (S_TS + 2 * T_SIZE + 1023) & ~1023u;
-// Per slot: [W ; Q~] hi | lo (64 rows; rows 0-31 hold k E until W replaces it),
+// Per slot: [W ; Q~]^T hi | lo, key-channel major (128 rows j of 64 elements: W[., j] in
+// elements 0-31, Q~[., j] in 32-63; elements 0-31 hold (k E)^T until W replaces them), so
+// that M3 reads it MN-major and M2b reads (k E)^T K-major,
 // R = k E^-1 hi | lo (32 rows), P (32 rows, K = 32: hi in K steps 0-1, lo in 2-3).
 constexpr uint32_t S_WQ = S_WX + 32768, WQ_SIZE = 32768;
 constexpr uint32_t S_R = S_WQ + 2 * WQ_SIZE, R_SIZE = 16384;
@@ -190,6 +192,17 @@ __device__ __forceinline__ void store_split_chunk(unsigned char *hi, unsigned ch
     split2(x[6], x[7], h.w, l.w);
     *reinterpret_cast<uint4 *>(lo_first ? lo : hi) = lo_first ? l : h;
     *reinterpret_cast<uint4 *>(lo_first ? hi : lo) = lo_first ? h : l;
+}
+
+// Elements e0 .. e0 + 3 (e0 % 4 == 0) of row j of a key-channel-major [128][64] bf16 tile
+// (128-byte swizzle), as hi and lo halves.
+__device__ __forceinline__ void store_t4(unsigned char *tile, int j, int e0, const float (&v)[4]) {
+    uint2 h, l;
+    split2(v[0], v[1], h.x, l.x);
+    split2(v[2], v[3], h.y, l.y);
+    const uint32_t o = (uint32_t)(j * 128 + ((((e0 >> 3) ^ (j & 7))) << 4) + (e0 & 4) * 2);
+    *reinterpret_cast<uint2 *>(tile + o) = h;
+    *reinterpret_cast<uint2 *>(tile + 16384 + o) = l;
 }
 
 // ---- group synchronisation (128-thread named barriers) ----------------------
@@ -532,6 +545,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             // Row order: threads with bit 1 of rg set take their rows in the order 2, 3, 0, 1,
             // so that the four rows a half-warp stores at once (8-byte accesses are served a
             // half-warp at a time) fall in four distinct 32-byte bank groups of the swizzled tile.
+            float kT[4][4];  // bf16 inputs: k E by channel t and loop step k
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const bool sw = (rg & 2) != 0;
@@ -557,6 +571,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                     xk[t] = kv[t] * E;    // k E
                     xq[t] = qv[t] * E;    // q E
                     xr[t] = kv[t] * EI;   // k E^-1
+                    if constexpr (!kLayer) kT[t][k] = xk[t];
                 }
                 uint2 h2, l2;
                 split2(xk[0], xk[1], h2.x, l2.x);
@@ -574,6 +589,17 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 dst = rr + tile_chunk(32, r, cc) + hb;
                 *reinterpret_cast<uint2 *>(dst) = h2;
                 *reinterpret_cast<uint2 *>(dst + 8192) = l2;
+            }
+            if constexpr (!kLayer) {
+                // (k E)^T -> wq elements 4 rg .. 4 rg + 3 of rows j = 4 q4 + t (M2b's A operand;
+                // layer mode writes it during the Gram instead, where it costs no registers here)
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const bool sw = (rg & 2) != 0;
+                    const float v[4] = {sw ? kT[t][2] : kT[t][0], sw ? kT[t][3] : kT[t][1],
+                                        sw ? kT[t][0] : kT[t][2], sw ? kT[t][1] : kT[t][3]};
+                    store_t4(wq, 4 * q4 + t, 4 * rg, v);
+                }
             }
         }
         if (c + 1 < nchunks) {
@@ -608,26 +634,55 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 mma_bf16(d, sw128_desc_k(xl, 64, s0 + k), sw128_desc_k(rh, 32, s0 + k), id, 1);
             mma_commit(bar + (tid == kPA ? B_PA : B_PB));
         }
-        // ---- while M1 runs: wq rows 32.. = Q~ = (q E) em, rebuilt from its hi + lo in wx (the
-        //      Gram only reads wx), and wq rows 0..31 = k E for M2b ----
+        // ---- while M1 runs: Q~ = (q E) em, rebuilt from its hi + lo in wx (the Gram only reads
+        //      wx) -> wq elements 32 + r of rows j; layer mode also (k E)^T -> elements r of rows
+        //      j (M2b's A operand), the hi and lo words of wx's k rows transposed 4 x 4 ----
         {
             const int cc = q4 >> 1, hb = (q4 & 1) * 8;
             const float4 em4 = *reinterpret_cast<const float4 *>(em_s + 4 * q4);
+            float qT[4][4];  // Q~ by channel t and loop step k (row 4 rg + (k ^ (rg & 2)))
+            uint2 kw[2][4];  // k E hi / lo words by loop step k
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int r = 4 * rg + (k ^ (rg & 2));  // the row order of F2/F3
-                const uint32_t oq = tile_chunk(64, 32 + r, cc) + hb, ok2 = tile_chunk(64, r, cc) + hb;
+                const uint32_t oq = tile_chunk(64, 32 + r, cc) + hb;
+                const uint32_t ok2 = tile_chunk(64, r, cc) + hb;
+                if constexpr (kLayer) {
+                    kw[0][k] = *reinterpret_cast<const uint2 *>(wx + ok2);
+                    kw[1][k] = *reinterpret_cast<const uint2 *>(wx + 16384 + ok2);
+                }
                 float qh4[4], ql4[4];
                 bf16x4_to_f32(*reinterpret_cast<const uint2 *>(wx + oq), qh4);
                 bf16x4_to_f32(*reinterpret_cast<const uint2 *>(wx + 16384 + oq), ql4);
-                uint2 h2, l2;
-                split2((qh4[0] + ql4[0]) * em4.x, (qh4[1] + ql4[1]) * em4.y, h2.x, l2.x);
-                split2((qh4[2] + ql4[2]) * em4.z, (qh4[3] + ql4[3]) * em4.w, h2.y, l2.y);
-                *reinterpret_cast<uint2 *>(wq + oq) = h2;
-                *reinterpret_cast<uint2 *>(wq + 16384 + oq) = l2;
-                *reinterpret_cast<uint2 *>(wq + ok2) = *reinterpret_cast<const uint2 *>(wx + ok2);
-                *reinterpret_cast<uint2 *>(wq + 16384 + ok2) =
-                    *reinterpret_cast<const uint2 *>(wx + 16384 + ok2);
+                qT[0][k] = (qh4[0] + ql4[0]) * em4.x;
+                qT[1][k] = (qh4[1] + ql4[1]) * em4.y;
+                qT[2][k] = (qh4[2] + ql4[2]) * em4.z;
+                qT[3][k] = (qh4[3] + ql4[3]) * em4.w;
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const bool sw = (rg & 2) != 0;
+                const float v[4] = {sw ? qT[t][2] : qT[t][0], sw ? qT[t][3] : qT[t][1],
+                                    sw ? qT[t][0] : qT[t][2], sw ? qT[t][1] : qT[t][3]};
+                store_t4(wq, 4 * q4 + t, 32 + 4 * rg, v);
+            }
+            const bool sw = (rg & 2) != 0;
+#pragma unroll
+            for (int hl = 0; hl < (kLayer ? 2 : 0); ++hl) {
+                // rows 4 rg .. 4 rg + 3 in order
+                const uint2 a = sw ? kw[hl][2] : kw[hl][0], b = sw ? kw[hl][3] : kw[hl][1];
+                const uint2 c2 = sw ? kw[hl][0] : kw[hl][2], d = sw ? kw[hl][1] : kw[hl][3];
+                const int e0 = 4 * rg;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {  // channel 4 q4 + t: 16-bit half t & 1 of word t >> 1
+                    const uint32_t sel = (t & 1) ? 0x7632u : 0x5410u;
+                    const uint32_t wa = (t >> 1) ? a.y : a.x, wb = (t >> 1) ? b.y : b.x;
+                    const uint32_t wc = (t >> 1) ? c2.y : c2.x, wd = (t >> 1) ? d.y : d.x;
+                    const int j = 4 * q4 + t;
+                    const uint32_t o = (uint32_t)(j * 128 + ((((e0 >> 3) ^ (j & 7))) << 4) + (e0 & 4) * 2);
+                    *reinterpret_cast<uint2 *>(wq + 16384 * hl + o) =
+                        make_uint2(__byte_perm(wa, wb, sel), __byte_perm(wc, wd, sel));
+                }
             }
         }
         {
@@ -848,21 +903,19 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                              1);
             }
             mma_commit(bar + B_CA);
-        } else if (tid == kCB) {  // M2b: W'^T = (k E)^T Tb^T, k E (wq rows 0-31) read MN-major
+        } else if (tid == kCB) {  // M2b: W'^T = (k E)^T Tb^T, (k E)^T (wq elements 0-31) K-major
             const uint32_t th = smem_u32(sm + S_TB + s * TB_SIZE);
-            const uint32_t idw = idesc_bf16_f32(128, 32) | kIdescAMN;
+            const uint32_t idw = idesc_bf16_f32(128, 32);
             const uint32_t xh = smem_u32(wq), xl = xh + 16384;
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-                mma_bf16(tb + TM_WT, sw128_desc_mn(xh + 2048 * k, 8192), sw128_desc_k(th, 32, k), idw,
-                         k > 0);
+                mma_bf16(tb + TM_WT, sw128_desc_k(xh, 128, k), sw128_desc_k(th, 32, k), idw, k > 0);
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-                mma_bf16(tb + TM_WT, sw128_desc_mn(xh + 2048 * k, 8192), sw128_desc_k(th, 32, 2 + k), idw,
-                         1);
+                mma_bf16(tb + TM_WT, sw128_desc_k(xh, 128, k), sw128_desc_k(th, 32, 2 + k), idw, 1);
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-                mma_bf16(tb + TM_WT, sw128_desc_mn(xl + 2048 * k, 8192), sw128_desc_k(th, 32, k), idw, 1);
+                mma_bf16(tb + TM_WT, sw128_desc_k(xl, 128, k), sw128_desc_k(th, 32, k), idw, 1);
             mma_commit(bar + B_CB);
         }
 
@@ -912,45 +965,42 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             fence_after_sync();
             if (!alive) break;
         }
-        // ---- F7: W = W' Diag(em) -> rows 0..31 of wq (the k E rows are dead); thread = key
-        //      channel j ----
+        // ---- F7: W = W' Diag(em) -> wq elements 0-31 of row j ((k E)^T is dead); thread = key
+        //      channel j, four 16-byte chunks per half ----
         {
             const int j = tid;
             float w[32];
             tmem_ld32(tl + TM_WT, w);
             const float emj = em[j];
-            const uint32_t cbase = (uint32_t)((j >> 6) * 64 * 128 + ((j & 7) << 1));
-            const int jc = (j & 63) >> 3;
 #pragma unroll
-            for (int r = 0; r < 32; r += 2) {
-                uint32_t hw, lw;
-                split2(w[r] * emj, w[r + 1] * emj, hw, lw);
-                const uint32_t o0 = cbase + r * 128 + ((jc ^ (r & 7)) << 4);
-                const uint32_t o1 = cbase + (r + 1) * 128 + ((jc ^ ((r + 1) & 7)) << 4);
-                *reinterpret_cast<uint16_t *>(wq + o0) = (uint16_t)(hw & 0xFFFFu);
-                *reinterpret_cast<uint16_t *>(wq + o1) = (uint16_t)(hw >> 16);
-                *reinterpret_cast<uint16_t *>(wq + 16384 + o0) = (uint16_t)(lw & 0xFFFFu);
-                *reinterpret_cast<uint16_t *>(wq + 16384 + o1) = (uint16_t)(lw >> 16);
+            for (int q = 0; q < 4; ++q) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = w[8 * q + e] * emj;
+                const uint32_t o = (uint32_t)(j * 128 + ((q ^ (j & 7)) << 4));
+                store_split_chunk(wq + o, wq + 16384 + o, x);
             }
         }
         publish(kChainBar);
         if (tid == kCA || tid == kCB) {
             // M3: [(W S0)^T | (Q~ S0)^T] = S0^T [W ; Q~]^T, K steps 0-3 -> D3A, 4-7 -> D3B
-            const uint32_t id = idesc_bf16_f32(128, 64);
+            // ([W ; Q~] read MN-major: K step k = rows 16 k .. 16 k + 15 of the key-channel-major tile)
+            const uint32_t id = idesc_bf16_f32(128, 64) | kIdescBMN;
             const int s0 = tid == kCA ? 0 : 4;
             const uint32_t d = tb + (tid == kCA ? TM_D3A : TM_D3B);
             const uint32_t bh = smem_u32(wq), bl = bh + 16384;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_bf16_tmem_a(d, tb + TM_OPS + 8 * (s0 + k), sw128_desc_k(bh, 64, s0 + k), id,
-                                k > 0);
+                mma_bf16_tmem_a(d, tb + TM_OPS + 8 * (s0 + k), sw128_desc_mn(bh + 2048 * (s0 + k), 16384),
+                                id, k > 0);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                mma_bf16_tmem_a(d, tb + TM_OPS + 8 * (s0 + k), sw128_desc_k(bl, 64, s0 + k), id, 1);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16_tmem_a(d, tb + TM_OPS + 64 + 8 * (s0 + k), sw128_desc_k(bh, 64, s0 + k),
+                mma_bf16_tmem_a(d, tb + TM_OPS + 8 * (s0 + k), sw128_desc_mn(bl + 2048 * (s0 + k), 16384),
                                 id, 1);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                mma_bf16_tmem_a(d, tb + TM_OPS + 64 + 8 * (s0 + k),
+                                sw128_desc_mn(bh + 2048 * (s0 + k), 16384), id, 1);
             mma_commit(bar + (tid == kCA ? B_CA : B_CB));
         }
         if constexpr (sizeof(Tout) == 2 && !kLayer) copy_out();  // previous chunk, while M3 runs
