@@ -51,8 +51,8 @@ E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the ke
 # was taken on: a changed kernel reports traffic null until it is captured again.
 TRAFFIC = {
     "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-                "3dc17cfea792637356e92d8843c492d08cce6950c605c062471cc9b4b922c8af",
-                (252.560384e6 + 37.892096e6) / (2048 * 96)),
+                "ca0a4d11e5ec7673bb7b4d21469df3785c68d06c082de6a96abc31b8a3c6db3b",
+                (252.558592e6 + 37.625600e6) / (2048 * 96)),
     "decode": ("gated_delta_rule_kda_gb300/csrc/kda_decode.cu",
                "1bf0e4585307540aec99de0bebe444ea914f399db22eb7540d6128919bfb40b0",
                (205.3e6 + 142.4e6) / (32 * 96)),
