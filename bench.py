@@ -48,10 +48,11 @@ E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the ke
 # DRAM traffic per unit (token-head for the prefill, request-head for decode) from the
 # committed ncu captures (profiles/prefill_tc_kernel_T2048_H96.md, profiles/decode_kernel_B32_H96.md),
 # taken on a smaller case and scaled by units.  Valid only for the kernel source the capture
-# was taken on: a changed kernel reports traffic null until it is captured again.
+# was taken on: a changed kernel reports traffic null until it is captured again (a digest is
+# carried over only across comment-only edits whose compiled kernel is byte-identical).
 TRAFFIC = {
     "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-                "ca0a4d11e5ec7673bb7b4d21469df3785c68d06c082de6a96abc31b8a3c6db3b",
+                "8802617ff1d76bdc6341c9155d3e784e6ab4c482d4cbbfc322da9e60f7b331e0",
                 (252.558592e6 + 37.625600e6) / (2048 * 96)),
     "decode": ("gated_delta_rule_kda_gb300/csrc/kda_decode.cu",
                "1bf0e4585307540aec99de0bebe444ea914f399db22eb7540d6128919bfb40b0",

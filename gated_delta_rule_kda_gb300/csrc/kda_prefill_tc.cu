@@ -38,8 +38,8 @@
 // channel j), so every product is an M = 128 tcgen05.mma:
 //   M1  G = [k E ; q E] . (k E^-1)^T                  (lanes 0-31 -> A, 32-63 -> P)
 //   M2  U~^T = V^T . Tb^T                            (V read MN-major from its staged tile)
-//   M2b W'^T = (k E)^T . Tb^T                        (k E read MN-major; lane = key channel)
-//   M3  [ (W S0)^T | (Q~ S0)^T ] = S0^T . [W ; Q~]^T   (A = S0^T from TMEM)
+//   M2b W'^T = (k E)^T . Tb^T                        ((k E)^T K-major; lane = key channel)
+//   M3  [ (W S0)^T | (Q~ S0)^T ] = S0^T . [W ; Q~]^T   (A = S0^T from TMEM, B read MN-major)
 //   M4  (Q~ S0 + P U)^T += U^T . P^T
 //   M5  X^T = (Diag(em) S0)^T + U^T . (k E^-1)        (the Gram's B tile, read MN-major)
 //
@@ -50,11 +50,12 @@
 // Warp roles.  Only M3 .. M5 depend on the state; everything before them
 // depends on the chunk's inputs alone.  Warps 4-11 (the prep group) therefore
 // build chunk c+1's operands (decay, [k E ; q E], k E^-1 and Q~, the Gram, the
-// triangular solve, U~ and W) while warps 0-3 (the chain group) run the
-// state-dependent products of chunk c.  The operands of a chunk live in one of
-// two slots (shared-memory tiles, U~ in TMEM); the groups hand slots over with
-// mbarriers ("full" prep -> chain, "empty" chain -> prep), and every wait is
-// bounded in time.
+// triangular solve, Tb) while warps 0-3 (the chain group) run chunk c: the U~
+// and W' products, W, and the state-dependent products.  The operands of a
+// chunk live in one of two slots (shared-memory tiles); the groups hand slots
+// over with mbarriers ("full" prep -> chain, "empty" chain -> prep, "v free"
+// chain -> prep once M2 has read the slot's v tile), and every wait is bounded
+// in time.
 //
 // Layer mode (kLayer): the same kernel also runs one whole KDA layer core
 // ("Kimi K3 · KDA layer", KDA equation list) with nothing but the layer's inputs
@@ -123,7 +124,7 @@ constexpr int B_TQKV = 0;   // [2] TMA q/k/v by slot
 constexpr int B_CA = 2, B_CB = 3, B_PA = 4, B_PB = 5;  // MMA completion, one per issuer
 constexpr int B_FULL = 6;   // [2] prep -> chain: slot holds a chunk's operands
 constexpr int B_EMPTY = 8;  // [2] chain -> prep: slot consumed
-constexpr int B_VFREE = 10; // [2] chain -> prep: the slot's v tile and beta were consumed (M2, Tb)
+constexpr int B_VFREE = 10; // [2] chain -> prep: M2 has read the slot's v tile
 constexpr int B_TG = 12;    // layer mode: TMA of the chunk's g tile (chain group)
 constexpr int kNumBars = 13;
 
@@ -247,8 +248,8 @@ __device__ __forceinline__ void publish(int id) {
 
 // Stage chunk [t0, t0 + 32) of head h: q/k/v into slot `slot` (TMA, one
 // thread), beta by threads pt < 32 (cp.async, zero past nrow).  Rows past the
-// sequence end are not masked here: log_alpha and beta are masked where they
-// are used, which keeps those rows out of every product (see the kernel).
+// sequence end are not masked here: log_alpha is zero and beta is zero there,
+// which keeps those rows out of every product (see the kernel).
 template <bool kLayer>
 __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *sm, uint64_t *bar,
                                             int slot, int t0, int nrow, int h, int tid,
@@ -921,9 +922,8 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
 
         // ---- F4 (while M2 and M2b run): S0 = Diag(e31_prev) X -> M3's A operand (hi | lo);
         //      X <- Diag(em) S0.  After the first quarter each issuer waits for its own
-        //      products, and M2's issuer releases slot s's v tile and beta (Tb read beta
-        //      before M2 was issued), so that the prep group can stage the chunk after next
-        //      early ----
+        //      products, and M2's issuer releases slot s's v tile, so that the prep group can
+        //      stage the chunk after next early ----
         bool m2_ok = true;
         {
             const float *e31p = vec + 2 * kD + s * kD;
