@@ -255,6 +255,40 @@ kda_status kda_layer_core_fused(int32_t num_seqs, int32_t total_tokens, int32_t 
     return from_cuda(launch_layer_tc(a, static_cast<cudaStream_t>(stream)));
 }
 
+kda_status kda_decode_layer(int32_t batch, int32_t num_heads, int32_t pool_size,
+                            const void *qp, const void *kp, const void *vp, const float *conv_w,
+                            const void *z, const float *A, const float *b, const void *beta_logit,
+                            const void *g, const int32_t *slot, float *S_pool, void *conv_pool,
+                            float scale, float l2_eps, float rms_eps, kda_dtype out_dtype,
+                            void *o, void *stream) {
+    if (!ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (batch < 1 || num_heads < 1 || pool_size < 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_ptr(qp) || !ok_ptr(kp) || !ok_ptr(vp) || !ok_ptr(z) || !ok_ptr(g) || !ok_ptr(conv_w) ||
+        !ok_ptr_elem(A, 4) || !ok_opt_ptr(b) || !ok_ptr_elem(beta_logit, 2) || !ok_ptr_elem(slot, 4) ||
+        !ok_ptr(S_pool) || !ok_ptr(conv_pool) || !ok_ptr(o))
+        return KDA_ERR_INVALID_ARGUMENT;
+    const size_t state_bytes = (size_t)pool_size * num_heads * kD * kD * sizeof(float);
+    const size_t conv_bytes = (size_t)pool_size * 9 * num_heads * kD * sizeof(__nv_bfloat16);
+    const uintptr_t sp = reinterpret_cast<uintptr_t>(S_pool), cp = reinterpret_cast<uintptr_t>(conv_pool);
+    if (sp < cp + conv_bytes && cp < sp + state_bytes) return KDA_ERR_INVALID_ARGUMENT;  // pools overlap
+    if ((int64_t)batch * num_heads > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+    DecodeLayerArgs a;
+    a.batch = batch; a.num_heads = num_heads; a.pool_size = pool_size;
+    a.qp = static_cast<const __nv_bfloat16 *>(qp);
+    a.kp = static_cast<const __nv_bfloat16 *>(kp);
+    a.vp = static_cast<const __nv_bfloat16 *>(vp);
+    a.z = static_cast<const __nv_bfloat16 *>(z);
+    a.beta_logit = static_cast<const __nv_bfloat16 *>(beta_logit);
+    a.g = static_cast<const __nv_bfloat16 *>(g);
+    a.conv_w = conv_w; a.A = A; a.b = b; a.slot = slot;
+    a.S_pool = S_pool;
+    a.conv_pool = static_cast<__nv_bfloat16 *>(conv_pool);
+    a.scale = scale; a.l2_eps = l2_eps; a.rms_eps = rms_eps;
+    a.out_dtype = out_dtype; a.o = o;
+    a.status = device_status();
+    return from_cuda(launch_decode_layer(a, static_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_get_device_status(void *stream, uint32_t *detail) {
     if (detail) *detail = 0;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)

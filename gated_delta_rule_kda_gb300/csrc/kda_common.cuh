@@ -77,6 +77,21 @@ struct DecodeArgs {
     DeviceStatus status;
 };
 
+// One decode step of the whole layer core for a batch of requests whose recurrent state
+// and short-convolution state live in pools indexed by slot.
+struct DecodeLayerArgs {
+    int32_t batch, num_heads, pool_size;
+    const __nv_bfloat16 *qp, *kp, *vp, *z, *beta_logit, *g;  // [B][H][128] ([B][H] for beta_logit)
+    const float *conv_w, *A, *b;                            // [3][H*128][4], [H], [H][128] or null
+    const int32_t *slot;                                    // [B]
+    float *S_pool;                                          // [P][H][128][128]
+    __nv_bfloat16 *conv_pool;                               // [P][3][3][H][128]
+    float scale, l2_eps, rms_eps;
+    kda_dtype out_dtype;
+    void *o;                                                // [B][H][128]
+    DeviceStatus status;
+};
+
 struct PrefillArgs {
     kda_dtype in_dtype, out_dtype;
     int32_t num_seqs, total_tokens, num_heads;
@@ -125,6 +140,7 @@ struct LayerArgs {
 };
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
+cudaError_t launch_decode_layer(const DecodeLayerArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_recurrent(const PrefillArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 cudaError_t launch_layer_tc(const LayerArgs &a, cudaStream_t stream);

@@ -46,6 +46,7 @@ EXPORTED = (
     "kda_layer_core",
     "kda_layer_core_noalloc",
     "kda_layer_core_fused",
+    "kda_decode_layer",
     "kda_get_device_status",
 )
 
@@ -94,6 +95,9 @@ def _load() -> ctypes.CDLL:
     lib.kda_layer_core_fused.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, F, F,
                                          F, ctypes.c_int, P, P, P]
     lib.kda_layer_core_fused.restype = ctypes.c_int
+    lib.kda_decode_layer.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, F, F, F,
+                                     ctypes.c_int, P, P]
+    lib.kda_decode_layer.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.kda_get_device_status.restype = ctypes.c_int
     return lib
@@ -276,6 +280,27 @@ def kda_layer_core_fused(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens,
                                    _dtype_code(o.dtype), _p(o), _p(S_final), _stream(stream))
     _check("kda_layer_core_fused", rc)
     return o, S_final
+
+
+def kda_decode_layer(qp, kp, vp, conv_w, z, A, b, beta_logit, g, slot, S_pool, conv_pool,
+                     scale=DEFAULT_SCALE, l2_eps=1e-6, rms_eps=1e-6, *, out_dtype=torch.bfloat16,
+                     o=None, stream=None):
+    """One decode step of the layer core for requests whose states sit in pools.
+
+    qp, kp, vp, z, g: [B, H, 128] bf16; beta_logit: [B, H] bf16; slot: [B] int32 (distinct
+    pool rows); S_pool: [P, H, 128, 128] fp32 and conv_pool: [P, 3, 3, H, 128] bf16, both
+    updated in place.  Returns o [B, H, 128].
+    """
+    B, H, _ = qp.shape
+    P = S_pool.shape[0]
+    if o is None:
+        o = torch.empty((B, H, HEAD_DIM), dtype=out_dtype, device=qp.device)
+    rc = _lib.kda_decode_layer(B, H, P, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A), _p(b),
+                               _p(beta_logit), _p(g), _p(slot), _p(S_pool), _p(conv_pool),
+                               float(scale), float(l2_eps), float(rms_eps), _dtype_code(o.dtype),
+                               _p(o), _stream(stream))
+    _check("kda_decode_layer", rc)
+    return o
 
 
 def kda_get_device_status(stream=None):

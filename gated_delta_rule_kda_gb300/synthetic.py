@@ -166,6 +166,47 @@ def layer_inputs(lengths: Sequence[int], H: int, seed: int = BASE_SEED + 5,
                        cu_from_lengths(lengths, device))
 
 
+@dataclass
+class DecodeLayerInputs:
+    qp: torch.Tensor          # [B, H, 128] bf16, this token's pre-convolution projections
+    kp: torch.Tensor
+    vp: torch.Tensor
+    conv_w: torch.Tensor      # [3, H*128, 4] fp32
+    z: torch.Tensor           # [B, H, 128] bf16
+    A: torch.Tensor           # [H] fp32
+    b: torch.Tensor           # [H, 128] fp32 (zero)
+    beta_logit: torch.Tensor  # [B, H] bf16
+    g: torch.Tensor           # [B, H, 128] bf16
+    slot: torch.Tensor        # [B] int32, distinct rows of the pools
+    S_pool: torch.Tensor      # [P, H, 128, 128] fp32
+    conv_pool: torch.Tensor   # [P, 3, 3, H, 128] bf16 (previous pre-convolution inputs)
+
+
+def decode_layer_inputs(B: int, H: int, P: int, seed: int = BASE_SEED + 6,
+                        s_std: float = 0.1, device="cpu") -> DecodeLayerInputs:
+    """One decode token per request, with the distributions of the layer-core workload
+    (pre-projection inputs ~N(0,1) bf16, conv w ~N(0,0.5), A ~N(0,0.5), b = 0,
+    beta logit ~N(0,1), g ~N(0,1)); the requests sit in B distinct, shuffled rows of
+    pools of P rows (state ~N(0, s_std), convolution history ~N(0,1) bf16)."""
+    if P < B:
+        raise ValueError("the pools need at least one row per request")
+    g = _gen(seed, device)
+    bf = torch.bfloat16
+    qp = _randn((B, H, D), g, device).to(bf)
+    kp = _randn((B, H, D), g, device).to(bf)
+    vp = _randn((B, H, D), g, device).to(bf)
+    conv_w = _randn((3, H * D, 4), g, device, 0.0, 0.5)
+    z = _randn((B, H, D), g, device).to(bf)
+    A = _randn((H,), g, device, 0.0, 0.5)
+    b = torch.zeros((H, D), dtype=torch.float32, device=device)
+    beta_logit = _randn((B, H), g, device).to(bf)
+    gg = _randn((B, H, D), g, device).to(bf)
+    slot = torch.randperm(P, generator=g, device=device)[:B].to(torch.int32)
+    S_pool = _randn((P, H, D, D), g, device, 0.0, s_std)
+    conv_pool = _randn((P, 3, 3, H, D), g, device).to(bf)
+    return DecodeLayerInputs(qp, kp, vp, conv_w, z, A, b, beta_logit, gg, slot, S_pool, conv_pool)
+
+
 def workload(index: int, device="cpu"):
     """The five named workloads (see the module docstring)."""
     seed = BASE_SEED + index

@@ -270,6 +270,53 @@ kda_status kda_layer_core_fused(int32_t num_seqs, int32_t total_tokens, int32_t 
                                 float *S_final, void *stream);
 
 /*
+ * kda_decode_layer - one decode step of the whole layer core for a batch of
+ * requests whose recurrent state and short-convolution state live in pools
+ * ("Kimi K3 · KDA layer", KDA equation list; a decoding request carries its own
+ * KDA state and short-convolution state: "Inside Kimi K3: How KDA, AttnRes, and
+ * 896 Experts Work", section "KDA writes corrections into a recurrent matrix";
+ * fixed per-request state blocks in a pool, mutated only in the request's own
+ * working slot: "Kimi K3: Architecture and SGLang Day-0 Support", sections
+ * "RadixAttention: prefix caching for KDA state" and "Memory management for two
+ * state types").
+ *
+ * For request b and head h, with n = slot[b]:
+ *   x^c = SiLU(w0 x^p + w1 x_{t-1} + w2 x_{t-2} + w3 x_{t-3}) for x in q, k, v, the three
+ *         previous inputs taken from conv_pool row n (which then shifts by one token);
+ *   q^, k^ = L2-normalised q^c, k^c; log_alpha = -5 sigmoid(e^A (z + b)); beta = sigmoid(beta_logit);
+ *   the recurrence step of kda_decode_step on S_pool row n (updated in place);
+ *   o = sigmoid(g) o~ / sqrt(mean(o~^2) + rms_eps).
+ * A request at the start of its sequence has a zeroed conv_pool row (zero history,
+ * as in the prefill) and the S0 it starts from in its S_pool row.
+ *
+ *   batch, num_heads, pool_size >= 1; P = pool_size rows in each pool
+ *   qp, kp, vp  [B][H][128] bf16: this token's pre-convolution projections
+ *   conv_w      [3][H*128][4] fp32 (taps: w0 multiplies the current token)
+ *   z, g        [B][H][128] bf16;  A [H] fp32;  b [H][128] fp32 or NULL (zero)
+ *   beta_logit  [B][H] bf16
+ *   slot        [B] int32, device: the pool row of each request; rows must be
+ *               distinct within a call (repeated rows race).  A row outside
+ *               [0, P) leaves that request untouched and records
+ *               KDA_ERR_DEVICE_CHECK (detail = b) in the device status word.
+ *   S_pool      [P][H][128][128] fp32, row j = key channel, updated in place
+ *   conv_pool   [P][3][3][H][128] bf16: stream (q, k, v), tap (t-1, t-2, t-3);
+ *               updated in place
+ *   o           [B][H][128] out_dtype
+ * All pointers are caller-owned device memory; qp, kp, vp, z, g, conv_w, S_pool,
+ * conv_pool and o 16-byte aligned; the pools must not overlap.  Nothing is
+ * allocated.
+ * Errors: KDA_ERR_INVALID_ARGUMENT (null/misaligned pointers, bad sizes or dtype,
+ * overlapping pools), KDA_ERR_UNSUPPORTED (batch * heads above 2^31 - 1),
+ * KDA_ERR_CUDA (launch failure).
+ */
+kda_status kda_decode_layer(int32_t batch, int32_t num_heads, int32_t pool_size,
+                            const void *qp, const void *kp, const void *vp, const float *conv_w,
+                            const void *z, const float *A, const float *b, const void *beta_logit,
+                            const void *g, const int32_t *slot, float *S_pool, void *conv_pool,
+                            float scale, float l2_eps, float rms_eps, kda_dtype out_dtype,
+                            void *o, void *stream);
+
+/*
  * kda_get_device_status - synchronises `stream`, then returns and clears the
  * device status word: KDA_OK, KDA_ERR_DEVICE_TIMEOUT or KDA_ERR_DEVICE_CHECK
  * (KDA_ERR_CUDA if the synchronisation itself fails).  If detail is not

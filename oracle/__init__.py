@@ -170,3 +170,56 @@ def kda_layer_core(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=No
                                         cu_seqlens, l2_eps, n_threads)
     ot, Sf = kda_prefill(qh, kh, vv, la, beta, cu_seqlens, S0, scale, n_threads)
     return kda_output_gate(ot, g, rms_eps, n_threads), Sf
+
+
+def kda_decode_layer(qp, kp, vp, conv_w, z, A, b, beta_logit, g, slot, S_pool, conv_pool,
+                     scale=None, l2_eps=1e-6, rms_eps=1e-6, n_threads=None):
+    """One decode step of the layer core over pooled states (fp64); inputs are not modified.
+
+    Follows the KDA equation list ("Kimi K3 · KDA layer") for one new token per request,
+    with the request's short-convolution state (its last three pre-convolution inputs per
+    channel; "Inside Kimi K3: How KDA, AttnRes, and 896 Experts Work", section "KDA writes
+    corrections into a recurrent matrix") and recurrent state taken from pool row slot[b].
+
+    qp, kp, vp, z, g: [B, H, d]; beta_logit: [B, H]; slot: [B] distinct rows of the pools;
+    S_pool: [P, H, d, d]; conv_pool: [P, 3 (q, k, v), 3 (taps t-1, t-2, t-3), H, d].
+    Returns (o_gated [B, H, d], S_pool_new, conv_pool_new).
+
+    The front end of request b is the pinned sequence front end run on the 4-token
+    window (x_{t-3}, x_{t-2}, x_{t-1}, x_t) as one sequence: the convolution of its last
+    token is the decode convolution.  Then one recurrence step on row slot[b] of S_pool,
+    then the output gate; row slot[b] of conv_pool shifts by one token.
+    """
+    qp, kp, vp, conv_w, z, A, b, bl, g = map(_f64, (qp, kp, vp, conv_w, z, A, b, beta_logit, g))
+    S_pool, conv_pool = _f64(S_pool), _f64(conv_pool)
+    slot = np.asarray(slot, dtype=np.int64)
+    B, H, d = qp.shape
+    P = S_pool.shape[0]
+    if slot.shape != (B,) or len(set(slot.tolist())) != B or slot.min() < 0 or slot.max() >= P:
+        raise ValueError("kda_decode_layer: slots must be B distinct rows in [0, P)")
+    windows = []
+    for s, xp in enumerate((qp, kp, vp)):
+        w = np.zeros((B, 4, H, d))
+        w[:, 0] = conv_pool[slot, s, 2]  # t-3
+        w[:, 1] = conv_pool[slot, s, 1]  # t-2
+        w[:, 2] = conv_pool[slot, s, 0]  # t-1
+        w[:, 3] = xp
+        windows.append(w.reshape(4 * B, H, d))
+    zw = np.zeros((B, 4, H, d)); zw[:, 3] = z
+    blw = np.zeros((B, 4, H)); blw[:, 3] = bl
+    cu = np.arange(0, 4 * B + 1, 4, dtype=np.int32)
+    qh, kh, vv, la, beta = kda_frontend(windows[0], windows[1], windows[2], conv_w,
+                                        zw.reshape(4 * B, H, d), A, b, blw.reshape(4 * B, H),
+                                        cu, l2_eps, n_threads)
+    last = np.arange(3, 4 * B, 4)
+    o_t, S_rows = kda_decode_step(qh[last], kh[last], vv[last], la[last], beta[last], S_pool[slot],
+                                  scale, n_threads)
+    o = kda_output_gate(o_t, g, rms_eps, n_threads)
+    S_new = S_pool.copy()
+    S_new[slot] = S_rows
+    conv_new = conv_pool.copy()
+    for s, xp in enumerate((qp, kp, vp)):
+        conv_new[slot, s, 2] = conv_pool[slot, s, 1]
+        conv_new[slot, s, 1] = conv_pool[slot, s, 0]
+        conv_new[slot, s, 0] = xp
+    return o, S_new, conv_new

@@ -138,3 +138,26 @@ def test_layer_core_fused_rejects_bad_arguments(kda, bad):
 
 def test_layer_core_fused_too_many_heads_unsupported(kda):
     assert _fused(kda.library(), H=70000) == 2
+
+
+def _decode_layer(lib, **kw):
+    a = dict(B=2, H=2, P=4, qp=FAKE, kp=FAKE, vp=FAKE, w=FAKE, z=FAKE, A=FAKE, b=None, bl=FAKE,
+             g=FAKE, slot=FAKE, S=FAKE, conv=FAKE + (1 << 24), out_dt=0, o=FAKE)
+    a.update(kw)
+    return lib.kda_decode_layer(a["B"], a["H"], a["P"], a["qp"], a["kp"], a["vp"], a["w"], a["z"],
+                                a["A"], a["b"], a["bl"], a["g"], a["slot"], a["S"], a["conv"],
+                                0.1, 1e-6, 1e-6, a["out_dt"], a["o"], None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(out_dt=5), dict(B=0), dict(H=0), dict(P=0), dict(qp=None), dict(kp=MIS), dict(vp=None),
+    dict(w=MIS), dict(z=None), dict(A=None), dict(b=MIS), dict(bl=None), dict(g=MIS),
+    dict(slot=None), dict(S=None), dict(conv=MIS), dict(o=None),
+    dict(conv=FAKE + 1024),  # the convolution pool inside the state pool
+])
+def test_decode_layer_rejects_bad_arguments(kda, bad):
+    assert _decode_layer(kda.library(), **bad) == 1  # KDA_ERR_INVALID_ARGUMENT, before any launch
+
+
+def test_decode_layer_grid_too_large_unsupported(kda):
+    assert _decode_layer(kda.library(), B=1 << 20, H=1 << 12, conv=FAKE + (1 << 40)) == 2

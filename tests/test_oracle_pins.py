@@ -407,3 +407,63 @@ def test_state_size_figures():
     mb = 69 * (96 // 8) * 128 * 128 * 4 / 1e6
     assert 53.5 < mb < 55.0
     assert not (53.5 < mb / 2 < 55.0)
+
+
+# --------------------------------------------------------------------------
+# P15 decode step of the layer core over pooled states: the layer core over
+#     T0 tokens, then one decode_layer step per further token (convolution
+#     state = the last three pre-convolution inputs, zero before the sequence
+#     start; recurrent state = the layer core's S_final, placed in an arbitrary
+#     pool row) reproduces the layer core over all T tokens, output by output;
+#     pool rows of other requests are untouched; the convolution state shifts.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("T0", [0, 1, 2, 5])
+def test_decode_layer_continues_the_layer_core(T0):
+    T, H, d, P = T0 + 4, 2, 8, 3
+    rng = np.random.default_rng(700 + T0)
+    qp, kp, vp, z, g = (rng.standard_normal((T, H, d)) for _ in range(5))
+    conv_w = rng.standard_normal((3, H * d, 4)) * 0.5
+    A = rng.standard_normal(H) * 0.5
+    b = rng.standard_normal((H, d)) * 0.3
+    bl = rng.standard_normal((T, H))
+    S0 = rng.standard_normal((1, H, d, d)) * 0.3
+    ref_o, ref_S = oracle.kda_layer_core(qp, kp, vp, conv_w, z, A, b, bl, g, [0, T], S0=S0)
+    row = 1  # this request's pool row; rows 0 and 2 belong to other requests
+    S_pool = rng.standard_normal((P, H, d, d))
+    conv_pool = rng.standard_normal((P, 3, 3, H, d))
+    if T0 > 0:
+        o0, S_T0 = oracle.kda_layer_core(qp[:T0], kp[:T0], vp[:T0], conv_w, z[:T0], A, b, bl[:T0],
+                                         g[:T0], [0, T0], S0=S0)
+        np.testing.assert_allclose(o0, ref_o[:T0], atol=1e-12)
+        S_pool[row] = S_T0[0]
+    else:
+        S_pool[row] = S0[0]
+    for s, xp in enumerate((qp, kp, vp)):  # the last three inputs before token T0
+        for tap in range(3):
+            t = T0 - 1 - tap
+            conv_pool[row, s, tap] = xp[t] if t >= 0 else 0.0
+    others = [r for r in range(P) if r != row]
+    S_others, conv_others = S_pool[others].copy(), conv_pool[others].copy()
+    for t in range(T0, T):
+        sl = slice(t, t + 1)
+        o, S_pool_new, conv_new = oracle.kda_decode_layer(qp[sl], kp[sl], vp[sl], conv_w, z[sl], A, b,
+                                                          bl[sl], g[sl], [row], S_pool, conv_pool)
+        np.testing.assert_allclose(o[0], ref_o[t], atol=1e-12)
+        for s, xp in enumerate((qp, kp, vp)):
+            np.testing.assert_array_equal(conv_new[row, s, 0], xp[t])
+            np.testing.assert_array_equal(conv_new[row, s, 1], conv_pool[row, s, 0])
+            np.testing.assert_array_equal(conv_new[row, s, 2], conv_pool[row, s, 1])
+        S_pool, conv_pool = S_pool_new, conv_new
+    np.testing.assert_allclose(S_pool[row], ref_S[0], atol=1e-12)
+    np.testing.assert_array_equal(S_pool[others], S_others)
+    np.testing.assert_array_equal(conv_pool[others], conv_others)
+
+
+def test_decode_layer_rejects_repeated_or_out_of_range_slots():
+    H, d, P = 1, 4, 2
+    x = np.zeros((2, H, d))
+    args = (x, x, x, np.zeros((3, H * d, 4)), x, np.zeros(H), np.zeros((H, d)), np.zeros((2, H)), x)
+    S_pool, conv_pool = np.zeros((P, H, d, d)), np.zeros((P, 3, 3, H, d))
+    for slots in ([0, 0], [0, 2], [-1, 1]):
+        with pytest.raises(ValueError):
+            oracle.kda_decode_layer(*args, slots, S_pool, conv_pool)
