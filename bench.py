@@ -40,6 +40,11 @@ STATE_BYTES = D * D * 4                                               # 64 KiB p
 # Decode, per (request, head): state read + write, q/k/v bf16, log_alpha fp32, beta, o bf16
 DECODE_BYTES_PER_UNIT = 2 * STATE_BYTES + 3 * D * 2 + D * 4 + 4 + D * 2  # 132,612 B
 DECODE_FLOP_PER_UNIT = 2 * 4 * D * D
+# Decode step of the layer core, per (request, head): state read + write, the short-convolution
+# state (3 streams x 3 taps x 128 bf16) read + write, q^p, k^p, v^p, z, g bf16, beta_logit, o^g
+# bf16; plus, once per step and head, the convolution weights and the decay parameters.
+DECODE_LAYER_BYTES_PER_UNIT = 2 * STATE_BYTES + 2 * 9 * D * 2 + 5 * D * 2 + 2 + D * 2  # 137,218 B
+DECODE_LAYER_BYTES_PER_HEAD = 3 * D * 4 * 4 + 4 + D * 4
 # Fused layer core, per (token, head): q^p, k^p, v^p, z, g bf16 in, o^g bf16 out, beta_logit.
 LAYER_BYTES_PER_TOKEN_HEAD = 5 * D * 2 + 2 + D * 2                      # 1,538 B
 E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the kernels)
@@ -372,6 +377,30 @@ def run_ours(args, world, rank, local):
     del dinp, od
     torch.cuda.empty_cache()
 
+    # ---------------- decode step of the whole layer core over state pools ----------------
+    linp1 = synthetic.decode_layer_inputs(256, 96, 256, device=dev)
+    odl = torch.empty((256, 96, D), dtype=torch.bfloat16, device=dev)
+
+    def decode_layer_step():
+        kda.kda_decode_layer(linp1.qp, linp1.kp, linp1.vp, linp1.conv_w, linp1.z, linp1.A,
+                             linp1.b, linp1.beta_logit, linp1.g, linp1.slot, linp1.S_pool,
+                             linp1.conv_pool, o=odl)
+
+    dl_total, dl_per = time_launches(decode_layer_step, args.steps, args.warmup, world)
+    dl_ms = max_over_ranks(dl_total / args.steps, world)
+    dl_launch = sum(dl_per) / len(dl_per)
+    dl_bytes = 256 * 96 * DECODE_LAYER_BYTES_PER_UNIT + 96 * DECODE_LAYER_BYTES_PER_HEAD
+    dl_ach = dl_bytes / (dl_launch / 1e3) / 1e9
+    decode_layer = {"tokens_per_s": aggregate_rate(256, dl_ms, world), "ms_per_step": dl_ms,
+                    "entry_point": "kda_decode_layer",
+                    "workload": "256 requests x 96 heads in shuffled rows of 256-row state and "
+                                "convolution pools; front end + recurrence + gate",
+                    "roofline": {"bound": "hbm", "achieved": dl_ach, "peak": hbm, "unit": "GB/s",
+                                 "frac": dl_ach / hbm, "traffic": None, "peak_kind": peak_kind,
+                                 "kernel": "kda_decode_layer"}}
+    del linp1, odl
+    torch.cuda.empty_cache()
+
     # ---------------- layer core (varlen, 16 sequences) ----------------
     layer = None
     if not args.skip_layer_core:
@@ -429,7 +458,7 @@ def run_ours(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
-            "layer_core": layer,
+            "decode_layer": decode_layer, "layer_core": layer,
             "clocks": clk, "gpu_launches": args.steps,
             "kernel_ms_mean": launch_ms,
         }
@@ -459,6 +488,14 @@ def run_only(args, local):
                                               linp.A, linp.b, linp.beta_logit, linp.g,
                                               linp.cu_seqlens, None, o=og, want_state=False)
         units = LT
+    elif args.only == "decode_layer":
+        B = 32 if args.small else 256
+        linp1 = synthetic.decode_layer_inputs(B, 96, B, device=dev)
+        odl = torch.empty((B, 96, D), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_decode_layer(linp1.qp, linp1.kp, linp1.vp, linp1.conv_w, linp1.z,
+                                          linp1.A, linp1.b, linp1.beta_logit, linp1.g, linp1.slot,
+                                          linp1.S_pool, linp1.conv_pool, o=odl)
+        units = B
     else:
         B = 32 if args.small else 256
         dinp = synthetic.decode_inputs(B, 96, torch.bfloat16, device=dev)
@@ -481,7 +518,7 @@ def main():
     ap.add_argument("--skip-layer-core", action="store_true")
     ap.add_argument("--skip-staged-layer-core", action="store_true",
                     help="time only the fused layer core, not the three-launch composition")
-    ap.add_argument("--only", choices=["prefill", "decode", "layer"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "decode_layer", "layer"], default=None,
                     help="profiling aid: run just this kernel (no baseline, no e2e)")
     ap.add_argument("--small", action="store_true",
                     help="with --only: a smaller case sized for ncu captures")

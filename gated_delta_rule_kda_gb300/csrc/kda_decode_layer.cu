@@ -1,19 +1,22 @@
 // KDA decode step of the whole layer core, for requests whose state lives in a pool.
 //
 // Per unit (request b, head h), with the request's pool row n = slot[b]
-// ("Kimi K3 · KDA layer", KDA equation list; the short-convolution state that each
-// request carries beside its recurrent state is the pages' own description of a
-// decoding request, "Kimi Linear", section on serving state):
+// ("Kimi K3 · KDA layer", KDA equation list; each decoding request carries a
+// short-convolution state beside its recurrent state: "Inside Kimi K3: How KDA,
+// AttnRes, and 896 Experts Work", section "KDA writes corrections into a recurrent
+// matrix"):
 //   x^c   = SiLU(w0 x^p_t + w1 x^p_{t-1} + w2 x^p_{t-2} + w3 x^p_{t-3})  for x in q, k, v,
 //           the three previous inputs read from the convolution state of row n;
-//   q^ = q^c / |q^c|,  k^ = k^c / |k^c|,  v = v^c
+//   q^ = q^c / |q^c|,  k^ = k^c / |k^c|,  v = v^c   (|x| = sqrt(sum x^2 + l2_eps))
 //   log alpha = -5 sigmoid(e^A (z + b)),  beta = sigmoid(beta_logit)
 //   S' = Diag(alpha) S,  u = beta (v - S'^T k^),  S <- S' + k^ u^T
 //   o~ = scale S^T q^ = scale (S'^T q^ + (k^.q^) u)
 //   o  = sigmoid(g) o~ / sqrt(mean(o~^2) + eps)
 // and the convolution state of row n shifts by one token (x^p_t becomes the newest).
 // As in the plain decode step the state is read and written once, in registers, so
-// the kernel is HBM-bound; the front end and the gate add ~3 KB to its 128 KB.
+// the kernel is HBM-bound; the front end and the gate add ~6 KB to its 128 KB.  The
+// front end's inputs are fetched before the state stream, and the state goes back
+// before the gate's reduction, so that neither lengthens a CTA's life.
 //
 // Layout: one 256-thread CTA per unit.  Warp w owns state rows [16w, 16w+16); lane l
 // owns columns [4l, 4l+4).  Front end: threads 0-127 take channel tid of q and k,
@@ -38,18 +41,31 @@ __device__ __forceinline__ void st_stream(float *p, float4 x) {
 __device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
 
-// Width-4 causal convolution of one channel followed by SiLU; shifts the channel's
-// convolution state (taps t-1, t-2, t-3 at hist[0], hist[HD], hist[2 HD]).
-__device__ __forceinline__ float conv_silu(const __nv_bfloat16 *xp_t, __nv_bfloat16 *hist,
-                                           size_t HD, const float4 w) {
-    const __nv_bfloat16 x0 = *xp_t, h1 = hist[0], h2 = hist[HD], h3 = hist[2 * HD];
-    float a = w.x * __bfloat162float(x0);
-    a = fmaf(w.y, __bfloat162float(h1), a);
-    a = fmaf(w.z, __bfloat162float(h2), a);
-    a = fmaf(w.w, __bfloat162float(h3), a);
-    hist[0] = x0;  // the newest input becomes tap t-1 of the next step
-    hist[HD] = h1;
-    hist[2 * HD] = h2;
+// One channel of one stream: the current input, its three previous inputs (taps t-1, t-2,
+// t-3 at hist[0], hist[HD], hist[2 HD] of the convolution state) and the four weights.
+struct ConvIn {
+    __nv_bfloat16 x0, h1, h2, h3;
+    float4 w;
+};
+__device__ __forceinline__ ConvIn conv_load(const __nv_bfloat16 *xp_t, const __nv_bfloat16 *hist,
+                                            size_t HD, const float *w) {
+    ConvIn c;
+    c.x0 = *xp_t;
+    c.h1 = hist[0];
+    c.h2 = hist[HD];
+    c.h3 = hist[2 * HD];
+    c.w = *reinterpret_cast<const float4 *>(w);
+    return c;
+}
+// Width-4 causal convolution followed by SiLU; shifts the convolution state by one token.
+__device__ __forceinline__ float conv_silu(const ConvIn &c, __nv_bfloat16 *hist, size_t HD) {
+    float a = c.w.x * __bfloat162float(c.x0);
+    a = fmaf(c.w.y, __bfloat162float(c.h1), a);
+    a = fmaf(c.w.z, __bfloat162float(c.h2), a);
+    a = fmaf(c.w.w, __bfloat162float(c.h3), a);
+    hist[0] = c.x0;  // the newest input becomes tap t-1 of the next step
+    hist[HD] = c.h1;
+    hist[2 * HD] = c.h2;
     return a * sigmoidf_(a);
 }
 
@@ -85,32 +101,38 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(const DecodeL
     const size_t unit = (size_t)b * H + h;
     float *Su = a.S_pool + ((size_t)n * H + h) * (size_t)(kD * kD);
 
-    // 1. Issue the whole state load first: 16 x 16 B per thread in flight.
+    // 1. The front end's few inputs first (they decide when the state work can start),
+    //    then the whole state load: 16 x 16 B per thread in flight.
+    const size_t HD = (size_t)H * kD;
+    __nv_bfloat16 *cpool = a.conv_pool + (size_t)n * 9 * HD;  // [stream][tap][H][128]
+    const int c = tid & (kD - 1);
+    const size_t ch = (size_t)h * kD + c;
+    ConvIn in0, in1;  // q, k (threads 0-127) or v (threads 128-255, in0 only)
+    float zb = 0.f, gl = 0.f, bl = 0.f;
+    if (tid < kD) {
+        in0 = conv_load(a.qp + unit * kD + c, cpool + 0 * 3 * HD + ch, HD, a.conv_w + (0 * HD + ch) * 4);
+        in1 = conv_load(a.kp + unit * kD + c, cpool + 1 * 3 * HD + ch, HD, a.conv_w + (1 * HD + ch) * 4);
+        gl = bf(a.g + unit * kD + c);
+        bl = bf(a.beta_logit + unit);
+    } else {
+        in0 = conv_load(a.vp + unit * kD + c, cpool + 2 * 3 * HD + ch, HD, a.conv_w + (2 * HD + ch) * 4);
+        zb = bf(a.z + unit * kD + c) + (a.b != nullptr ? a.b[ch] : 0.f);
+    }
     float4 s[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i)
         s[i] = ld_stream(Su + (size_t)(warp * kRowsPerWarp + i) * kD + 4 * lane);
 
     // 2. Front end while the state streams in.
-    const size_t HD = (size_t)H * kD;
-    __nv_bfloat16 *cpool = a.conv_pool + (size_t)n * 9 * HD;  // [stream][tap][H][128]
     if (tid < kD) {
-        const int c = tid;
-        const size_t ch = (size_t)h * kD + c;
-        const float4 wq = *reinterpret_cast<const float4 *>(a.conv_w + (0 * HD + ch) * 4);
-        const float4 wk = *reinterpret_cast<const float4 *>(a.conv_w + (1 * HD + ch) * 4);
-        const float yq = conv_silu(a.qp + unit * kD + c, cpool + 0 * 3 * HD + ch, HD, wq);
-        const float yk = conv_silu(a.kp + unit * kD + c, cpool + 1 * 3 * HD + ch, HD, wk);
+        const float yq = conv_silu(in0, cpool + 0 * 3 * HD + ch, HD);
+        const float yk = conv_silu(in1, cpool + 1 * 3 * HD + ch, HD);
         const float2 ss = sum128(yq * yq, yk * yk, &s_part);
         s_q[c] = yq * rsqrtf(ss.x + a.l2_eps);
         s_k[c] = yk * rsqrtf(ss.y + a.l2_eps);
     } else {
-        const int c = tid - kD;
-        const size_t ch = (size_t)h * kD + c;
-        const float4 wv = *reinterpret_cast<const float4 *>(a.conv_w + (2 * HD + ch) * 4);
-        s_v[c] = conv_silu(a.vp + unit * kD + c, cpool + 2 * 3 * HD + ch, HD, wv);
-        const float bias = a.b != nullptr ? a.b[ch] : 0.f;
-        const float la = -5.f * sigmoidf_(expf(a.A[h]) * (bf(a.z + unit * kD + c) + bias));
+        s_v[c] = conv_silu(in0, cpool + 2 * 3 * HD + ch, HD);
+        const float la = -5.f * sigmoidf_(expf(a.A[h]) * zb);
         s_a[c] = expf(la);
     }
     __syncthreads();
@@ -139,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(const DecodeL
     }
     __syncthreads();
 
-    // 4. u = beta (v - r), o~ = scale (p + (k.q) u), then the gate (one channel per thread).
+    // 4. u = beta (v - r) and o~ = scale (p + (k.q) u), one channel per thread.
+    float ot = 0.f;
     if (tid < kD) {
         float rr = 0.f, pp = 0.f;
 #pragma unroll
@@ -147,17 +170,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(const DecodeL
             rr += s_red_r[w][tid];
             pp += s_red_p[w][tid];
         }
-        const float beta = sigmoidf_(bf(a.beta_logit + unit));
-        const float u = beta * (s_v[tid] - rr);
+        const float u = sigmoidf_(bl) * (s_v[tid] - rr);
         s_u[tid] = u;
-        const float ot = a.scale * fmaf(s_kq, u, pp);
-        const float ms = sum128(ot * ot, 0.f, &s_part2).x * (1.f / kD);
-        const float og = sigmoidf_(bf(a.g + unit * kD + tid)) * ot * rsqrtf(ms + a.rms_eps);
-        Elem<Tout>::store(static_cast<Tout *>(a.o) + unit * kD + tid, og);
+        ot = a.scale * fmaf(s_kq, u, pp);
     }
     __syncthreads();
 
-    // 5. Rank-1 write S = S' + k u^T and stream the state back.
+    // 5. Rank-1 write S = S' + k u^T and stream the state back (before the gate's reduction).
     const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[4 * lane]);
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
@@ -166,6 +185,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(const DecodeL
         s[i].x = fmaf(kj, u4.x, s[i].x); s[i].y = fmaf(kj, u4.y, s[i].y);
         s[i].z = fmaf(kj, u4.z, s[i].z); s[i].w = fmaf(kj, u4.w, s[i].w);
         st_stream(Su + (size_t)j * kD + 4 * lane, s[i]);
+    }
+
+    // 6. Output gate: sigmoid(g) o~ / sqrt(mean(o~^2) + eps) over the head's 128 channels.
+    if (tid < kD) {
+        const float ms = sum128(ot * ot, 0.f, &s_part2).x * (1.f / kD);
+        const float og = sigmoidf_(gl) * ot * rsqrtf(ms + a.rms_eps);
+        Elem<Tout>::store(static_cast<Tout *>(a.o) + unit * kD + tid, og);
     }
 }
 
