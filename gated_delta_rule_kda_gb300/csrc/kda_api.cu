@@ -43,6 +43,13 @@ bool overlap(const void *a, const void *b, size_t bytes) {
 
 kda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+// Checkpoint arguments: none (every == 0), or every a positive multiple of the prefill's
+// 32-token chunk with the offsets and the states both given.
+bool ok_checkpoints(int32_t every, const int32_t *base, const float *states) {
+    if (every == 0) return true;
+    return every > 0 && every % 32 == 0 && ok_ptr_elem(base, 4) && ok_ptr(states);
+}
+
 }  // namespace
 }  // namespace kda
 
@@ -76,7 +83,21 @@ kda_status kda_prefill(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs
                        const void *v, const float *log_alpha, const float *beta,
                        const float *S0, const int32_t *cu_seqlens, float scale, void *o,
                        float *S_final, void *workspace, size_t workspace_bytes, void *stream) {
+    return kda_prefill_with_checkpoints(in_dtype, out_dtype, num_seqs, total_tokens, num_heads, q,
+                                        k, v, log_alpha, beta, S0, cu_seqlens, scale, o, S_final,
+                                        workspace, workspace_bytes, 0, nullptr, nullptr, stream);
+}
+
+kda_status kda_prefill_with_checkpoints(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
+                                        int32_t total_tokens, int32_t num_heads, const void *q,
+                                        const void *k, const void *v, const float *log_alpha,
+                                        const float *beta, const float *S0,
+                                        const int32_t *cu_seqlens, float scale, void *o,
+                                        float *S_final, void *workspace, size_t workspace_bytes,
+                                        int32_t ckpt_every, const int32_t *ckpt_base,
+                                        float *ckpt_states, void *stream) {
     if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_checkpoints(ckpt_every, ckpt_base, ckpt_states)) return KDA_ERR_INVALID_ARGUMENT;
     if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
     if (!ok_ptr_elem(cu_seqlens, 4)) return KDA_ERR_INVALID_ARGUMENT;
     if (total_tokens > 0) {
@@ -99,6 +120,7 @@ kda_status kda_prefill(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta; a.S0 = S0;
     a.cu_seqlens = cu_seqlens; a.scale = scale; a.o = o; a.S_final = S_final;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
+    a.ckpt = Checkpoints{ckpt_every, ckpt_base, ckpt_states};
     a.status = device_status();
     // bf16 inputs: chunked tensor-core kernel; fp32 inputs: full-precision recurrent kernel.
     if (in_dtype == KDA_BF16)
@@ -226,7 +248,20 @@ kda_status kda_layer_core_fused(int32_t num_seqs, int32_t total_tokens, int32_t 
                                 const int32_t *cu_seqlens, const float *S0, float scale,
                                 float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
                                 float *S_final, void *stream) {
+    return kda_layer_core_fused_with_checkpoints(num_seqs, total_tokens, num_heads, qp, kp, vp,
+                                                 conv_w, z, A, b, beta_logit, g, cu_seqlens, S0,
+                                                 scale, l2_eps, rms_eps, out_dtype, o_gated, S_final,
+                                                 0, nullptr, nullptr, stream);
+}
+
+kda_status kda_layer_core_fused_with_checkpoints(
+    int32_t num_seqs, int32_t total_tokens, int32_t num_heads, const void *qp, const void *kp,
+    const void *vp, const float *conv_w, const void *z, const float *A, const float *b,
+    const void *beta_logit, const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
+    float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated, float *S_final,
+    int32_t ckpt_every, const int32_t *ckpt_base, float *ckpt_states, void *stream) {
     if (!ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_checkpoints(ckpt_every, ckpt_base, ckpt_states)) return KDA_ERR_INVALID_ARGUMENT;
     if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
     if (!ok_ptr_elem(cu_seqlens, 4) || !ok_ptr(conv_w) || !ok_ptr_elem(A, 4) || !ok_opt_ptr(b))
         return KDA_ERR_INVALID_ARGUMENT;
@@ -251,6 +286,7 @@ kda_status kda_layer_core_fused(int32_t num_seqs, int32_t total_tokens, int32_t 
     a.conv_w = conv_w; a.A = A; a.b = b; a.S0 = S0; a.cu_seqlens = cu_seqlens;
     a.scale = scale; a.l2_eps = l2_eps; a.rms_eps = rms_eps;
     a.out_dtype = out_dtype; a.o = o_gated; a.S_final = S_final;
+    a.ckpt = Checkpoints{ckpt_every, ckpt_base, ckpt_states};
     a.status = device_status();
     return from_cuda(launch_layer_tc(a, static_cast<cudaStream_t>(stream)));
 }

@@ -77,6 +77,15 @@ struct DecodeArgs {
     DeviceStatus status;
 };
 
+// State snapshots during a prefill: for sequence n, snapshot k (k = 0, 1, ...) is the state
+// after its first (k + 1) * every tokens, written to states[(base[n] + k)][h][j][c] while
+// k < base[n + 1] - base[n].  every == 0: none.
+struct Checkpoints {
+    int32_t every;
+    const int32_t *base;
+    float *states;
+};
+
 // One decode step of the whole layer core for a batch of requests whose recurrent state
 // and short-convolution state live in pools indexed by slot.
 struct DecodeLayerArgs {
@@ -103,6 +112,7 @@ struct PrefillArgs {
     float *S_final;
     void *workspace;
     size_t workspace_bytes;
+    Checkpoints ckpt;
     DeviceStatus status;
 };
 
@@ -136,6 +146,7 @@ struct LayerArgs {
     kda_dtype out_dtype;
     void *o;
     float *S_final;
+    Checkpoints ckpt;
     DeviceStatus status;
 };
 

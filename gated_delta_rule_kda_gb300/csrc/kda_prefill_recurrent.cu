@@ -30,13 +30,13 @@ constexpr int kPadRow = kD + 16; // padded vector: 4 floats after every 32 rows
 
 __device__ __forceinline__ int prow(int row) { return row + 4 * (row >> 5); }
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, bool kCkpt>
 __global__ void __launch_bounds__(kThreads)
 prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                          const Tin *__restrict__ v, const float *__restrict__ log_alpha,
                          const float *__restrict__ beta, const float *__restrict__ S0,
                          const int32_t *__restrict__ cu_seqlens, int H, float scale,
-                         Tout *__restrict__ o, float *__restrict__ S_final) {
+                         Tout *__restrict__ o, float *__restrict__ S_final, const Checkpoints ckpt) {
     __shared__ __align__(16) float s_q[kTB][kPadRow];
     __shared__ __align__(16) float s_k[kTB][kPadRow];
     __shared__ __align__(16) float s_a[kTB][kPadRow];
@@ -149,6 +149,18 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             p += __shfl_xor_sync(0xffffffffu, p, 1);
             p += __shfl_xor_sync(0xffffffffu, p, 2);
             if (rq == 0) s_o[tt][cl] = scale * p;
+            if (kCkpt) {  // snapshot after every `every` tokens of the sequence
+                const int done = t0 + tt + 1 - t_begin;
+                if (done % ckpt.every == 0) {
+                    const int kk = done / ckpt.every - 1;
+                    const int base = ckpt.base[n];
+                    if (kk < ckpt.base[n + 1] - base) {
+                        float *dst = ckpt.states + ((size_t)(base + kk) * H + h) * (size_t)(kD * kD);
+#pragma unroll
+                        for (int i = 0; i < kRows; ++i) dst[(size_t)(kRows * rq + i) * kD + col0 + cl] = s[i];
+                    }
+                }
+            }
         }
         __syncthreads();
         // write the batch's outputs: nb tokens x 32 columns
@@ -168,10 +180,13 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 template <typename Tin, typename Tout>
 cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
     dim3 grid(kSplit, a.num_heads, a.num_seqs);
-    prefill_recurrent_kernel<Tin, Tout><<<grid, kThreads, 0, stream>>>(
+    // snapshots are a separate instantiation, so the loop without them is untouched
+    auto kernel = a.ckpt.every > 0 ? prefill_recurrent_kernel<Tin, Tout, true>
+                                   : prefill_recurrent_kernel<Tin, Tout, false>;
+    kernel<<<grid, kThreads, 0, stream>>>(
         static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k),
         static_cast<const Tin *>(a.v), a.log_alpha, a.beta, a.S0, a.cu_seqlens, a.num_heads,
-        a.scale, static_cast<Tout *>(a.o), a.S_final);
+        a.scale, static_cast<Tout *>(a.o), a.S_final, a.ckpt);
     return cudaGetLastError();
 }
 

@@ -165,6 +165,7 @@ struct Params {
     const __nv_bfloat16 *z, *beta_logit, *g;
     const float *conv_w, *A, *b;
     float l2_eps, rms_eps;
+    Checkpoints ckpt;  // read only by the instantiation that takes snapshots
 };
 
 // 1 / (1 + 2^(-x log2 e)) on the SFU: ex2.approx and rcp.approx, each within about
@@ -804,7 +805,23 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
 // ============================================================================
 // Chain group (warps 0-3): the state-dependent products, chunk by chunk.
 // ============================================================================
-template <typename Tout, bool kLayer>
+template <bool B>
+struct BoolTag {
+    static constexpr bool value = B;
+};
+
+// Snapshot slot for the state after `done` tokens of a sequence whose slots are
+// [base, base + count) (head h), or null when `done` is not a positive multiple of the
+// interval or the sequence has no slot for it.
+__device__ __forceinline__ float *snapshot_dst(const Params &p, int base, int count, int h,
+                                               int done) {
+    if (done <= 0 || done % p.ckpt.every != 0) return nullptr;
+    const int k = done / p.ckpt.every - 1;
+    if (k >= count) return nullptr;
+    return p.ckpt.states + ((size_t)(base + k) * p.H + h) * (size_t)(kD * kD);
+}
+
+template <typename Tout, bool kLayer, bool kCkpt>
 __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, uint32_t tb,
                                             int h, int n, int t_begin, int t_end, int nchunks) {
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -817,6 +834,11 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
     Tout *o = static_cast<Tout *>(p.o);
     uint32_t ph = 0;  // MMA barrier phase (CA and CB)
     bool alive = true;
+    int snap_base = 0, snap_count = 0;  // this sequence's snapshot slots
+    if constexpr (kCkpt) {
+        snap_base = p.ckpt.base[n];
+        snap_count = p.ckpt.base[n + 1] - snap_base;
+    }
 
     // ---- entering state -> TMEM, transposed (lane c, column j) ----
 #pragma unroll
@@ -927,36 +949,52 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
         bool m2_ok = true;
         {
             const float *e31p = vec + 2 * kD + s * kD;
+            auto f4 = [&](auto with_snapshot, float *snap) {
+                constexpr bool kSnap = decltype(with_snapshot)::value;
 #pragma unroll
-            for (int part = 0; part < 4; ++part) {
-                if (part == 1 && (tid == kCA || tid == kCB)) {
-                    m2_ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p.status, 24);
-                    if (m2_ok && tid == kCA) mbar_arrive(bar + B_VFREE + s);
-                }
-                const int j0 = 32 * part;
-                float sv[32];
-                tmem_ld32(tl + TM_ST + j0, sv);
-                uint32_t hw[16], lw[16], yv[32];
+                for (int part = 0; part < 4; ++part) {
+                    if (part == 1 && (tid == kCA || tid == kCB)) {
+                        m2_ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p.status, 24);
+                        if (m2_ok && tid == kCA) mbar_arrive(bar + B_VFREE + s);
+                    }
+                    const int j0 = 32 * part;
+                    float sv[32];
+                    tmem_ld32(tl + TM_ST + j0, sv);
+                    uint32_t hw[16], lw[16], yv[32];
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 4) {
-                    const float4 ep = *reinterpret_cast<const float4 *>(e31p + j0 + jj);
-                    const float4 mm = *reinterpret_cast<const float4 *>(em + j0 + jj);
-                    const float2 a = mul2(make_float2(sv[jj], sv[jj + 1]), make_float2(ep.x, ep.y));
-                    const float2 b =
-                        mul2(make_float2(sv[jj + 2], sv[jj + 3]), make_float2(ep.z, ep.w));
-                    split2(a.x, a.y, hw[jj >> 1], lw[jj >> 1]);
-                    split2(b.x, b.y, hw[(jj >> 1) + 1], lw[(jj >> 1) + 1]);
-                    const float2 ya = mul2(a, make_float2(mm.x, mm.y));
-                    const float2 yb = mul2(b, make_float2(mm.z, mm.w));
-                    yv[jj] = __float_as_uint(ya.x);
-                    yv[jj + 1] = __float_as_uint(ya.y);
-                    yv[jj + 2] = __float_as_uint(yb.x);
-                    yv[jj + 3] = __float_as_uint(yb.y);
+                    for (int jj = 0; jj < 32; jj += 4) {
+                        const float4 ep = *reinterpret_cast<const float4 *>(e31p + j0 + jj);
+                        const float4 mm = *reinterpret_cast<const float4 *>(em + j0 + jj);
+                        const float2 a = mul2(make_float2(sv[jj], sv[jj + 1]), make_float2(ep.x, ep.y));
+                        const float2 b =
+                            mul2(make_float2(sv[jj + 2], sv[jj + 3]), make_float2(ep.z, ep.w));
+                        split2(a.x, a.y, hw[jj >> 1], lw[jj >> 1]);
+                        split2(b.x, b.y, hw[(jj >> 1) + 1], lw[(jj >> 1) + 1]);
+                        if constexpr (kSnap) {
+                            float *d = snap + (size_t)(j0 + jj) * kD + c_lane;
+                            d[0] = a.x; d[kD] = a.y; d[2 * kD] = b.x; d[3 * kD] = b.y;
+                        }
+                        const float2 ya = mul2(a, make_float2(mm.x, mm.y));
+                        const float2 yb = mul2(b, make_float2(mm.z, mm.w));
+                        yv[jj] = __float_as_uint(ya.x);
+                        yv[jj + 1] = __float_as_uint(ya.y);
+                        yv[jj + 2] = __float_as_uint(yb.x);
+                        yv[jj + 3] = __float_as_uint(yb.y);
+                    }
+                    tmem_st16u(tl + TM_OPS + (j0 >> 1), hw);
+                    tmem_st16u(tl + TM_OPS + 64 + (j0 >> 1), lw);
+                    tmem_st32(tl + TM_ST + j0, yv);
                 }
-                tmem_st16u(tl + TM_OPS + (j0 >> 1), hw);
-                tmem_st16u(tl + TM_OPS + 64 + (j0 >> 1), lw);
-                tmem_st32(tl + TM_ST + j0, yv);
-            }
+            };
+            // The entering state S0 is the state after kC c tokens: a snapshot when that is a
+            // multiple of the interval (F4 computes S0 in fp32 anyway).  Chunks without one
+            // run the loop without the stores.
+            float *snap = nullptr;
+            if constexpr (kCkpt) snap = snapshot_dst(p, snap_base, snap_count, h, kC * c);
+            if (kCkpt && snap != nullptr)
+                f4(BoolTag<true>{}, snap);
+            else
+                f4(BoolTag<false>{}, nullptr);
         }
         // ---- M2 and M2b done (W'^T is read next) ----
         {
@@ -1155,8 +1193,13 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             mbar_wait_bounded(bar + B_TG, (g_issued - 1) & 1, kWaitNs);
     }
 
-    // ---- final state S = Diag(e31_last) X (lane c, column j) -> S_final[j][c] ----
-    if (alive && p.S_final != nullptr) {
+    // ---- final state S = Diag(e31_last) X (lane c, column j) -> S_final[j][c], and the
+    //      last snapshot when the sequence ends on one ----
+    float *snap = nullptr;
+    if constexpr (kCkpt) {
+        if (nchunks > 0) snap = snapshot_dst(p, snap_base, snap_count, h, t_end - t_begin);
+    }
+    if (alive && (p.S_final != nullptr || snap != nullptr)) {
         const float *e31_last = vec + 4 * kD + ((nchunks - 1) & 1) * kD;
 #pragma unroll
         for (int part = 0; part < 4; ++part) {
@@ -1164,14 +1207,16 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             float sv[32];
             tmem_ld32(tl + TM_ST + j0, sv);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-                p.S_final[state_off + (size_t)(j0 + jj) * kD + c_lane] =
-                    nchunks > 0 ? sv[jj] * e31_last[j0 + jj] : sv[jj];
+            for (int jj = 0; jj < 32; ++jj) {
+                const float x = nchunks > 0 ? sv[jj] * e31_last[j0 + jj] : sv[jj];
+                if (p.S_final != nullptr) p.S_final[state_off + (size_t)(j0 + jj) * kD + c_lane] = x;
+                if (kCkpt && snap != nullptr) snap[(size_t)(j0 + jj) * kD + c_lane] = x;
+            }
         }
     }
 }
 
-template <typename Tout, bool kLayer>
+template <typename Tout, bool kLayer, bool kCkpt>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -1216,7 +1261,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     if (warp >= 4)
         prep_group<kLayer>(p, sm, tb, h, t_begin, t_end, nchunks);
     else
-        chain_group<Tout, kLayer>(p, sm, tb, h, n, t_begin, t_end, nchunks);
+        chain_group<Tout, kLayer, kCkpt>(p, sm, tb, h, n, t_begin, t_end, nchunks);
 
     fence_before_sync();
     __syncthreads();
@@ -1255,14 +1300,22 @@ bool encode_bf16_tiles(CUtensorMap *m, const void *base, int T, int H, int box_r
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <typename Tout, bool kLayer>
-cudaError_t launch_params(const Params &p, int num_seqs, int num_heads, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<Tout, kLayer>,
+template <typename Tout, bool kLayer, bool kCkpt>
+cudaError_t launch_kernel(const Params &p, int num_seqs, int num_heads, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<Tout, kLayer, kCkpt>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM_DYN);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)num_seqs * (unsigned)num_heads;
-    prefill_tc_kernel<Tout, kLayer><<<grid, kThreads, SM_DYN, stream>>>(p);
+    prefill_tc_kernel<Tout, kLayer, kCkpt><<<grid, kThreads, SM_DYN, stream>>>(p);
     return cudaGetLastError();
+}
+
+// Snapshots are a separate instantiation: the kernel without them is compiled as if the
+// snapshot code did not exist.
+template <typename Tout, bool kLayer>
+cudaError_t launch_params(const Params &p, int num_seqs, int num_heads, cudaStream_t stream) {
+    if (p.ckpt.every > 0) return launch_kernel<Tout, kLayer, true>(p, num_seqs, num_heads, stream);
+    return launch_kernel<Tout, kLayer, false>(p, num_seqs, num_heads, stream);
 }
 
 template <typename Tout>
@@ -1283,6 +1336,7 @@ cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
     p.scale = a.scale;
     p.o = a.o;
     p.S_final = a.S_final;
+    p.ckpt = a.ckpt;
     p.status = a.status;
     return launch_params<Tout, false>(p, a.num_seqs, a.num_heads, stream);
 }
@@ -1306,6 +1360,7 @@ cudaError_t launch_layer_typed(const LayerArgs &a, cudaStream_t stream) {
     p.scale = a.scale;
     p.o = a.o;
     p.S_final = a.S_final;
+    p.ckpt = a.ckpt;
     p.status = a.status;
     p.z = a.z;
     p.beta_logit = a.beta_logit;

@@ -39,6 +39,7 @@ EXPORTED = (
     "kda_version",
     "kda_prefill_workspace_size",
     "kda_prefill",
+    "kda_prefill_with_checkpoints",
     "kda_decode_step",
     "kda_frontend",
     "kda_output_gate",
@@ -46,6 +47,7 @@ EXPORTED = (
     "kda_layer_core",
     "kda_layer_core_noalloc",
     "kda_layer_core_fused",
+    "kda_layer_core_fused_with_checkpoints",
     "kda_decode_layer",
     "kda_get_device_status",
 )
@@ -76,6 +78,9 @@ def _load() -> ctypes.CDLL:
     lib.kda_prefill.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, I32, P, P, P, P, P, P, P,
                                 F, P, P, P, SZ, P]
     lib.kda_prefill.restype = ctypes.c_int
+    lib.kda_prefill_with_checkpoints.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, I32, P, P,
+                                                 P, P, P, P, P, F, P, P, P, SZ, I32, P, P, P]
+    lib.kda_prefill_with_checkpoints.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, P, P, P, P, P, P, F,
                                     P, P]
     lib.kda_decode_step.restype = ctypes.c_int
@@ -95,6 +100,10 @@ def _load() -> ctypes.CDLL:
     lib.kda_layer_core_fused.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, F, F,
                                          F, ctypes.c_int, P, P, P]
     lib.kda_layer_core_fused.restype = ctypes.c_int
+    lib.kda_layer_core_fused_with_checkpoints.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P,
+                                                          P, P, P, F, F, F, ctypes.c_int, P, P,
+                                                          I32, P, P, P]
+    lib.kda_layer_core_fused_with_checkpoints.restype = ctypes.c_int
     lib.kda_decode_layer.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, F, F, F,
                                      ctypes.c_int, P, P]
     lib.kda_decode_layer.restype = ctypes.c_int
@@ -175,6 +184,52 @@ def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, scale=DEFAULT_SCA
                           _p(S_final), _p(workspace), wbytes, _stream(stream))
     _check("kda_prefill", rc)
     return o, S_final
+
+
+def checkpoint_offsets(cu_seqlens, every: int) -> torch.Tensor:
+    """Snapshot offsets [N+1] int32 (host) for one snapshot per `every` tokens of each
+    sequence: base[n+1] - base[n] = len_n // every."""
+    cu = torch.as_tensor(cu_seqlens).to("cpu", torch.int64)
+    counts = torch.div(cu[1:] - cu[:-1], every, rounding_mode="floor")
+    return torch.cat([torch.zeros(1, dtype=torch.int64), counts.cumsum(0)]).to(torch.int32)
+
+
+def _checkpoint_args(cu_seqlens, H, every, ckpt_base, ckpt_states, device):
+    if ckpt_base is None:
+        ckpt_base = checkpoint_offsets(cu_seqlens, every).to(device)
+    if ckpt_states is None:
+        total = int(ckpt_base[-1])
+        ckpt_states = torch.empty((total, H, HEAD_DIM, HEAD_DIM), dtype=torch.float32,
+                                  device=device)
+    return ckpt_base, ckpt_states
+
+
+def kda_prefill_with_checkpoints(q, k, v, log_alpha, beta, cu_seqlens, every, S0=None,
+                                 scale=DEFAULT_SCALE, *, ckpt_base=None, ckpt_states=None,
+                                 out_dtype=None, o=None, S_final=None, want_state=True,
+                                 workspace=None, stream=None):
+    """kda_prefill that also writes the state after every `every` tokens of each sequence
+    (every: a positive multiple of 32).  ckpt_base [N+1] int32 (device) defaults to
+    checkpoint_offsets(cu_seqlens, every).  Returns (o, S_final, ckpt_base, ckpt_states)."""
+    T, H, _ = q.shape
+    N = cu_seqlens.shape[0] - 1
+    out_dtype = out_dtype or q.dtype
+    if o is None:
+        o = torch.empty((T, H, HEAD_DIM), dtype=out_dtype, device=q.device)
+    if S_final is None and want_state:
+        S_final = torch.empty((N, H, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=q.device)
+    ckpt_base, ckpt_states = _checkpoint_args(cu_seqlens, H, every, ckpt_base, ckpt_states,
+                                              q.device)
+    need = kda_prefill_workspace_size(N, T, H, q.dtype)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = _lib.kda_prefill_with_checkpoints(
+        _dt(q), _dtype_code(o.dtype), N, T, H, _p(q), _p(k), _p(v), _p(log_alpha), _p(beta),
+        _p(S0), _p(cu_seqlens), float(scale), _p(o), _p(S_final), _p(workspace), wbytes,
+        int(every), _p(ckpt_base), _p(ckpt_states), _stream(stream))
+    _check("kda_prefill_with_checkpoints", rc)
+    return o, S_final, ckpt_base, ckpt_states
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, S_inout, scale=DEFAULT_SCALE, *, out_dtype=None,
@@ -280,6 +335,30 @@ def kda_layer_core_fused(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens,
                                    _dtype_code(o.dtype), _p(o), _p(S_final), _stream(stream))
     _check("kda_layer_core_fused", rc)
     return o, S_final
+
+
+def kda_layer_core_fused_with_checkpoints(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens,
+                                          every, S0=None, scale=DEFAULT_SCALE, l2_eps=1e-6,
+                                          rms_eps=1e-6, *, ckpt_base=None, ckpt_states=None,
+                                          out_dtype=torch.bfloat16, o=None, S_final=None,
+                                          want_state=True, stream=None):
+    """kda_layer_core_fused that also writes the recurrent state after every `every` tokens
+    of each sequence.  Returns (o_gated, S_final, ckpt_base, ckpt_states)."""
+    T, H, _ = qp.shape
+    N = cu_seqlens.shape[0] - 1
+    if o is None:
+        o = torch.empty((T, H, HEAD_DIM), dtype=out_dtype, device=qp.device)
+    if S_final is None and want_state:
+        S_final = torch.empty((N, H, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=qp.device)
+    ckpt_base, ckpt_states = _checkpoint_args(cu_seqlens, H, every, ckpt_base, ckpt_states,
+                                              qp.device)
+    rc = _lib.kda_layer_core_fused_with_checkpoints(
+        N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A), _p(b), _p(beta_logit), _p(g),
+        _p(cu_seqlens), _p(S0), float(scale), float(l2_eps), float(rms_eps),
+        _dtype_code(o.dtype), _p(o), _p(S_final), int(every), _p(ckpt_base), _p(ckpt_states),
+        _stream(stream))
+    _check("kda_layer_core_fused_with_checkpoints", rc)
+    return o, S_final, ckpt_base, ckpt_states
 
 
 def kda_decode_layer(qp, kp, vp, conv_w, z, A, b, beta_logit, g, slot, S_pool, conv_pool,

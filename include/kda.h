@@ -115,6 +115,43 @@ kda_status kda_prefill(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs
                        float *S_final, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kda_prefill_with_checkpoints - kda_prefill that also leaves read-only state
+ * snapshots at fixed token intervals, the states a prefix cache keeps for later
+ * requests that share the prefix ("Kimi K3: Architecture and SGLang Day-0
+ * Support", section "RadixAttention: prefix caching for KDA state": a cached
+ * KDA state is a read-only checkpoint that a request copies into its own slot
+ * before it writes).
+ *
+ * For sequence n, snapshot i (i = 0, 1, ...) is the state after the sequence's
+ * first (i + 1) * ckpt_every tokens, written to
+ * ckpt_states[ckpt_base[n] + i][h][128][128] (fp32, row = key channel) for
+ * every i < ckpt_base[n + 1] - ckpt_base[n] whose token count lies inside the
+ * sequence; the caller sizes ckpt_base[n + 1] - ckpt_base[n] (at most
+ * floor(len_n / ckpt_every) snapshots are written; slots beyond are left as
+ * they are).  A snapshot equals, to rounding, the S_final of a kda_prefill
+ * over that prefix alone.
+ *
+ *   ckpt_every   0 (no snapshots: identical to kda_prefill) or a positive
+ *                multiple of 32, the tensor-core kernel's chunk length
+ *   ckpt_base    [N+1] int32 (device), non-decreasing snapshot offsets;
+ *                read only when ckpt_every > 0
+ *   ckpt_states  [ckpt_base[N]][H][128][128] fp32 (device, 16-byte aligned);
+ *                must not overlap any other argument
+ *   (all other arguments as kda_prefill)
+ * Errors: as kda_prefill; KDA_ERR_INVALID_ARGUMENT also for a ckpt_every that
+ * is negative or not a multiple of 32, or null/misaligned ckpt_base/ckpt_states
+ * when ckpt_every > 0.
+ */
+kda_status kda_prefill_with_checkpoints(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
+                                        int32_t total_tokens, int32_t num_heads, const void *q,
+                                        const void *k, const void *v, const float *log_alpha,
+                                        const float *beta, const float *S0,
+                                        const int32_t *cu_seqlens, float scale, void *o,
+                                        float *S_final, void *workspace, size_t workspace_bytes,
+                                        int32_t ckpt_every, const int32_t *ckpt_base,
+                                        float *ckpt_states, void *stream);
+
+/*
  * kda_decode_step - one token per request, state updated in place.
  *
  * One step of the recurrence for each (request b, head h): "each step reads
@@ -268,6 +305,21 @@ kda_status kda_layer_core_fused(int32_t num_seqs, int32_t total_tokens, int32_t 
                                 const int32_t *cu_seqlens, const float *S0, float scale,
                                 float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
                                 float *S_final, void *stream);
+
+/*
+ * kda_layer_core_fused_with_checkpoints - kda_layer_core_fused that also leaves
+ * the recurrent state's snapshots every ckpt_every tokens of each sequence, as
+ * kda_prefill_with_checkpoints does (same ckpt_every, ckpt_base, ckpt_states
+ * meaning, layout and errors).  A snapshot holds only the recurrent state; the
+ * short convolution's state at that token is the three pre-convolution inputs
+ * before it, which the caller already holds in qp, kp, vp.
+ */
+kda_status kda_layer_core_fused_with_checkpoints(
+    int32_t num_seqs, int32_t total_tokens, int32_t num_heads, const void *qp, const void *kp,
+    const void *vp, const float *conv_w, const void *z, const float *A, const float *b,
+    const void *beta_logit, const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
+    float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated, float *S_final,
+    int32_t ckpt_every, const int32_t *ckpt_base, float *ckpt_states, void *stream);
 
 /*
  * kda_decode_layer - one decode step of the whole layer core for a batch of

@@ -140,6 +140,55 @@ def test_layer_core_fused_too_many_heads_unsupported(kda):
     assert _fused(kda.library(), H=70000) == 2
 
 
+# Checkpoint arguments: every must be 0 or a positive multiple of 32; with every > 0 the
+# offsets need 4-byte and the snapshot states 16-byte alignment.
+BAD_CKPT = [dict(every=-32), dict(every=16), dict(every=48), dict(every=1),
+            dict(every=32, base=None), dict(every=32, base=FAKE + 2),
+            dict(every=32, states=None), dict(every=64, states=MIS)]
+
+
+def _ckpt(kw):
+    c = dict(every=32, base=FAKE, states=FAKE + (1 << 30))
+    c.update(kw)
+    return c
+
+
+@pytest.mark.parametrize("bad", BAD_CKPT)
+def test_prefill_with_checkpoints_rejects_bad_checkpoint_arguments(kda, bad):
+    c = _ckpt(bad)
+    rc = kda.library().kda_prefill_with_checkpoints(
+        0, 0, 1, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 0.1, FAKE, None, None, 0,
+        c["every"], c["base"], c["states"], None)
+    assert rc == 1
+
+
+@pytest.mark.parametrize("bad", BAD_CKPT)
+def test_layer_core_fused_with_checkpoints_rejects_bad_checkpoint_arguments(kda, bad):
+    c = _ckpt(bad)
+    rc = kda.library().kda_layer_core_fused_with_checkpoints(
+        1, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, 0.1, 1e-6,
+        1e-6, 0, FAKE, None, c["every"], c["base"], c["states"], None)
+    assert rc == 1
+
+
+def test_with_checkpoints_still_validates_the_prefill_arguments(kda):
+    lib = kda.library()
+    rc = lib.kda_prefill_with_checkpoints(0, 0, 1, 4, 2, None, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                          0.1, FAKE, None, None, 0, 32, FAKE, FAKE + (1 << 30),
+                                          None)
+    assert rc == 1  # q missing
+    rc = lib.kda_layer_core_fused_with_checkpoints(1, 4, 70000, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                                   None, FAKE, FAKE, FAKE, None, 0.1, 1e-6, 1e-6,
+                                                   0, FAKE, None, 32, FAKE, FAKE + (1 << 30), None)
+    assert rc == 2  # too many heads
+
+
+def test_checkpoint_offsets(kda):
+    base = kda.checkpoint_offsets([0, 100, 100, 164, 500], 32)
+    assert base.tolist() == [0, 3, 3, 5, 15]
+    assert kda.checkpoint_offsets([0, 31], 32).tolist() == [0, 0]
+
+
 def _decode_layer(lib, **kw):
     a = dict(B=2, H=2, P=4, qp=FAKE, kp=FAKE, vp=FAKE, w=FAKE, z=FAKE, A=FAKE, b=None, bl=FAKE,
              g=FAKE, slot=FAKE, S=FAKE, conv=FAKE + (1 << 24), out_dt=0, o=FAKE)
