@@ -57,8 +57,8 @@ E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the ke
 # carried over only across comment-only edits whose compiled kernel is byte-identical).
 TRAFFIC = {
     "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-                "8802617ff1d76bdc6341c9155d3e784e6ab4c482d4cbbfc322da9e60f7b331e0",
-                (252.558592e6 + 37.625600e6) / (2048 * 96)),
+                "5303b22009e876fdca151866d5e7d3aa69ce6e133ce435008f6712411f876b2e",
+                (252.618240e6 + 37.963008e6) / (2048 * 96)),
     "decode": ("gated_delta_rule_kda_gb300/csrc/kda_decode.cu",
                "1bf0e4585307540aec99de0bebe444ea914f399db22eb7540d6128919bfb40b0",
                (205.3e6 + 142.4e6) / (32 * 96)),
@@ -288,6 +288,25 @@ def run_ours(args, world, rank, local):
                 "binding_roofline_frac": max(alg_bytes / (hbm * 1e9),
                                              alg_flop / (tc * 1e12)) / (launch_ms / 1e3)}
 
+    # ---------------- the same prefill leaving a state snapshot every 1024 tokens ----------------
+    ck_every = 1024
+    ck_base = kda.checkpoint_offsets(inp.cu_seqlens, ck_every).to(dev)
+    ck_states = torch.empty((int(ck_base[-1]), H, D, D), dtype=torch.float32, device=dev)
+
+    def checkpoint_step():
+        kda.kda_prefill_with_checkpoints(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta,
+                                         inp.cu_seqlens, ck_every, None, ckpt_base=ck_base,
+                                         ckpt_states=ck_states, o=o, S_final=Sf)
+
+    ck_total, _ = time_launches(checkpoint_step, args.steps, args.warmup, world)
+    ck_ms = max_over_ranks(ck_total / args.steps, world)
+    checkpoints = {"entry_point": "kda_prefill_with_checkpoints", "every_tokens": ck_every,
+                   "snapshots": int(ck_base[-1]) * H,
+                   "snapshot_bytes": ck_states.numel() * 4, "ms_per_step": ck_ms,
+                   "tokens_per_s": aggregate_rate(tokens_per_step, ck_ms, world),
+                   "overhead_vs_prefill": ck_ms / ms_step - 1.0}
+    del ck_states
+
     # ---------------- end to end through the C ABI with host buffers ----------------
     host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "log_alpha", "beta")}
     dev_bufs = {n: getattr(inp, n) for n in host}
@@ -457,7 +476,8 @@ def run_ours(args, world, rank, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "decode": decode,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "prefill_checkpoints": checkpoints, "decode": decode,
             "decode_layer": decode_layer, "layer_core": layer,
             "clocks": clk, "gpu_launches": args.steps,
             "kernel_ms_mean": launch_ms,
