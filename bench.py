@@ -45,6 +45,10 @@ DECODE_FLOP_PER_UNIT = 2 * 4 * D * D
 # bf16; plus, once per step and head, the convolution weights and the decay parameters.
 DECODE_LAYER_BYTES_PER_UNIT = 2 * STATE_BYTES + 2 * 9 * D * 2 + 5 * D * 2 + 2 + D * 2  # 137,218 B
 DECODE_LAYER_BYTES_PER_HEAD = 3 * D * 4 * 4 + 4 + D * 4
+# Several tokens per request from a pooled state, per (request, head) and token: q, k, v bf16,
+# log_alpha fp32, beta, o bf16; per (request, head): the state read, and written back when the
+# accepted tokens are replayed.
+DECODE_TOKENS_BYTES_PER_TOKEN = 3 * D * 2 + D * 4 + 4 + D * 2           # 1,540 B
 # Fused layer core, per (token, head): q^p, k^p, v^p, z, g bf16 in, o^g bf16 out, beta_logit.
 LAYER_BYTES_PER_TOKEN_HEAD = 5 * D * 2 + 2 + D * 2                      # 1,538 B
 E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the kernels)
@@ -420,6 +424,30 @@ def run_ours(args, world, rank, local):
     del linp1, odl
     torch.cuda.empty_cache()
 
+    # ---------------- a 4-token draft per request: verify, then replay ----------------
+    ntok = 4
+    tinp = synthetic.decode_tokens_inputs([ntok] * 256, 96, 256, device=dev)
+    ot = torch.empty((256 * ntok, 96, D), dtype=torch.bfloat16, device=dev)
+    spec = {"workload": f"256 requests x {ntok} tokens x 96 heads from shuffled rows of a "
+                        "256-row state pool", "entry_point": "kda_decode_tokens"}
+    for mode, wb in (("verify", False), ("replay", True)):
+        def tokens_step():
+            kda.kda_decode_tokens(tinp.q, tinp.k, tinp.v, tinp.log_alpha, tinp.beta,
+                                  tinp.cu_tokens, tinp.slot, tinp.S_pool, wb, o=ot)
+
+        t_total, t_per = time_launches(tokens_step, args.steps, args.warmup, world)
+        t_ms = max_over_ranks(t_total / args.steps, world)
+        t_launch = sum(t_per) / len(t_per)
+        t_bytes = 256 * 96 * ((2 if wb else 1) * STATE_BYTES + ntok * DECODE_TOKENS_BYTES_PER_TOKEN)
+        t_ach = t_bytes / (t_launch / 1e3) / 1e9
+        spec[mode] = {"tokens_per_s": aggregate_rate(256 * ntok, t_ms, world), "ms_per_step": t_ms,
+                      "write_back": wb,
+                      "roofline": {"bound": "hbm", "achieved": t_ach, "peak": hbm, "unit": "GB/s",
+                                   "frac": t_ach / hbm, "traffic": None, "peak_kind": peak_kind,
+                                   "kernel": "kda_decode_tokens"}}
+    del tinp, ot
+    torch.cuda.empty_cache()
+
     # ---------------- layer core (varlen, 16 sequences) ----------------
     layer = None
     if not args.skip_layer_core:
@@ -478,7 +506,7 @@ def run_ours(args, world, rank, local):
             "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "prefill_checkpoints": checkpoints, "decode": decode,
-            "decode_layer": decode_layer, "layer_core": layer,
+            "decode_layer": decode_layer, "speculative": spec, "layer_core": layer,
             "clocks": clk, "gpu_launches": args.steps,
             "kernel_ms_mean": launch_ms,
         }
@@ -516,6 +544,13 @@ def run_only(args, local):
                                           linp1.A, linp1.b, linp1.beta_logit, linp1.g, linp1.slot,
                                           linp1.S_pool, linp1.conv_pool, o=odl)
         units = B
+    elif args.only == "decode_tokens":
+        B = 32 if args.small else 256
+        tinp = synthetic.decode_tokens_inputs([4] * B, 96, B, device=dev)
+        ot = torch.empty((4 * B, 96, D), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_decode_tokens(tinp.q, tinp.k, tinp.v, tinp.log_alpha, tinp.beta,
+                                           tinp.cu_tokens, tinp.slot, tinp.S_pool, True, o=ot)
+        units = B
     else:
         B = 32 if args.small else 256
         dinp = synthetic.decode_inputs(B, 96, torch.bfloat16, device=dev)
@@ -538,7 +573,8 @@ def main():
     ap.add_argument("--skip-layer-core", action="store_true")
     ap.add_argument("--skip-staged-layer-core", action="store_true",
                     help="time only the fused layer core, not the three-launch composition")
-    ap.add_argument("--only", choices=["prefill", "decode", "decode_layer", "layer"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "decode_layer", "decode_tokens", "layer"],
+                    default=None,
                     help="profiling aid: run just this kernel (no baseline, no e2e)")
     ap.add_argument("--small", action="store_true",
                     help="with --only: a smaller case sized for ncu captures")

@@ -325,6 +325,42 @@ kda_status kda_decode_layer(int32_t batch, int32_t num_heads, int32_t pool_size,
     return from_cuda(launch_decode_layer(a, static_cast<cudaStream_t>(stream)));
 }
 
+kda_status kda_decode_tokens(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batch,
+                             int32_t num_heads, int32_t pool_size, int32_t total_tokens,
+                             const int32_t *cu_tokens, const int32_t *slot, const void *q,
+                             const void *k, const void *v, const float *log_alpha,
+                             const float *beta, float *S_pool, int32_t write_back, float *S_final,
+                             float scale, void *o, void *stream) {
+    if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (batch < 1 || num_heads < 1 || pool_size < 1 || total_tokens < 0)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (write_back != 0 && write_back != 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_ptr_elem(cu_tokens, 4) || !ok_ptr_elem(slot, 4) || !ok_ptr(S_pool) ||
+        !ok_opt_ptr(S_final))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (total_tokens > 0 && (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(log_alpha) ||
+                             !ok_ptr_elem(beta, 4) || !ok_ptr(o)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    const size_t unit_bytes = (size_t)num_heads * kD * kD * sizeof(float);
+    if (S_final != nullptr) {
+        const uintptr_t sp = reinterpret_cast<uintptr_t>(S_pool), fp = reinterpret_cast<uintptr_t>(S_final);
+        if (sp < fp + batch * unit_bytes && fp < sp + pool_size * unit_bytes)
+            return KDA_ERR_INVALID_ARGUMENT;  // S_final overlaps the pool
+    }
+    // (the persistent kernel steps unit indices by its grid: they stay below 2^31)
+    if ((int64_t)batch * num_heads > 0x7fff0000LL || (int64_t)total_tokens * num_heads > 0x7fffffffLL)
+        return KDA_ERR_UNSUPPORTED;
+    DecodeTokensArgs a;
+    a.in_dtype = in_dtype; a.out_dtype = out_dtype;
+    a.batch = batch; a.num_heads = num_heads; a.pool_size = pool_size; a.total_tokens = total_tokens;
+    a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta;
+    a.cu_tokens = cu_tokens; a.slot = slot;
+    a.S_pool = S_pool; a.write_back = write_back; a.S_final = S_final;
+    a.scale = scale; a.o = o;
+    a.status = device_status();
+    return from_cuda(launch_decode_tokens(a, static_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_get_device_status(void *stream, uint32_t *detail) {
     if (detail) *detail = 0;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)

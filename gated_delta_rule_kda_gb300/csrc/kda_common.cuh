@@ -77,6 +77,22 @@ struct DecodeArgs {
     DeviceStatus status;
 };
 
+// Several tokens per request from a pooled state: request b's tokens are rows
+// [cu_tokens[b], cu_tokens[b+1]) of q, k, v, log_alpha, beta; its state is S_pool[slot[b]].
+struct DecodeTokensArgs {
+    kda_dtype in_dtype, out_dtype;
+    int32_t batch, num_heads, pool_size, total_tokens;
+    const void *q, *k, *v;                 // [T][H][128]
+    const float *log_alpha, *beta;         // [T][H][128], [T][H]
+    const int32_t *cu_tokens, *slot;       // [B+1], [B]
+    float *S_pool;                         // [P][H][128][128]
+    int32_t write_back;                    // 1: the final state goes back to the pool row
+    float *S_final;                        // [B][H][128][128] or null
+    float scale;
+    void *o;                               // [T][H][128]
+    DeviceStatus status;
+};
+
 // State snapshots during a prefill: for sequence n, snapshot k (k = 0, 1, ...) is the state
 // after its first (k + 1) * every tokens, written to states[(base[n] + k)][h][j][c] while
 // k < base[n + 1] - base[n].  every == 0: none.
@@ -152,6 +168,7 @@ struct LayerArgs {
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_decode_layer(const DecodeLayerArgs &a, cudaStream_t stream);
+cudaError_t launch_decode_tokens(const DecodeTokensArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_recurrent(const PrefillArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 cudaError_t launch_layer_tc(const LayerArgs &a, cudaStream_t stream);

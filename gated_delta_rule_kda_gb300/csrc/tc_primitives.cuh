@@ -343,6 +343,15 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(x), "l"(y));
     return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
 }
+// Packed fp32x2 fused multiply-add: (a0 b0 + c0, a1 b1 + c1), each rounded once.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t x = ((uint64_t)__float_as_uint(a.y) << 32) | __float_as_uint(a.x);
+    uint64_t y = ((uint64_t)__float_as_uint(b.y) << 32) | __float_as_uint(b.x);
+    uint64_t z = ((uint64_t)__float_as_uint(c.y) << 32) | __float_as_uint(c.x);
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(x), "l"(y), "l"(z));
+    return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
 // 2^x on the SFU (max relative error about 2^-22).
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;

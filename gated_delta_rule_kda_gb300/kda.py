@@ -49,6 +49,7 @@ EXPORTED = (
     "kda_layer_core_fused",
     "kda_layer_core_fused_with_checkpoints",
     "kda_decode_layer",
+    "kda_decode_tokens",
     "kda_get_device_status",
 )
 
@@ -107,6 +108,9 @@ def _load() -> ctypes.CDLL:
     lib.kda_decode_layer.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P, F, F, F,
                                      ctypes.c_int, P, P]
     lib.kda_decode_layer.restype = ctypes.c_int
+    lib.kda_decode_tokens.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, I32, I32, P, P, P, P,
+                                      P, P, P, P, I32, P, F, P, P]
+    lib.kda_decode_tokens.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.kda_get_device_status.restype = ctypes.c_int
     return lib
@@ -379,6 +383,26 @@ def kda_decode_layer(qp, kp, vp, conv_w, z, A, b, beta_logit, g, slot, S_pool, c
                                float(scale), float(l2_eps), float(rms_eps), _dtype_code(o.dtype),
                                _p(o), _stream(stream))
     _check("kda_decode_layer", rc)
+    return o
+
+
+def kda_decode_tokens(q, k, v, log_alpha, beta, cu_tokens, slot, S_pool, write_back,
+                      scale=DEFAULT_SCALE, *, S_final=None, out_dtype=None, o=None, stream=None):
+    """A few tokens per request from pool rows (speculative verify: write_back=False;
+    replay of accepted tokens: write_back=True).  q, k, v [T, H, 128]; log_alpha
+    [T, H, 128] fp32; beta [T, H] fp32; cu_tokens [B+1] int32 and slot [B] int32 (device);
+    S_pool [P, H, 128, 128] fp32.  Returns o [T, H, 128]."""
+    T, H, _ = q.shape
+    B = slot.shape[0]
+    P = S_pool.shape[0]
+    out_dtype = out_dtype or q.dtype
+    if o is None:
+        o = torch.empty((T, H, HEAD_DIM), dtype=out_dtype, device=q.device)
+    rc = _lib.kda_decode_tokens(_dt(q), _dtype_code(o.dtype), B, H, P, T, _p(cu_tokens),
+                                _p(slot), _p(q), _p(k), _p(v), _p(log_alpha), _p(beta),
+                                _p(S_pool), int(bool(write_back)), _p(S_final), float(scale),
+                                _p(o), _stream(stream))
+    _check("kda_decode_tokens", rc)
     return o
 
 

@@ -207,6 +207,40 @@ def decode_layer_inputs(B: int, H: int, P: int, seed: int = BASE_SEED + 6,
     return DecodeLayerInputs(qp, kp, vp, conv_w, z, A, b, beta_logit, gg, slot, S_pool, conv_pool)
 
 
+@dataclass
+class DecodeTokensInputs:
+    q: torch.Tensor           # [T, H, 128] dtype, the requests' tokens packed
+    k: torch.Tensor
+    v: torch.Tensor
+    log_alpha: torch.Tensor   # [T, H, 128] fp32, in (-5, 0)
+    beta: torch.Tensor        # [T, H] fp32
+    cu_tokens: torch.Tensor   # [B+1] int32
+    slot: torch.Tensor        # [B] int32, distinct shuffled rows of the pool
+    S_pool: torch.Tensor      # [P, H, 128, 128] fp32
+
+
+def decode_tokens_inputs(lengths: Sequence[int], H: int, P: int, dtype=torch.bfloat16,
+                         seed: int = BASE_SEED + 7, x_std: float = 2.0, s_std: float = 0.1,
+                         device="cpu") -> DecodeTokensInputs:
+    """A few tokens per request (a speculative draft), with the decode workload's
+    distributions; request b has lengths[b] tokens and its state in row slot[b] of a
+    P-row pool (state ~N(0, s_std))."""
+    B = len(lengths)
+    if P < B:
+        raise ValueError("the pool needs at least one row per request")
+    g = _gen(seed, device)
+    T = int(sum(lengths))
+    q = _unit_rows(_randn((T, H, D), g, device)).to(dtype)
+    k = _unit_rows(_randn((T, H, D), g, device)).to(dtype)
+    v = _randn((T, H, D), g, device).to(dtype)
+    la = torch.sigmoid(_randn((T, H, D), g, device, 0.0, x_std)).mul_(-5.0)
+    beta = torch.sigmoid(_randn((T, H), g, device))
+    slot = torch.randperm(P, generator=g, device=device)[:B].to(torch.int32)
+    S_pool = _randn((P, H, D, D), g, device, 0.0, s_std)
+    return DecodeTokensInputs(q, k, v, la.contiguous(), beta.contiguous(),
+                              cu_from_lengths(lengths, device), slot, S_pool)
+
+
 def workload(index: int, device="cpu"):
     """The five named workloads (see the module docstring)."""
     seed = BASE_SEED + index

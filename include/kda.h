@@ -369,6 +369,58 @@ kda_status kda_decode_layer(int32_t batch, int32_t num_heads, int32_t pool_size,
                             void *o, void *stream);
 
 /*
+ * kda_decode_tokens - a few tokens per request from a state held in a pool:
+ * the verify and replay steps of speculative decoding.
+ *
+ * For each request b, its tokens t in [cu_tokens[b], cu_tokens[b+1]) run the
+ * recurrence in order, starting from S_pool[slot[b]][h], exactly as kda_prefill
+ * over that sequence with S0 = that row.  o~ is written for every token.  The
+ * state after the request's last token goes back to the pool row when
+ * write_back = 1, and to S_final[b] when S_final is not NULL.
+ *   Verify (write_back = 0): the draft tokens are scored against the row
+ *   without changing it, so rows may be shared by several requests (branches
+ *   from one cached state).  Replay (write_back = 1): the accepted tokens are
+ *   run again and the row advances ("Inside Kimi K3: How KDA, AttnRes, and 896
+ *   Experts Work", section "What could go wrong": a rejected draft cannot be
+ *   rolled back in a recurrent state, so the accepted inputs are replayed;
+ *   "Kimi K3: Architecture and SGLang Day-0 Support", section "RadixAttention:
+ *   prefix caching for KDA state": a request mutates only its own slot).
+ * Each (request, head) reads its state once and writes it at most twice, with
+ * all of the request's tokens applied in registers in between: meant for a few
+ * tokens (a speculative draft); longer inputs belong to kda_prefill.
+ *
+ *   in_dtype, out_dtype  as kda_decode_step
+ *   batch        B >= 1 requests; num_heads H >= 1; pool_size P >= 1 rows
+ *   total_tokens T >= 0 rows of q, k, v, log_alpha, beta, o
+ *   cu_tokens    [B+1] int32 (device): 0 <= cu[b] <= cu[b+1] <= T (request b
+ *                may have zero tokens: its state is then copied unchanged)
+ *   slot         [B] int32 (device) pool rows in [0, P); with write_back = 1
+ *                no two requests may name the same row
+ *   q, k         [T][H][128] in_dtype, expected unit-norm per head
+ *   v            [T][H][128] in_dtype
+ *   log_alpha    [T][H][128] fp32 (-inf allowed: alpha = 0)
+ *   beta         [T][H] fp32
+ *   S_pool       [P][H][128][128] fp32
+ *   write_back   0 or 1
+ *   S_final      [B][H][128][128] fp32 or NULL; must not overlap S_pool
+ *   o            [T][H][128] out_dtype
+ * Pointers are caller-owned device memory, 16-byte aligned (beta, cu_tokens and
+ * slot 4-byte); q, k, v, log_alpha, beta and o may be NULL when T = 0.
+ * Errors: KDA_ERR_INVALID_ARGUMENT (null/misaligned pointers, bad sizes, dtype
+ * or write_back, S_final overlapping the pool), KDA_ERR_UNSUPPORTED (B * H above
+ * 2^31 - 2^16 or T * H above 2^31 - 1), KDA_ERR_CUDA (launch failure).  A request whose slot
+ * lies outside [0, P) or whose token range lies outside [0, T) is refused by
+ * the kernel: nothing is read or written for it and kda_get_device_status
+ * reports KDA_ERR_DEVICE_CHECK with detail = b.
+ */
+kda_status kda_decode_tokens(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batch,
+                             int32_t num_heads, int32_t pool_size, int32_t total_tokens,
+                             const int32_t *cu_tokens, const int32_t *slot, const void *q,
+                             const void *k, const void *v, const float *log_alpha,
+                             const float *beta, float *S_pool, int32_t write_back, float *S_final,
+                             float scale, void *o, void *stream);
+
+/*
  * kda_get_device_status - synchronises `stream`, then returns and clears the
  * device status word: KDA_OK, KDA_ERR_DEVICE_TIMEOUT or KDA_ERR_DEVICE_CHECK
  * (KDA_ERR_CUDA if the synchronisation itself fails).  If detail is not

@@ -223,3 +223,34 @@ def kda_decode_layer(qp, kp, vp, conv_w, z, A, b, beta_logit, g, slot, S_pool, c
         conv_new[slot, s, 1] = conv_pool[slot, s, 0]
         conv_new[slot, s, 0] = xp
     return o, S_new, conv_new
+
+
+def kda_decode_tokens(q, k, v, log_alpha, beta, cu_tokens, slot, S_pool, write_back, scale=None,
+                      n_threads=None):
+    """A few tokens per request from pooled states (fp64); inputs are not modified.
+
+    Request b runs the recurrence over its tokens [cu_tokens[b], cu_tokens[b+1]) from
+    S_pool[slot[b]]: the prefill recurrence with S0 = that row.  Speculative verify leaves
+    the pool as it is (write_back false); replay of the accepted tokens writes the state
+    after each request's last token back to its row (write_back true; "Inside Kimi K3: How
+    KDA, AttnRes, and 896 Experts Work", section "What could go wrong").
+
+    q, k: [T, H, dk]; v: [T, H, dv]; log_alpha: [T, H, dk]; beta: [T, H];
+    cu_tokens: [B+1]; slot: [B] rows in [0, P) (distinct when write_back);
+    S_pool: [P, H, dk, dv].  Returns (o [T, H, dv], S_pool_new, S_final [B, H, dk, dv]).
+    """
+    S_pool = _f64(S_pool)
+    slot = np.asarray(slot, dtype=np.int64)
+    P = S_pool.shape[0]
+    B = slot.shape[0]
+    cu = np.asarray(cu_tokens, dtype=np.int64)
+    if cu.shape != (B + 1,) or slot.size == 0 or slot.min() < 0 or slot.max() >= P:
+        raise ValueError("kda_decode_tokens: slots must lie in [0, P), one per request")
+    if write_back and len(set(slot.tolist())) != B:
+        raise ValueError("kda_decode_tokens: write-back needs distinct slots")
+    o, S_final = kda_prefill(q, k, v, log_alpha, beta, cu.astype(np.int32), S0=S_pool[slot],
+                             scale=scale, n_threads=n_threads)
+    S_new = S_pool.copy()
+    if write_back:
+        S_new[slot] = S_final
+    return o, S_new, S_final

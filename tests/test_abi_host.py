@@ -210,3 +210,28 @@ def test_decode_layer_rejects_bad_arguments(kda, bad):
 
 def test_decode_layer_grid_too_large_unsupported(kda):
     assert _decode_layer(kda.library(), B=1 << 20, H=1 << 12, conv=FAKE + (1 << 40)) == 2
+
+
+def _decode_tokens(lib, **kw):
+    a = dict(in_dt=0, out_dt=0, B=2, H=2, P=4, T=6, cu=FAKE, slot=FAKE, q=FAKE, k=FAKE, v=FAKE,
+             la=FAKE, beta=FAKE, S=FAKE, wb=1, Sf=None, o=FAKE)
+    a.update(kw)
+    return lib.kda_decode_tokens(a["in_dt"], a["out_dt"], a["B"], a["H"], a["P"], a["T"], a["cu"],
+                                 a["slot"], a["q"], a["k"], a["v"], a["la"], a["beta"], a["S"],
+                                 a["wb"], a["Sf"], 0.1, a["o"], None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(in_dt=4), dict(out_dt=2), dict(B=0), dict(H=0), dict(P=0), dict(T=-1), dict(wb=2),
+    dict(cu=None), dict(cu=FAKE + 2), dict(slot=None), dict(q=None), dict(k=MIS), dict(v=None),
+    dict(la=MIS), dict(beta=None), dict(S=None), dict(S=MIS), dict(Sf=MIS), dict(o=None),
+    dict(Sf=FAKE + 4 * 2 * 128 * 128 * 4 - 16),  # S_final starts inside the pool's last row
+    dict(S=FAKE + (1 << 30), Sf=FAKE + (1 << 30) - 16),  # S_final ends inside the pool
+])
+def test_decode_tokens_rejects_bad_arguments(kda, bad):
+    assert _decode_tokens(kda.library(), **bad) == 1
+
+
+def test_decode_tokens_too_large_unsupported(kda):
+    assert _decode_tokens(kda.library(), B=1 << 20, H=1 << 12, Sf=None) == 2
+    assert _decode_tokens(kda.library(), T=1 << 30, H=4) == 2

@@ -467,3 +467,67 @@ def test_decode_layer_rejects_repeated_or_out_of_range_slots():
     for slots in ([0, 0], [0, 2], [-1, 1]):
         with pytest.raises(ValueError):
             oracle.kda_decode_layer(*args, slots, S_pool, conv_pool)
+
+
+# P16 several tokens per request from pooled states (speculative verify and replay):
+#     the same as one decode step per token on the request's row, taken in order;
+#     verify leaves the pool untouched (and may share a row), replay advances only the
+#     rows it names ("Inside Kimi K3: How KDA, AttnRes, and 896 Experts Work", section
+#     "What could go wrong": accepted inputs are replayed).
+def test_decode_tokens_equals_decode_steps():
+    H, d, P = 2, 8, 5
+    lens, slot = [3, 0, 1, 4], [4, 0, 2, 1]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    rng = np.random.default_rng(800)
+    q, k = (unit(rng.standard_normal((T, H, d))) for _ in range(2))
+    v = rng.standard_normal((T, H, d))
+    la = -5.0 / (1.0 + np.exp(-rng.standard_normal((T, H, d)) * 2))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))
+    S_pool = rng.standard_normal((P, H, d, d)) * 0.3
+    for wb in (False, True):
+        o, S_new, S_fin = oracle.kda_decode_tokens(q, k, v, la, beta, cu, slot, S_pool, wb)
+        for b, n in enumerate(slot):
+            S = S_pool[n:n + 1]
+            for t in range(cu[b], cu[b + 1]):
+                sl = slice(t, t + 1)
+                ot, S = oracle.kda_decode_step(q[sl], k[sl], v[sl], la[sl], beta[sl], S)
+                np.testing.assert_allclose(o[t], ot[0], atol=1e-12)
+            np.testing.assert_allclose(S_fin[b], S[0], atol=1e-12)
+            np.testing.assert_array_equal(S_new[n], S[0] if wb else S_pool[n])
+        untouched = sorted(set(range(P)) - set(slot))
+        np.testing.assert_array_equal(S_new[untouched], S_pool[untouched])
+
+
+def test_decode_tokens_verify_then_replay():
+    """Verify a 4-token draft from a row, accept the first 2 (the draft's outputs for them
+    are the accepted outputs), replay them: the row equals the prefill over the accepted
+    prefix, and verifying the rest of the draft from it reproduces the draft's outputs."""
+    H, d = 2, 8
+    rng = np.random.default_rng(801)
+    q, k = (unit(rng.standard_normal((4, H, d))) for _ in range(2))
+    v = rng.standard_normal((4, H, d))
+    la = -5.0 / (1.0 + np.exp(-rng.standard_normal((4, H, d)) * 2))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((4, H))))
+    S_pool = rng.standard_normal((2, H, d, d)) * 0.3
+    o_draft, S_v, _ = oracle.kda_decode_tokens(q, k, v, la, beta, [0, 4], [1], S_pool, False)
+    np.testing.assert_array_equal(S_v, S_pool)
+    a = slice(0, 2)
+    _, S_r, _ = oracle.kda_decode_tokens(q[a], k[a], v[a], la[a], beta[a], [0, 2], [1], S_pool, True)
+    _, S_pre = oracle.kda_prefill(q[a], k[a], v[a], la[a], beta[a], [0, 2], S0=S_pool[1:2])
+    np.testing.assert_allclose(S_r[1], S_pre[0], atol=1e-12)
+    np.testing.assert_array_equal(S_r[0], S_pool[0])
+    r = slice(2, 4)
+    o_rest, _, _ = oracle.kda_decode_tokens(q[r], k[r], v[r], la[r], beta[r], [0, 2], [1], S_r, False)
+    np.testing.assert_allclose(o_rest, o_draft[2:], atol=1e-12)
+
+
+def test_decode_tokens_rejects_bad_slots():
+    z = np.zeros((2, 1, 4))
+    S = np.zeros((3, 1, 4, 4))
+    zb = np.zeros((2, 1))
+    with pytest.raises(ValueError):
+        oracle.kda_decode_tokens(z, z, z, z, zb, [0, 1, 2], [0, 3], S, False)
+    with pytest.raises(ValueError):
+        oracle.kda_decode_tokens(z, z, z, z, zb, [0, 1, 2], [1, 1], S, True)
+    oracle.kda_decode_tokens(z, z, z, z, zb, [0, 1, 2], [1, 1], S, False)  # shared row: verify only
