@@ -61,8 +61,8 @@ E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the ke
 # carried over only across comment-only edits whose compiled kernel is byte-identical).
 TRAFFIC = {
     "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-                "5303b22009e876fdca151866d5e7d3aa69ce6e133ce435008f6712411f876b2e",
-                (252.618240e6 + 37.963008e6) / (2048 * 96)),
+                "ea5cf3c551115ce9336f4d54ee528bc3935b50e9eaa2eefbb5a62dd4c3468568",
+                (252.724992e6 + 37.786880e6) / (2048 * 96)),
     "decode": ("gated_delta_rule_kda_gb300/csrc/kda_decode.cu",
                "1bf0e4585307540aec99de0bebe444ea914f399db22eb7540d6128919bfb40b0",
                (205.3e6 + 142.4e6) / (32 * 96)),
@@ -311,6 +311,26 @@ def run_ours(args, world, rank, local):
                    "overhead_vs_prefill": ck_ms / ms_step - 1.0}
     del ck_states
 
+    # ---------------- the Gated DeltaNet case: one decay per (token, head) ----------------
+    la_head = inp.log_alpha[:, :, 0].contiguous()  # [T, H]: one channel's draws as the head's decay
+
+    def head_decay_step():
+        kda.kda_prefill_head_decay(inp.q, inp.k, inp.v, la_head, inp.beta, inp.cu_seqlens, None,
+                                   o=o, S_final=Sf)
+
+    hd_total, hd_per = time_launches(head_decay_step, args.steps, args.warmup, world)
+    hd_ms = max_over_ranks(hd_total / args.steps, world)
+    hd_launch = sum(hd_per) / len(hd_per)
+    hd_bytes = T * H * (PREFILL_BYTES_PER_TOKEN_HEAD - D * 4 + 4) + H * STATE_BYTES
+    head_decay = {"entry_point": "kda_prefill_head_decay", "ms_per_step": hd_ms,
+                  "tokens_per_s": aggregate_rate(tokens_per_step, hd_ms, world),
+                  "roofline": {"bound": "hbm", "achieved": hd_bytes / (hd_launch / 1e3) / 1e9,
+                               "peak": hbm, "unit": "GB/s",
+                               "frac": hd_bytes / (hd_launch / 1e3) / 1e9 / hbm,
+                               "traffic": None, "peak_kind": peak_kind,
+                               "kernel": "kda_prefill_head_decay"}}
+    del la_head
+
     # ---------------- end to end through the C ABI with host buffers ----------------
     host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "log_alpha", "beta")}
     dev_bufs = {n: getattr(inp, n) for n in host}
@@ -505,7 +525,8 @@ def run_ours(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "prefill_checkpoints": checkpoints, "decode": decode,
+            "prefill_checkpoints": checkpoints, "prefill_head_decay": head_decay,
+            "decode": decode,
             "decode_layer": decode_layer, "speculative": spec, "layer_core": layer,
             "clocks": clk, "gpu_launches": args.steps,
             "kernel_ms_mean": launch_ms,

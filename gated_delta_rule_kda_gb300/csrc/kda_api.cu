@@ -88,21 +88,24 @@ kda_status kda_prefill(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs
                                         workspace, workspace_bytes, 0, nullptr, nullptr, stream);
 }
 
-kda_status kda_prefill_with_checkpoints(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
-                                        int32_t total_tokens, int32_t num_heads, const void *q,
-                                        const void *k, const void *v, const float *log_alpha,
-                                        const float *beta, const float *S0,
-                                        const int32_t *cu_seqlens, float scale, void *o,
-                                        float *S_final, void *workspace, size_t workspace_bytes,
-                                        int32_t ckpt_every, const int32_t *ckpt_base,
-                                        float *ckpt_states, void *stream) {
+}  // extern "C"
+
+namespace {
+// kda_prefill in full: per-channel decay ([T][H][128]) or one decay per (token, head) ([T][H]).
+kda_status prefill_impl(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
+                        int32_t total_tokens, int32_t num_heads, const void *q, const void *k,
+                        const void *v, const float *log_alpha, bool head_decay, const float *beta,
+                        const float *S0, const int32_t *cu_seqlens, float scale, void *o,
+                        float *S_final, void *workspace, size_t workspace_bytes,
+                        int32_t ckpt_every, const int32_t *ckpt_base, float *ckpt_states,
+                        void *stream) {
     if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
     if (!ok_checkpoints(ckpt_every, ckpt_base, ckpt_states)) return KDA_ERR_INVALID_ARGUMENT;
     if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
     if (!ok_ptr_elem(cu_seqlens, 4)) return KDA_ERR_INVALID_ARGUMENT;
     if (total_tokens > 0) {
-        if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(log_alpha) || !ok_ptr_elem(beta, 4) ||
-            !ok_ptr(o))
+        const bool la_ok = head_decay ? ok_ptr_elem(log_alpha, 4) : ok_ptr(log_alpha);
+        if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !la_ok || !ok_ptr_elem(beta, 4) || !ok_ptr(o))
             return KDA_ERR_INVALID_ARGUMENT;
     }
     if (!ok_opt_ptr(S0) || !ok_opt_ptr(S_final)) return KDA_ERR_INVALID_ARGUMENT;
@@ -121,6 +124,7 @@ kda_status kda_prefill_with_checkpoints(kda_dtype in_dtype, kda_dtype out_dtype,
     a.cu_seqlens = cu_seqlens; a.scale = scale; a.o = o; a.S_final = S_final;
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
     a.ckpt = Checkpoints{ckpt_every, ckpt_base, ckpt_states};
+    a.head_decay = head_decay ? 1 : 0;
     a.status = device_status();
     // bf16 inputs: chunked tensor-core kernel; fp32 inputs: full-precision recurrent kernel.
     if (in_dtype == KDA_BF16)
@@ -128,13 +132,46 @@ kda_status kda_prefill_with_checkpoints(kda_dtype in_dtype, kda_dtype out_dtype,
     return from_cuda(launch_prefill_recurrent(a, static_cast<cudaStream_t>(stream)));
 }
 
-kda_status kda_decode_step(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batch,
-                           int32_t num_heads, const void *q, const void *k, const void *v,
-                           const float *log_alpha, const float *beta, float *S_inout,
-                           float scale, void *o, void *stream) {
+}  // namespace
+
+extern "C" {
+
+kda_status kda_prefill_with_checkpoints(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
+                                        int32_t total_tokens, int32_t num_heads, const void *q,
+                                        const void *k, const void *v, const float *log_alpha,
+                                        const float *beta, const float *S0,
+                                        const int32_t *cu_seqlens, float scale, void *o,
+                                        float *S_final, void *workspace, size_t workspace_bytes,
+                                        int32_t ckpt_every, const int32_t *ckpt_base,
+                                        float *ckpt_states, void *stream) {
+    return prefill_impl(in_dtype, out_dtype, num_seqs, total_tokens, num_heads, q, k, v, log_alpha,
+                        false, beta, S0, cu_seqlens, scale, o, S_final, workspace, workspace_bytes,
+                        ckpt_every, ckpt_base, ckpt_states, stream);
+}
+
+kda_status kda_prefill_head_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
+                                  int32_t total_tokens, int32_t num_heads, const void *q,
+                                  const void *k, const void *v, const float *log_alpha,
+                                  const float *beta, const float *S0, const int32_t *cu_seqlens,
+                                  float scale, void *o, float *S_final, void *workspace,
+                                  size_t workspace_bytes, int32_t ckpt_every,
+                                  const int32_t *ckpt_base, float *ckpt_states, void *stream) {
+    return prefill_impl(in_dtype, out_dtype, num_seqs, total_tokens, num_heads, q, k, v, log_alpha,
+                        true, beta, S0, cu_seqlens, scale, o, S_final, workspace, workspace_bytes,
+                        ckpt_every, ckpt_base, ckpt_states, stream);
+}
+
+}  // extern "C"
+
+namespace {
+kda_status decode_impl(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batch, int32_t num_heads,
+                       const void *q, const void *k, const void *v, const float *log_alpha,
+                       bool head_decay, const float *beta, float *S_inout, float scale, void *o,
+                       void *stream) {
     if (!ok_dtype(in_dtype) || !ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
     if (batch < 1 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
-    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(log_alpha) || !ok_ptr_elem(beta, 4) ||
+    const bool la_ok = head_decay ? ok_ptr_elem(log_alpha, 4) : ok_ptr(log_alpha);
+    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !la_ok || !ok_ptr_elem(beta, 4) ||
         !ok_ptr(S_inout) || !ok_ptr(o))
         return KDA_ERR_INVALID_ARGUMENT;
     if ((int64_t)batch * num_heads > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
@@ -142,9 +179,29 @@ kda_status kda_decode_step(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batc
     a.in_dtype = in_dtype; a.out_dtype = out_dtype;
     a.batch = batch; a.num_heads = num_heads;
     a.q = q; a.k = k; a.v = v; a.log_alpha = log_alpha; a.beta = beta;
+    a.head_decay = head_decay ? 1 : 0;
     a.S = S_inout; a.scale = scale; a.o = o;
     a.status = device_status();
     return from_cuda(launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" {
+
+kda_status kda_decode_step(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batch,
+                           int32_t num_heads, const void *q, const void *k, const void *v,
+                           const float *log_alpha, const float *beta, float *S_inout,
+                           float scale, void *o, void *stream) {
+    return decode_impl(in_dtype, out_dtype, batch, num_heads, q, k, v, log_alpha, false, beta,
+                       S_inout, scale, o, stream);
+}
+
+kda_status kda_decode_step_head_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batch,
+                                      int32_t num_heads, const void *q, const void *k,
+                                      const void *v, const float *log_alpha, const float *beta,
+                                      float *S_inout, float scale, void *o, void *stream) {
+    return decode_impl(in_dtype, out_dtype, batch, num_heads, q, k, v, log_alpha, true, beta,
+                       S_inout, scale, o, stream);
 }
 
 kda_status kda_frontend(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,

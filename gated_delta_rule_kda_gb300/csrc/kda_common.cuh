@@ -71,6 +71,7 @@ struct DecodeArgs {
     int32_t batch, num_heads;
     const void *q, *k, *v;
     const float *log_alpha, *beta;
+    int32_t head_decay;  // 1: log_alpha is [B][H], one decay per (request, head)
     float *S;
     float scale;
     void *o;
@@ -129,6 +130,7 @@ struct PrefillArgs {
     void *workspace;
     size_t workspace_bytes;
     Checkpoints ckpt;
+    int32_t head_decay;  // 1: log_alpha is [T][H], one decay per (token, head)
     DeviceStatus status;
 };
 

@@ -29,7 +29,7 @@ __device__ __forceinline__ void st_stream(float *p, float4 x) {
     __stcs(reinterpret_cast<float4 *>(p), x);
 }
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, bool kHeadDecay>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
               const float *__restrict__ log_alpha, const float *__restrict__ beta,
@@ -55,7 +55,8 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
     } else {
         const int c = tid - kD;
         s_v[c] = Elem<Tin>::load(v + unit * kD + c);
-        s_a[c] = expf(log_alpha[unit * kD + c]);
+        // kHeadDecay: one decay per (request, head), log_alpha [B][H]
+        s_a[c] = expf(kHeadDecay ? log_alpha[unit] : log_alpha[unit * kD + c]);
     }
     __syncthreads();
 
@@ -112,7 +113,8 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
 template <typename Tin, typename Tout>
 cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
     const size_t units = (size_t)a.batch * a.num_heads;
-    decode_kernel<Tin, Tout><<<(unsigned)units, kThreads, 0, stream>>>(
+    auto kernel = a.head_decay ? decode_kernel<Tin, Tout, true> : decode_kernel<Tin, Tout, false>;
+    kernel<<<(unsigned)units, kThreads, 0, stream>>>(
         static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k),
         static_cast<const Tin *>(a.v), a.log_alpha, a.beta, a.S, a.scale,
         static_cast<Tout *>(a.o));

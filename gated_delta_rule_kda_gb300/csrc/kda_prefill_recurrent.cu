@@ -30,7 +30,7 @@ constexpr int kPadRow = kD + 16; // padded vector: 4 floats after every 32 rows
 
 __device__ __forceinline__ int prow(int row) { return row + 4 * (row >> 5); }
 
-template <typename Tin, typename Tout, bool kCkpt>
+template <typename Tin, typename Tout, bool kCkpt, bool kHeadDecay>
 __global__ void __launch_bounds__(kThreads)
 prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                          const Tin *__restrict__ v, const float *__restrict__ log_alpha,
@@ -80,7 +80,10 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 const size_t off = ((size_t)t * H + h) * kD + 4 * quad;
                 if (arr == 0) x = load4(q + off);
                 else if (arr == 1) x = load4(k + off);
-                else x = load4(log_alpha + off);
+                else if constexpr (kHeadDecay) {  // one decay per (token, head): [T][H]
+                    const float y = log_alpha[(size_t)t * H + h];
+                    x = make_float4(y, y, y, y);
+                } else x = load4(log_alpha + off);
             }
             pre[m] = x;
         }
@@ -180,9 +183,13 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 template <typename Tin, typename Tout>
 cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
     dim3 grid(kSplit, a.num_heads, a.num_seqs);
-    // snapshots are a separate instantiation, so the loop without them is untouched
-    auto kernel = a.ckpt.every > 0 ? prefill_recurrent_kernel<Tin, Tout, true>
-                                   : prefill_recurrent_kernel<Tin, Tout, false>;
+    // snapshots and the per-head decay are separate instantiations, so the loop without
+    // them is untouched
+    auto kernel = a.head_decay
+                      ? (a.ckpt.every > 0 ? prefill_recurrent_kernel<Tin, Tout, true, true>
+                                          : prefill_recurrent_kernel<Tin, Tout, false, true>)
+                      : (a.ckpt.every > 0 ? prefill_recurrent_kernel<Tin, Tout, true, false>
+                                          : prefill_recurrent_kernel<Tin, Tout, false, false>);
     kernel<<<grid, kThreads, 0, stream>>>(
         static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k),
         static_cast<const Tin *>(a.v), a.log_alpha, a.beta, a.S0, a.cu_seqlens, a.num_heads,

@@ -288,16 +288,28 @@ __device__ __forceinline__ void issue_loads(const Params &p, unsigned char *sm, 
 }
 
 // log_alpha of chunk [t0, t0 + 32): rows 4 rg .. 4 rg + 3, channels 4 q4 .. 4 q4 + 3
-// (rows past nrow zero).
+// (rows past nrow zero).  kHeadDecay: log_alpha is [T][H], one decay per (token, head)
+// shared by all channels (the Gated DeltaNet case), broadcast here.
+template <bool kHeadDecay>
 __device__ __forceinline__ void load_log_alpha(const Params &p, int t0, int nrow, int h, int q4,
                                                int rg, float4 (&la)[4]) {
-    const float *src = p.log_alpha + ((size_t)t0 * p.H + h) * kD + 4 * q4;
-    const size_t stride = (size_t)p.H * kD;
+    if constexpr (kHeadDecay) {
+        const float *src = p.log_alpha + (size_t)t0 * p.H + h;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int r = 4 * rg + k;
-        la[k] = r < nrow ? __ldg(reinterpret_cast<const float4 *>(src + r * stride))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < 4; ++k) {
+            const int r = 4 * rg + k;
+            const float x = r < nrow ? __ldg(src + (size_t)r * p.H) : 0.f;
+            la[k] = make_float4(x, x, x, x);
+        }
+    } else {
+        const float *src = p.log_alpha + ((size_t)t0 * p.H + h) * kD + 4 * q4;
+        const size_t stride = (size_t)p.H * kD;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int r = 4 * rg + k;
+            la[k] = r < nrow ? __ldg(reinterpret_cast<const float4 *>(src + r * stride))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
 }
 
@@ -320,7 +332,7 @@ __device__ __forceinline__ void load_gate_inputs(const Params &p, int t0, int nr
 // ============================================================================
 // Prep group (warps 4-11, 256 threads): operands of every chunk, in order.
 // ============================================================================
-template <bool kLayer>
+template <bool kLayer, bool kHeadDecay>
 __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, uint32_t tb,
                                            int h, int t_begin, int t_end, int nchunks) {
     const int tid = threadIdx.x, pt = tid - 128, lane = tid & 31;
@@ -354,7 +366,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         issue_loads<kLayer>(p, sm, bar, 0, t_begin, n0, h, tid, false);
         issued = 1;
         if constexpr (kLayer) load_gate_inputs(p, t_begin, n0, h, q4, rg, pt, zr, bl);
-        else load_log_alpha(p, t_begin, n0, h, q4, rg, la);
+        else load_log_alpha<kHeadDecay>(p, t_begin, n0, h, q4, rg, la);
     }
 
     for (int c = 0; c < nchunks; ++c) {
@@ -606,7 +618,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         }
         if (c + 1 < nchunks) {
             if constexpr (kLayer) load_gate_inputs(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, pt, zr, bl);
-            else load_log_alpha(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, la);
+            else load_log_alpha<kHeadDecay>(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, la);
         }
         publish(kPrepBar);
         if (c + 1 < nchunks) {  // stage chunk c+1 into slot s^1 once chunk c-1 no longer needs it
@@ -1216,7 +1228,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
     }
 }
 
-template <typename Tout, bool kLayer, bool kCkpt>
+template <typename Tout, bool kLayer, bool kCkpt, bool kHeadDecay>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -1259,7 +1271,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int nchunks = t_end > t_begin ? (t_end - t_begin + kC - 1) / kC : 0;
 
     if (warp >= 4)
-        prep_group<kLayer>(p, sm, tb, h, t_begin, t_end, nchunks);
+        prep_group<kLayer, kHeadDecay>(p, sm, tb, h, t_begin, t_end, nchunks);
     else
         chain_group<Tout, kLayer, kCkpt>(p, sm, tb, h, n, t_begin, t_end, nchunks);
 
@@ -1300,22 +1312,23 @@ bool encode_bf16_tiles(CUtensorMap *m, const void *base, int T, int H, int box_r
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <typename Tout, bool kLayer, bool kCkpt>
+template <typename Tout, bool kLayer, bool kCkpt, bool kHeadDecay>
 cudaError_t launch_kernel(const Params &p, int num_seqs, int num_heads, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<Tout, kLayer, kCkpt>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<Tout, kLayer, kCkpt, kHeadDecay>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM_DYN);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)num_seqs * (unsigned)num_heads;
-    prefill_tc_kernel<Tout, kLayer, kCkpt><<<grid, kThreads, SM_DYN, stream>>>(p);
+    prefill_tc_kernel<Tout, kLayer, kCkpt, kHeadDecay><<<grid, kThreads, SM_DYN, stream>>>(p);
     return cudaGetLastError();
 }
 
-// Snapshots are a separate instantiation: the kernel without them is compiled as if the
-// snapshot code did not exist.
-template <typename Tout, bool kLayer>
+// Snapshots and the per-head decay are separate instantiations: the kernel without them is
+// compiled as if their code did not exist.
+template <typename Tout, bool kLayer, bool kHeadDecay>
 cudaError_t launch_params(const Params &p, int num_seqs, int num_heads, cudaStream_t stream) {
-    if (p.ckpt.every > 0) return launch_kernel<Tout, kLayer, true>(p, num_seqs, num_heads, stream);
-    return launch_kernel<Tout, kLayer, false>(p, num_seqs, num_heads, stream);
+    if (p.ckpt.every > 0)
+        return launch_kernel<Tout, kLayer, true, kHeadDecay>(p, num_seqs, num_heads, stream);
+    return launch_kernel<Tout, kLayer, false, kHeadDecay>(p, num_seqs, num_heads, stream);
 }
 
 template <typename Tout>
@@ -1338,7 +1351,8 @@ cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
     p.S_final = a.S_final;
     p.ckpt = a.ckpt;
     p.status = a.status;
-    return launch_params<Tout, false>(p, a.num_seqs, a.num_heads, stream);
+    if (a.head_decay) return launch_params<Tout, false, true>(p, a.num_seqs, a.num_heads, stream);
+    return launch_params<Tout, false, false>(p, a.num_seqs, a.num_heads, stream);
 }
 
 template <typename Tout>
@@ -1370,7 +1384,7 @@ cudaError_t launch_layer_typed(const LayerArgs &a, cudaStream_t stream) {
     p.b = a.b;
     p.l2_eps = a.l2_eps;
     p.rms_eps = a.rms_eps;
-    return launch_params<Tout, true>(p, a.num_seqs, a.num_heads, stream);
+    return launch_params<Tout, true, false>(p, a.num_seqs, a.num_heads, stream);
 }
 
 }  // namespace

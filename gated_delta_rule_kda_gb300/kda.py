@@ -40,7 +40,9 @@ EXPORTED = (
     "kda_prefill_workspace_size",
     "kda_prefill",
     "kda_prefill_with_checkpoints",
+    "kda_prefill_head_decay",
     "kda_decode_step",
+    "kda_decode_step_head_decay",
     "kda_frontend",
     "kda_output_gate",
     "kda_layer_core_workspace_size",
@@ -82,9 +84,13 @@ def _load() -> ctypes.CDLL:
     lib.kda_prefill_with_checkpoints.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, I32, P, P,
                                                  P, P, P, P, P, F, P, P, P, SZ, I32, P, P, P]
     lib.kda_prefill_with_checkpoints.restype = ctypes.c_int
+    lib.kda_prefill_head_decay.argtypes = lib.kda_prefill_with_checkpoints.argtypes
+    lib.kda_prefill_head_decay.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, P, P, P, P, P, P, F,
                                     P, P]
     lib.kda_decode_step.restype = ctypes.c_int
+    lib.kda_decode_step_head_decay.argtypes = lib.kda_decode_step.argtypes
+    lib.kda_decode_step_head_decay.restype = ctypes.c_int
     lib.kda_frontend.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, F, ctypes.c_int,
                                  P, P, P, P, P, P]
     lib.kda_frontend.restype = ctypes.c_int
@@ -211,7 +217,7 @@ def _checkpoint_args(cu_seqlens, H, every, ckpt_base, ckpt_states, device):
 def kda_prefill_with_checkpoints(q, k, v, log_alpha, beta, cu_seqlens, every, S0=None,
                                  scale=DEFAULT_SCALE, *, ckpt_base=None, ckpt_states=None,
                                  out_dtype=None, o=None, S_final=None, want_state=True,
-                                 workspace=None, stream=None):
+                                 workspace=None, stream=None, _entry="kda_prefill_with_checkpoints"):
     """kda_prefill that also writes the state after every `every` tokens of each sequence
     (every: a positive multiple of 32).  ckpt_base [N+1] int32 (device) defaults to
     checkpoint_offsets(cu_seqlens, every).  Returns (o, S_final, ckpt_base, ckpt_states)."""
@@ -222,32 +228,52 @@ def kda_prefill_with_checkpoints(q, k, v, log_alpha, beta, cu_seqlens, every, S0
         o = torch.empty((T, H, HEAD_DIM), dtype=out_dtype, device=q.device)
     if S_final is None and want_state:
         S_final = torch.empty((N, H, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=q.device)
-    ckpt_base, ckpt_states = _checkpoint_args(cu_seqlens, H, every, ckpt_base, ckpt_states,
-                                              q.device)
+    if every:
+        ckpt_base, ckpt_states = _checkpoint_args(cu_seqlens, H, every, ckpt_base, ckpt_states,
+                                                  q.device)
     need = kda_prefill_workspace_size(N, T, H, q.dtype)
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = _lib.kda_prefill_with_checkpoints(
+    rc = getattr(_lib, _entry)(
         _dt(q), _dtype_code(o.dtype), N, T, H, _p(q), _p(k), _p(v), _p(log_alpha), _p(beta),
         _p(S0), _p(cu_seqlens), float(scale), _p(o), _p(S_final), _p(workspace), wbytes,
         int(every), _p(ckpt_base), _p(ckpt_states), _stream(stream))
-    _check("kda_prefill_with_checkpoints", rc)
+    _check(_entry, rc)
     return o, S_final, ckpt_base, ckpt_states
 
 
+def kda_prefill_head_decay(q, k, v, log_alpha, beta, cu_seqlens, S0=None, scale=DEFAULT_SCALE, *,
+                           every=0, ckpt_base=None, ckpt_states=None, out_dtype=None, o=None,
+                           S_final=None, want_state=True, workspace=None, stream=None):
+    """The Gated DeltaNet case: log_alpha [T, H] fp32, one decay per (token, head).
+    Returns (o, S_final, ckpt_base, ckpt_states) (the last two None without snapshots)."""
+    return kda_prefill_with_checkpoints(q, k, v, log_alpha, beta, cu_seqlens, every, S0, scale,
+                                        ckpt_base=ckpt_base, ckpt_states=ckpt_states,
+                                        out_dtype=out_dtype, o=o, S_final=S_final,
+                                        want_state=want_state, workspace=workspace, stream=stream,
+                                        _entry="kda_prefill_head_decay")
+
+
 def kda_decode_step(q, k, v, log_alpha, beta, S_inout, scale=DEFAULT_SCALE, *, out_dtype=None,
-                    o=None, stream=None):
+                    o=None, stream=None, _entry="kda_decode_step"):
     """One decode step; S_inout [B, H, 128, 128] fp32 is updated in place.  Returns o."""
     B, H, _ = q.shape
     out_dtype = out_dtype or q.dtype
     if o is None:
         o = torch.empty((B, H, HEAD_DIM), dtype=out_dtype, device=q.device)
-    rc = _lib.kda_decode_step(_dt(q), _dtype_code(o.dtype), B, H, _p(q), _p(k), _p(v),
-                              _p(log_alpha), _p(beta), _p(S_inout), float(scale), _p(o),
-                              _stream(stream))
-    _check("kda_decode_step", rc)
+    rc = getattr(_lib, _entry)(_dt(q), _dtype_code(o.dtype), B, H, _p(q), _p(k), _p(v),
+                               _p(log_alpha), _p(beta), _p(S_inout), float(scale), _p(o),
+                               _stream(stream))
+    _check(_entry, rc)
     return o
+
+
+def kda_decode_step_head_decay(q, k, v, log_alpha, beta, S_inout, scale=DEFAULT_SCALE, *,
+                               out_dtype=None, o=None, stream=None):
+    """kda_decode_step with log_alpha [B, H] fp32 (one decay per request and head)."""
+    return kda_decode_step(q, k, v, log_alpha, beta, S_inout, scale, out_dtype=out_dtype, o=o,
+                           stream=stream, _entry="kda_decode_step_head_decay")
 
 
 def kda_frontend(qp, kp, vp, conv_w, z, A, b, beta_logit, cu_seqlens, l2_eps=1e-6, *,

@@ -80,16 +80,18 @@ def cu_from_lengths(lengths: Sequence[int], device="cpu") -> torch.Tensor:
 
 def prefill_inputs(lengths: Sequence[int], H: int, dtype=torch.bfloat16, seed: int = BASE_SEED,
                    x_mean: float = 0.0, x_std: float = 2.0, s0_std: Optional[float] = None,
-                   device="cpu") -> PrefillInputs:
+                   device="cpu", head_decay: bool = False) -> PrefillInputs:
     """q,k ~ N(0,1) unit-normalised per head, v ~ N(0,1), log_alpha = -5 sigmoid(x),
-    beta = sigmoid(N(0,1)); all rounded to ``dtype`` (log_alpha, beta stay fp32)."""
+    beta = sigmoid(N(0,1)); all rounded to ``dtype`` (log_alpha, beta stay fp32).
+    head_decay: one log_alpha per (token, head), shape [T, H] (the Gated DeltaNet case)."""
     g = _gen(seed, device)
     T = int(sum(lengths))
     N = len(lengths)
     q = _unit_rows(_randn((T, H, D), g, device)).to(dtype)
     k = _unit_rows(_randn((T, H, D), g, device)).to(dtype)
     v = _randn((T, H, D), g, device).to(dtype)
-    la = torch.sigmoid(_randn((T, H, D), g, device, x_mean, x_std)).mul_(-5.0)
+    la_shape = (T, H) if head_decay else (T, H, D)
+    la = torch.sigmoid(_randn(la_shape, g, device, x_mean, x_std)).mul_(-5.0)
     beta = torch.sigmoid(_randn((T, H), g, device))
     S0 = None
     if s0_std is not None:
@@ -110,12 +112,13 @@ class DecodeInputs:
 
 def decode_inputs(B: int, H: int, dtype=torch.bfloat16, seed: int = BASE_SEED + 3,
                   x_mean: float = 0.0, x_std: float = 2.0, s_std: float = 0.1,
-                  device="cpu") -> DecodeInputs:
+                  device="cpu", head_decay: bool = False) -> DecodeInputs:
     g = _gen(seed, device)
     q = _unit_rows(_randn((B, H, D), g, device)).to(dtype)
     k = _unit_rows(_randn((B, H, D), g, device)).to(dtype)
     v = _randn((B, H, D), g, device).to(dtype)
-    la = torch.sigmoid(_randn((B, H, D), g, device, x_mean, x_std)).mul_(-5.0)
+    la_shape = (B, H) if head_decay else (B, H, D)
+    la = torch.sigmoid(_randn(la_shape, g, device, x_mean, x_std)).mul_(-5.0)
     beta = torch.sigmoid(_randn((B, H), g, device))
     S = _randn((B, H, D, D), g, device, 0.0, s_std)
     return DecodeInputs(q, k, v, la, beta, S)

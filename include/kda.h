@@ -152,6 +152,26 @@ kda_status kda_prefill_with_checkpoints(kda_dtype in_dtype, kda_dtype out_dtype,
                                         float *ckpt_states, void *stream);
 
 /*
+ * kda_prefill_head_decay - kda_prefill_with_checkpoints for the Gated DeltaNet
+ * case: one decay per (token, head) shared by all 128 key channels, i.e.
+ * Diag(alpha_t) = alpha_t I ("Kimi K3's Architecture: Kimi Delta Attention,
+ * Attention Residuals, and 896 Experts", section "Channel-wise decay, and the
+ * floor K3 puts under it": Gated DeltaNet keeps one decay value per head, KDA
+ * one per key channel).  The same kernels run it; only the decay is read as a
+ * scalar and broadcast.
+ *
+ *   log_alpha    [T][H] fp32 (4-byte aligned), each in [-5, 0] as for kda_prefill
+ *   (all other arguments, checkpoints included, as kda_prefill_with_checkpoints)
+ */
+kda_status kda_prefill_head_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
+                                  int32_t total_tokens, int32_t num_heads, const void *q,
+                                  const void *k, const void *v, const float *log_alpha,
+                                  const float *beta, const float *S0, const int32_t *cu_seqlens,
+                                  float scale, void *o, float *S_final, void *workspace,
+                                  size_t workspace_bytes, int32_t ckpt_every,
+                                  const int32_t *ckpt_base, float *ckpt_states, void *stream);
+
+/*
  * kda_decode_step - one token per request, state updated in place.
  *
  * One step of the recurrence for each (request b, head h): "each step reads
@@ -170,6 +190,16 @@ kda_status kda_decode_step(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batc
                            int32_t num_heads, const void *q, const void *k, const void *v,
                            const float *log_alpha, const float *beta, float *S_inout,
                            float scale, void *o, void *stream);
+
+/*
+ * kda_decode_step_head_decay - kda_decode_step with one decay per (request,
+ * head): log_alpha is [B][H] fp32 (4-byte aligned), broadcast over the 128 key
+ * channels (the Gated DeltaNet case, as kda_prefill_head_decay).
+ */
+kda_status kda_decode_step_head_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32_t batch,
+                                      int32_t num_heads, const void *q, const void *k,
+                                      const void *v, const float *log_alpha, const float *beta,
+                                      float *S_inout, float scale, void *o, void *stream);
 
 /*
  * kda_frontend - inputs of the recurrence from the pre-convolution

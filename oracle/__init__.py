@@ -254,3 +254,15 @@ def kda_decode_tokens(q, k, v, log_alpha, beta, cu_tokens, slot, S_pool, write_b
     if write_back:
         S_new[slot] = S_final
     return o, S_new, S_final
+
+
+def kda_prefill_head_decay(q, k, v, log_alpha, beta, cu_seqlens, S0=None, scale=None,
+                           n_threads=None):
+    """The Gated DeltaNet case (fp64): one log-decay per (token, head), log_alpha [T, H],
+    shared by every key channel ("Kimi K3's Architecture: Kimi Delta Attention, Attention
+    Residuals, and 896 Experts", section "Channel-wise decay, and the floor K3 puts under
+    it").  The per-channel recurrence with the decay repeated over the channels."""
+    la = _f64(log_alpha)
+    dk = _f64(q).shape[2]
+    return kda_prefill(q, k, v, np.repeat(la[:, :, None], dk, axis=2), beta, cu_seqlens, S0,
+                       scale, n_threads)

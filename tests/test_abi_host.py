@@ -235,3 +235,24 @@ def test_decode_tokens_rejects_bad_arguments(kda, bad):
 def test_decode_tokens_too_large_unsupported(kda):
     assert _decode_tokens(kda.library(), B=1 << 20, H=1 << 12, Sf=None) == 2
     assert _decode_tokens(kda.library(), T=1 << 30, H=4) == 2
+
+
+def test_head_decay_entries_validate(kda):
+    lib = kda.library()
+    # log_alpha needs only 4-byte alignment here: a 4-byte-aligned pointer passes that check
+    # and the call fails on the next one (o missing), never reaching a launch
+    rc = lib.kda_prefill_head_decay(0, 0, 1, 4, 2, FAKE, FAKE, FAKE, FAKE + 4, FAKE, None, FAKE,
+                                    0.1, None, None, None, 0, 0, None, None, None)
+    assert rc == 1
+    rc = lib.kda_prefill_head_decay(0, 0, 1, 4, 2, FAKE, FAKE, FAKE, FAKE + 2, FAKE, None, FAKE,
+                                    0.1, FAKE, None, None, 0, 0, None, None, None)
+    assert rc == 1  # log_alpha misaligned
+    rc = lib.kda_prefill_head_decay(0, 0, 1, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                    0.1, FAKE, None, None, 0, 16, FAKE, FAKE, None)
+    assert rc == 1  # checkpoint interval not a multiple of 32
+    rc = lib.kda_decode_step_head_decay(0, 0, 2, 2, FAKE, FAKE, FAKE, FAKE + 2, FAKE, FAKE, 0.1,
+                                        FAKE, None)
+    assert rc == 1
+    rc = lib.kda_decode_step_head_decay(0, 0, 0, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1,
+                                        FAKE, None)
+    assert rc == 1

@@ -531,3 +531,26 @@ def test_decode_tokens_rejects_bad_slots():
     with pytest.raises(ValueError):
         oracle.kda_decode_tokens(z, z, z, z, zb, [0, 1, 2], [1, 1], S, True)
     oracle.kda_decode_tokens(z, z, z, z, zb, [0, 1, 2], [1, 1], S, False)  # shared row: verify only
+
+
+# P17 the Gated DeltaNet case [Arch-K3, "Channel-wise decay, and the floor K3 puts under
+#     it": one decay per head]: with Diag(alpha) = alpha I the recurrence is the scalar-gated
+#     delta rule S_t = alpha_t (I - beta_t k k^T) S_{t-1} + beta_t k v^T, written here with
+#     plain matrix products, and o_t = scale S_t^T q_t.
+def test_head_decay_is_the_scalar_gated_delta_rule():
+    T, H, d = 9, 2, 6
+    rng = np.random.default_rng(900)
+    q = unit(rng.standard_normal((T, H, d)))
+    k = unit(rng.standard_normal((T, H, d)))
+    v = rng.standard_normal((T, H, d))
+    la = -5.0 / (1.0 + np.exp(-rng.standard_normal((T, H)) * 2))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))
+    S0 = rng.standard_normal((1, H, d, d)) * 0.3
+    o, Sf = oracle.kda_prefill_head_decay(q, k, v, la, beta, [0, T], S0=S0, scale=0.5)
+    for h in range(H):
+        S = S0[0, h].copy()
+        for t in range(T):
+            kk = k[t, h][:, None]
+            S = np.exp(la[t, h]) * (np.eye(d) - beta[t, h] * kk @ kk.T) @ S + beta[t, h] * kk @ v[t, h][None, :]
+            np.testing.assert_allclose(o[t, h], 0.5 * S.T @ q[t, h], atol=1e-12)
+        np.testing.assert_allclose(Sf[0, h], S, atol=1e-12)
