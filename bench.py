@@ -64,8 +64,8 @@ TRAFFIC = {
                 "ea5cf3c551115ce9336f4d54ee528bc3935b50e9eaa2eefbb5a62dd4c3468568",
                 (252.724992e6 + 37.786880e6) / (2048 * 96)),
     "decode": ("gated_delta_rule_kda_gb300/csrc/kda_decode.cu",
-               "1bf0e4585307540aec99de0bebe444ea914f399db22eb7540d6128919bfb40b0",
-               (205.3e6 + 142.4e6) / (32 * 96)),
+               "9f1e6145572ad4787343166be5659867b8c38d020db25a2e19651c2bcc6a5657",
+               (205.287936e6 + 142.316800e6) / (32 * 96)),
 }
 
 

@@ -117,6 +117,15 @@ kda_status prefill_impl(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seq
     if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
         return KDA_ERR_WORKSPACE;
 
+#ifdef KDA_DEBUG
+    // debug builds: the contents checks run before every prefill
+    {
+        CheckArgs c{num_seqs, total_tokens, num_heads, head_decay ? 1 : 0,
+                    total_tokens > 0 ? log_alpha : nullptr, cu_seqlens, device_status()};
+        if (launch_check_prefill(c, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+#endif
     PrefillArgs a;
     a.in_dtype = in_dtype; a.out_dtype = out_dtype;
     a.num_seqs = num_seqs; a.total_tokens = total_tokens; a.num_heads = num_heads;
@@ -416,6 +425,19 @@ kda_status kda_decode_tokens(kda_dtype in_dtype, kda_dtype out_dtype, int32_t ba
     a.scale = scale; a.o = o;
     a.status = device_status();
     return from_cuda(launch_decode_tokens(a, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_check_prefill_inputs(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                    const float *log_alpha, int32_t head_decay,
+                                    const int32_t *cu_seqlens, void *stream) {
+    if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (head_decay != 0 && head_decay != 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_ptr_elem(cu_seqlens, 4)) return KDA_ERR_INVALID_ARGUMENT;
+    if (log_alpha != nullptr && !(head_decay ? ok_ptr_elem(log_alpha, 4) : ok_ptr(log_alpha)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    CheckArgs a{num_seqs, total_tokens, num_heads, head_decay, log_alpha, cu_seqlens,
+                device_status()};
+    return from_cuda(launch_check_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
 kda_status kda_get_device_status(void *stream, uint32_t *detail) {

@@ -168,6 +168,15 @@ struct LayerArgs {
     DeviceStatus status;
 };
 
+// Contents checks of prefill inputs (offsets monotonic, log alpha in [-5, 0]).
+struct CheckArgs {
+    int32_t num_seqs, total_tokens, num_heads, head_decay;
+    const float *log_alpha;  // [T][H][128] ([T][H] with head_decay) or null
+    const int32_t *cu_seqlens;
+    DeviceStatus status;
+};
+
+cudaError_t launch_check_prefill(const CheckArgs &a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_decode_layer(const DecodeLayerArgs &a, cudaStream_t stream);
 cudaError_t launch_decode_tokens(const DecodeTokensArgs &a, cudaStream_t stream);

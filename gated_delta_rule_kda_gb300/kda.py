@@ -52,6 +52,7 @@ EXPORTED = (
     "kda_layer_core_fused_with_checkpoints",
     "kda_decode_layer",
     "kda_decode_tokens",
+    "kda_check_prefill_inputs",
     "kda_get_device_status",
 )
 
@@ -117,6 +118,8 @@ def _load() -> ctypes.CDLL:
     lib.kda_decode_tokens.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, I32, I32, P, P, P, P,
                                       P, P, P, P, I32, P, F, P, P]
     lib.kda_decode_tokens.restype = ctypes.c_int
+    lib.kda_check_prefill_inputs.argtypes = [I32, I32, I32, P, I32, P, P]
+    lib.kda_check_prefill_inputs.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.kda_get_device_status.restype = ctypes.c_int
     return lib
@@ -430,6 +433,22 @@ def kda_decode_tokens(q, k, v, log_alpha, beta, cu_tokens, slot, S_pool, write_b
                                 _p(o), _stream(stream))
     _check("kda_decode_tokens", rc)
     return o
+
+
+def kda_check_prefill_inputs(cu_seqlens, log_alpha=None, total_tokens=None, num_heads=1,
+                             stream=None):
+    """Queue the contents checks of prefill inputs (offsets, decay range); read the result
+    with kda_get_device_status.  log_alpha [T, H, 128] or [T, H] (per-head decay), or None
+    to check the offsets alone against total_tokens."""
+    N = cu_seqlens.shape[0] - 1
+    if log_alpha is None:
+        T, H, head = int(total_tokens), int(num_heads), 0
+    else:
+        T, H = log_alpha.shape[:2]
+        head = 1 if log_alpha.dim() == 2 else 0
+    rc = _lib.kda_check_prefill_inputs(N, T, H, _p(log_alpha), head, _p(cu_seqlens),
+                                       _stream(stream))
+    _check("kda_check_prefill_inputs", rc)
 
 
 def kda_get_device_status(stream=None):

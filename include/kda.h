@@ -451,6 +451,29 @@ kda_status kda_decode_tokens(kda_dtype in_dtype, kda_dtype out_dtype, int32_t ba
                              float scale, void *o, void *stream);
 
 /*
+ * kda_check_prefill_inputs - the contents checks the host cannot make before a
+ * prefill: cu_seqlens starts at 0, never decreases and ends at total_tokens;
+ * every log alpha lies in [-5, 0] and is not NaN (the floor g_min = -5 bounds the
+ * chunk's reciprocal decays: "Kimi K3's Architecture: Kimi Delta Attention,
+ * Attention Residuals, and 896 Experts", section "Channel-wise decay, and the
+ * floor K3 puts under it").  One read of log_alpha on `stream`; a failure is
+ * reported by kda_get_device_status as KDA_ERR_DEVICE_CHECK with detail =
+ * (kind << 28) | index, kind 1 = cu_seqlens (index = n), kind 2 = log alpha
+ * (index = the token of a failing value).  A library built with KDA_DEBUG
+ * defined runs these checks inside every kda_prefill* call.
+ *
+ *   log_alpha    [T][H][128] fp32 (16-byte aligned), or [T][H] (4-byte aligned)
+ *                with head_decay = 1, or NULL to check cu_seqlens only
+ *   head_decay   0 or 1
+ *   cu_seqlens   [N+1] int32 (device)
+ * Errors: KDA_ERR_INVALID_ARGUMENT (sizes, flags, null or misaligned pointers),
+ * KDA_ERR_CUDA (launch failure).
+ */
+kda_status kda_check_prefill_inputs(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                    const float *log_alpha, int32_t head_decay,
+                                    const int32_t *cu_seqlens, void *stream);
+
+/*
  * kda_get_device_status - synchronises `stream`, then returns and clears the
  * device status word: KDA_OK, KDA_ERR_DEVICE_TIMEOUT or KDA_ERR_DEVICE_CHECK
  * (KDA_ERR_CUDA if the synchronisation itself fails).  If detail is not

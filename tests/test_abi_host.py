@@ -256,3 +256,13 @@ def test_head_decay_entries_validate(kda):
     rc = lib.kda_decode_step_head_decay(0, 0, 0, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1,
                                         FAKE, None)
     assert rc == 1
+
+
+def test_check_prefill_inputs_validates(kda):
+    lib = kda.library()
+    assert lib.kda_check_prefill_inputs(0, 4, 2, FAKE, 0, FAKE, None) == 1      # no sequences
+    assert lib.kda_check_prefill_inputs(1, -1, 2, FAKE, 0, FAKE, None) == 1     # negative T
+    assert lib.kda_check_prefill_inputs(1, 4, 2, FAKE, 2, FAKE, None) == 1      # bad flag
+    assert lib.kda_check_prefill_inputs(1, 4, 2, FAKE, 0, None, None) == 1      # no offsets
+    assert lib.kda_check_prefill_inputs(1, 4, 2, FAKE + 4, 0, FAKE, None) == 1  # misaligned
+    assert lib.kda_check_prefill_inputs(1, 4, 2, FAKE + 2, 1, FAKE, None) == 1  # misaligned
