@@ -102,6 +102,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.proc = None
         self.path = None
+        self.start_wait_s = None
         self.gpu = gpu_index
         if shutil.which("nvidia-smi") is None:
             return
@@ -112,6 +113,14 @@ class ClockSampler:
             ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
              "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f,
             stderr=subprocess.DEVNULL)
+        # nvidia-smi takes a while to start: wait (up to 5 s) for its first sample, so that
+        # the samples cover the timed region that follows
+        t0 = time.time()
+        while time.time() < t0 + 5.0 and os.path.getsize(self.path) == 0:
+            if self.proc.poll() is not None:
+                break
+            time.sleep(0.02)
+        self.start_wait_s = round(time.time() - t0, 3)
 
     def stop(self):
         if self.proc is None:
@@ -139,7 +148,8 @@ class ClockSampler:
                         reasons.add(nm)
         os.unlink(self.path)
         med = statistics.median(sm) if sm else None
-        return {"sm_mhz": med, "sm_max_mhz": smax, "samples": len(sm), "reasons": sorted(reasons)}
+        return {"sm_mhz": med, "sm_max_mhz": smax, "samples": len(sm), "reasons": sorted(reasons),
+                "sampler_start_s": self.start_wait_s}
 
 
 def dist_setup():
@@ -468,6 +478,35 @@ def run_ours(args, world, rank, local):
     del tinp, ot
     torch.cuda.empty_cache()
 
+    # the same draft through the whole layer core (convolution state included)
+    linp2 = synthetic.decode_layer_tokens_inputs([ntok] * 256, 96, 256, device=dev)
+    og2 = torch.empty((256 * ntok, 96, D), dtype=torch.bfloat16, device=dev)
+    spec_layer = {"workload": f"256 requests x {ntok} tokens x 96 heads from shuffled rows of "
+                              "256-row state and convolution pools; front end + recurrence + gate",
+                  "entry_point": "kda_decode_layer_tokens"}
+    for mode, wb in (("verify", False), ("replay", True)):
+        def layer_tokens_step():
+            kda.kda_decode_layer_tokens(linp2.qp, linp2.kp, linp2.vp, linp2.conv_w, linp2.z,
+                                        linp2.A, linp2.b, linp2.beta_logit, linp2.g,
+                                        linp2.cu_tokens, linp2.slot, linp2.S_pool,
+                                        linp2.conv_pool, wb, o=og2)
+
+        t_total, t_per = time_launches(layer_tokens_step, args.steps, args.warmup, world)
+        t_ms = max_over_ranks(t_total / args.steps, world)
+        t_launch = sum(t_per) / len(t_per)
+        per_unit = (2 if wb else 1) * (STATE_BYTES + 9 * D * 2) + ntok * LAYER_BYTES_PER_TOKEN_HEAD
+        t_bytes = 256 * 96 * per_unit + 96 * DECODE_LAYER_BYTES_PER_HEAD
+        t_ach = t_bytes / (t_launch / 1e3) / 1e9
+        spec_layer[mode] = {"tokens_per_s": aggregate_rate(256 * ntok, t_ms, world),
+                            "ms_per_step": t_ms, "write_back": wb,
+                            "roofline": {"bound": "hbm", "achieved": t_ach, "peak": hbm,
+                                         "unit": "GB/s", "frac": t_ach / hbm, "traffic": None,
+                                         "peak_kind": peak_kind,
+                                         "kernel": "kda_decode_layer_tokens"}}
+    spec["layer"] = spec_layer
+    del linp2, og2
+    torch.cuda.empty_cache()
+
     # ---------------- layer core (varlen, 16 sequences) ----------------
     layer = None
     if not args.skip_layer_core:
@@ -565,6 +604,15 @@ def run_only(args, local):
                                           linp1.A, linp1.b, linp1.beta_logit, linp1.g, linp1.slot,
                                           linp1.S_pool, linp1.conv_pool, o=odl)
         units = B
+    elif args.only == "decode_layer_tokens":
+        B = 32 if args.small else 256
+        linp2 = synthetic.decode_layer_tokens_inputs([4] * B, 96, B, device=dev)
+        og2 = torch.empty((4 * B, 96, D), dtype=torch.bfloat16, device=dev)
+        fn = lambda: kda.kda_decode_layer_tokens(linp2.qp, linp2.kp, linp2.vp, linp2.conv_w,
+                                                 linp2.z, linp2.A, linp2.b, linp2.beta_logit,
+                                                 linp2.g, linp2.cu_tokens, linp2.slot,
+                                                 linp2.S_pool, linp2.conv_pool, True, o=og2)
+        units = B
     elif args.only == "decode_tokens":
         B = 32 if args.small else 256
         tinp = synthetic.decode_tokens_inputs([4] * B, 96, B, device=dev)
@@ -587,14 +635,15 @@ def run_only(args, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-layer-core", action="store_true")
     ap.add_argument("--skip-staged-layer-core", action="store_true",
                     help="time only the fused layer core, not the three-launch composition")
-    ap.add_argument("--only", choices=["prefill", "decode", "decode_layer", "decode_tokens", "layer"],
+    ap.add_argument("--only", choices=["prefill", "decode", "decode_layer", "decode_tokens",
+                                       "decode_layer_tokens", "layer"],
                     default=None,
                     help="profiling aid: run just this kernel (no baseline, no e2e)")
     ap.add_argument("--small", action="store_true",

@@ -427,6 +427,49 @@ kda_status kda_decode_tokens(kda_dtype in_dtype, kda_dtype out_dtype, int32_t ba
     return from_cuda(launch_decode_tokens(a, static_cast<cudaStream_t>(stream)));
 }
 
+kda_status kda_decode_layer_tokens(int32_t batch, int32_t num_heads, int32_t pool_size,
+                                   int32_t total_tokens, const int32_t *cu_tokens,
+                                   const int32_t *slot, const void *qp, const void *kp,
+                                   const void *vp, const float *conv_w, const void *z,
+                                   const float *A, const float *b, const void *beta_logit,
+                                   const void *g, float *S_pool, void *conv_pool,
+                                   int32_t write_back, float scale, float l2_eps, float rms_eps,
+                                   kda_dtype out_dtype, void *o, void *stream) {
+    if (!ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
+    if (batch < 1 || num_heads < 1 || pool_size < 1 || total_tokens < 0)
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (write_back != 0 && write_back != 1) return KDA_ERR_INVALID_ARGUMENT;
+    if (!ok_ptr_elem(cu_tokens, 4) || !ok_ptr_elem(slot, 4) || !ok_ptr(S_pool) ||
+        !ok_ptr(conv_pool) || !ok_ptr(conv_w) || !ok_ptr_elem(A, 4) || !ok_opt_ptr(b))
+        return KDA_ERR_INVALID_ARGUMENT;
+    if (total_tokens > 0 && (!ok_ptr(qp) || !ok_ptr(kp) || !ok_ptr(vp) || !ok_ptr(z) || !ok_ptr(g) ||
+                             !ok_ptr_elem(beta_logit, 2) || !ok_ptr(o)))
+        return KDA_ERR_INVALID_ARGUMENT;
+    const size_t state_bytes = (size_t)pool_size * num_heads * kD * kD * sizeof(float);
+    const size_t conv_bytes = (size_t)pool_size * 9 * num_heads * kD * sizeof(__nv_bfloat16);
+    const uintptr_t sp = reinterpret_cast<uintptr_t>(S_pool), cp = reinterpret_cast<uintptr_t>(conv_pool);
+    if (sp < cp + conv_bytes && cp < sp + state_bytes) return KDA_ERR_INVALID_ARGUMENT;  // pools overlap
+    if ((int64_t)batch * num_heads > 0x7fffffffLL || (int64_t)total_tokens * num_heads > 0x7fffffffLL)
+        return KDA_ERR_UNSUPPORTED;
+    DecodeLayerTokensArgs a;
+    a.batch = batch; a.num_heads = num_heads; a.pool_size = pool_size; a.total_tokens = total_tokens;
+    a.qp = static_cast<const __nv_bfloat16 *>(qp);
+    a.kp = static_cast<const __nv_bfloat16 *>(kp);
+    a.vp = static_cast<const __nv_bfloat16 *>(vp);
+    a.z = static_cast<const __nv_bfloat16 *>(z);
+    a.beta_logit = static_cast<const __nv_bfloat16 *>(beta_logit);
+    a.g = static_cast<const __nv_bfloat16 *>(g);
+    a.conv_w = conv_w; a.A = A; a.b = b;
+    a.cu_tokens = cu_tokens; a.slot = slot;
+    a.S_pool = S_pool;
+    a.conv_pool = static_cast<__nv_bfloat16 *>(conv_pool);
+    a.write_back = write_back;
+    a.scale = scale; a.l2_eps = l2_eps; a.rms_eps = rms_eps;
+    a.out_dtype = out_dtype; a.o = o;
+    a.status = device_status();
+    return from_cuda(launch_decode_layer_tokens(a, static_cast<cudaStream_t>(stream)));
+}
+
 kda_status kda_check_prefill_inputs(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
                                     const float *log_alpha, int32_t head_decay,
                                     const int32_t *cu_seqlens, void *stream) {

@@ -78,6 +78,23 @@ struct DecodeArgs {
     DeviceStatus status;
 };
 
+// The whole layer core for a few tokens per request from pooled recurrent and
+// short-convolution states (speculative verify / replay at the layer level).
+constexpr int kDecodeLayerMaxTokens = KDA_DECODE_LAYER_MAX_TOKENS;
+struct DecodeLayerTokensArgs {
+    int32_t batch, num_heads, pool_size, total_tokens;
+    const __nv_bfloat16 *qp, *kp, *vp, *z, *beta_logit, *g;  // [T][H][128] ([T][H] for beta_logit)
+    const float *conv_w, *A, *b;                            // [3][H*128][4], [H], [H][128] or null
+    const int32_t *cu_tokens, *slot;                        // [B+1], [B]
+    float *S_pool;                                          // [P][H][128][128]
+    __nv_bfloat16 *conv_pool;                               // [P][3][3][H][128]
+    int32_t write_back;
+    float scale, l2_eps, rms_eps;
+    kda_dtype out_dtype;
+    void *o;                                                // [T][H][128]
+    DeviceStatus status;
+};
+
 // Several tokens per request from a pooled state: request b's tokens are rows
 // [cu_tokens[b], cu_tokens[b+1]) of q, k, v, log_alpha, beta; its state is S_pool[slot[b]].
 struct DecodeTokensArgs {
@@ -180,6 +197,7 @@ cudaError_t launch_check_prefill(const CheckArgs &a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t stream);
 cudaError_t launch_decode_layer(const DecodeLayerArgs &a, cudaStream_t stream);
 cudaError_t launch_decode_tokens(const DecodeTokensArgs &a, cudaStream_t stream);
+cudaError_t launch_decode_layer_tokens(const DecodeLayerTokensArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_recurrent(const PrefillArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 cudaError_t launch_layer_tc(const LayerArgs &a, cudaStream_t stream);

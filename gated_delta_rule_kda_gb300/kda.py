@@ -52,6 +52,7 @@ EXPORTED = (
     "kda_layer_core_fused_with_checkpoints",
     "kda_decode_layer",
     "kda_decode_tokens",
+    "kda_decode_layer_tokens",
     "kda_check_prefill_inputs",
     "kda_get_device_status",
 )
@@ -118,6 +119,9 @@ def _load() -> ctypes.CDLL:
     lib.kda_decode_tokens.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, I32, I32, P, P, P, P,
                                       P, P, P, P, I32, P, F, P, P]
     lib.kda_decode_tokens.restype = ctypes.c_int
+    lib.kda_decode_layer_tokens.argtypes = [I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P,
+                                            P, P, I32, F, F, F, ctypes.c_int, P, P]
+    lib.kda_decode_layer_tokens.restype = ctypes.c_int
     lib.kda_check_prefill_inputs.argtypes = [I32, I32, I32, P, I32, P, P]
     lib.kda_check_prefill_inputs.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
@@ -432,6 +436,28 @@ def kda_decode_tokens(q, k, v, log_alpha, beta, cu_tokens, slot, S_pool, write_b
                                 _p(S_pool), int(bool(write_back)), _p(S_final), float(scale),
                                 _p(o), _stream(stream))
     _check("kda_decode_tokens", rc)
+    return o
+
+
+DECODE_LAYER_MAX_TOKENS = 16  # KDA_DECODE_LAYER_MAX_TOKENS in include/kda.h
+
+
+def kda_decode_layer_tokens(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_tokens, slot, S_pool,
+                            conv_pool, write_back, scale=DEFAULT_SCALE, l2_eps=1e-6, rms_eps=1e-6,
+                            *, out_dtype=torch.bfloat16, o=None, stream=None):
+    """The layer core for a few tokens per request from pooled states (verify:
+    write_back=False; replay: write_back=True).  Returns o_gated [T, H, 128]."""
+    T, H, _ = qp.shape
+    B = slot.shape[0]
+    P = S_pool.shape[0]
+    if o is None:
+        o = torch.empty((T, H, HEAD_DIM), dtype=out_dtype, device=qp.device)
+    rc = _lib.kda_decode_layer_tokens(B, H, P, T, _p(cu_tokens), _p(slot), _p(qp), _p(kp), _p(vp),
+                                      _p(conv_w), _p(z), _p(A), _p(b), _p(beta_logit), _p(g),
+                                      _p(S_pool), _p(conv_pool), int(bool(write_back)),
+                                      float(scale), float(l2_eps), float(rms_eps),
+                                      _dtype_code(o.dtype), _p(o), _stream(stream))
+    _check("kda_decode_layer_tokens", rc)
     return o
 
 

@@ -211,6 +211,49 @@ def decode_layer_inputs(B: int, H: int, P: int, seed: int = BASE_SEED + 6,
 
 
 @dataclass
+class DecodeLayerTokensInputs:
+    qp: torch.Tensor          # [T, H, 128] bf16, the requests' tokens packed
+    kp: torch.Tensor
+    vp: torch.Tensor
+    conv_w: torch.Tensor      # [3, H*128, 4] fp32
+    z: torch.Tensor           # [T, H, 128] bf16
+    A: torch.Tensor           # [H] fp32
+    b: torch.Tensor           # [H, 128] fp32 (zero)
+    beta_logit: torch.Tensor  # [T, H] bf16
+    g: torch.Tensor           # [T, H, 128] bf16
+    cu_tokens: torch.Tensor   # [B+1] int32
+    slot: torch.Tensor        # [B] int32, distinct shuffled rows of the pools
+    S_pool: torch.Tensor      # [P, H, 128, 128] fp32
+    conv_pool: torch.Tensor   # [P, 3, 3, H, 128] bf16
+
+
+def decode_layer_tokens_inputs(lengths: Sequence[int], H: int, P: int, seed: int = BASE_SEED + 8,
+                               s_std: float = 0.1, device="cpu") -> DecodeLayerTokensInputs:
+    """A few tokens per request through the layer core, with the layer-core workload's
+    distributions (as decode_layer_inputs), the requests in shuffled rows of P-row pools."""
+    B = len(lengths)
+    if P < B:
+        raise ValueError("the pools need at least one row per request")
+    g = _gen(seed, device)
+    T = int(sum(lengths))
+    bf = torch.bfloat16
+    qp = _randn((T, H, D), g, device).to(bf)
+    kp = _randn((T, H, D), g, device).to(bf)
+    vp = _randn((T, H, D), g, device).to(bf)
+    conv_w = _randn((3, H * D, 4), g, device, 0.0, 0.5)
+    z = _randn((T, H, D), g, device).to(bf)
+    A = _randn((H,), g, device, 0.0, 0.5)
+    b = torch.zeros((H, D), dtype=torch.float32, device=device)
+    beta_logit = _randn((T, H), g, device).to(bf)
+    gg = _randn((T, H, D), g, device).to(bf)
+    slot = torch.randperm(P, generator=g, device=device)[:B].to(torch.int32)
+    S_pool = _randn((P, H, D, D), g, device, 0.0, s_std)
+    conv_pool = _randn((P, 3, 3, H, D), g, device).to(bf)
+    return DecodeLayerTokensInputs(qp, kp, vp, conv_w, z, A, b, beta_logit, gg,
+                                   cu_from_lengths(lengths, device), slot, S_pool, conv_pool)
+
+
+@dataclass
 class DecodeTokensInputs:
     q: torch.Tensor           # [T, H, 128] dtype, the requests' tokens packed
     k: torch.Tensor

@@ -450,6 +450,47 @@ kda_status kda_decode_tokens(kda_dtype in_dtype, kda_dtype out_dtype, int32_t ba
                              const float *beta, float *S_pool, int32_t write_back, float *S_final,
                              float scale, void *o, void *stream);
 
+/* Most tokens one request may bring to kda_decode_layer_tokens in one call. */
+#define KDA_DECODE_LAYER_MAX_TOKENS 16
+
+/*
+ * kda_decode_layer_tokens - the whole layer core (short convolution, L2 norms,
+ * gates, recurrence, output gate) for a few tokens per request whose recurrent
+ * and short-convolution states live in pools: the layer-level verify and replay
+ * steps of speculative decoding ("Kimi K3 · KDA layer", KDA equation list;
+ * "Inside Kimi K3: How KDA, AttnRes, and 896 Experts Work", sections "KDA writes
+ * corrections into a recurrent matrix" and "What could go wrong").
+ *
+ * Request b's tokens are rows [cu_tokens[b], cu_tokens[b+1]) (at most
+ * KDA_DECODE_LAYER_MAX_TOKENS).  Its convolution window is the row's
+ * convolution state (the three earlier pre-convolution inputs) followed by its
+ * tokens' q^p, k^p, v^p; the recurrence runs from S_pool[slot[b]] over the
+ * tokens; o_gated is written for every token.  Exactly as kda_decode_layer
+ * applied to the tokens one after another, except that with write_back = 0
+ * (verify) neither pool changes (rows may then be shared by several requests),
+ * and with write_back = 1 (replay; distinct rows) both rows advance past the
+ * last token.  A request with no tokens changes nothing.
+ *
+ *   Pools, weights and per-token inputs as kda_decode_layer, with the per-token
+ *   inputs packed over all requests' tokens: qp, kp, vp, z, g [T][H][128] bf16,
+ *   beta_logit [T][H] bf16, o_gated [T][H][128] out_dtype; cu_tokens [B+1] and
+ *   slot [B] int32 (device).  Per-token pointers may be NULL when T = 0.
+ * Errors: KDA_ERR_INVALID_ARGUMENT (null/misaligned pointers, bad sizes, dtype or
+ * write_back, overlapping pools), KDA_ERR_UNSUPPORTED (B * H or T * H above
+ * 2^31 - 1), KDA_ERR_CUDA (launch failure).  A request whose slot lies outside
+ * [0, P), whose token range lies outside [0, T) or holds more than
+ * KDA_DECODE_LAYER_MAX_TOKENS tokens is refused by the kernel (nothing read or
+ * written for it; KDA_ERR_DEVICE_CHECK with detail = b).
+ */
+kda_status kda_decode_layer_tokens(int32_t batch, int32_t num_heads, int32_t pool_size,
+                                   int32_t total_tokens, const int32_t *cu_tokens,
+                                   const int32_t *slot, const void *qp, const void *kp,
+                                   const void *vp, const float *conv_w, const void *z,
+                                   const float *A, const float *b, const void *beta_logit,
+                                   const void *g, float *S_pool, void *conv_pool,
+                                   int32_t write_back, float scale, float l2_eps, float rms_eps,
+                                   kda_dtype out_dtype, void *o, void *stream);
+
 /*
  * kda_check_prefill_inputs - the contents checks the host cannot make before a
  * prefill: cu_seqlens starts at 0, never decreases and ends at total_tokens;

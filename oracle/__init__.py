@@ -266,3 +266,64 @@ def kda_prefill_head_decay(q, k, v, log_alpha, beta, cu_seqlens, S0=None, scale=
     dk = _f64(q).shape[2]
     return kda_prefill(q, k, v, np.repeat(la[:, :, None], dk, axis=2), beta, cu_seqlens, S0,
                        scale, n_threads)
+
+
+def kda_decode_layer_tokens(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_tokens, slot, S_pool,
+                            conv_pool, write_back, scale=None, l2_eps=1e-6, rms_eps=1e-6,
+                            n_threads=None, return_o_tilde=False):
+    """A few tokens per request through the whole layer core from pooled states (fp64):
+    the layer-level speculative verify (write_back false: both pools unchanged) and replay
+    (write_back true: each request's rows advance past its tokens).  Inputs not modified.
+
+    Request b's tokens are rows [cu_tokens[b], cu_tokens[b+1]) of qp, kp, vp, z, g
+    [T, H, d] and beta_logit [T, H]; its recurrent state is S_pool[slot[b]] and its
+    short-convolution state conv_pool[slot[b]] ([3 streams][3 taps (t-1, t-2, t-3)][H][d]).
+    The pinned sequence front end runs on the window (the three earlier inputs, then the
+    request's tokens) as one sequence, the recurrence from the row's state over the tokens,
+    then the output gate ("Kimi K3 · KDA layer", KDA equation list; "Inside Kimi K3: How
+    KDA, AttnRes, and 896 Experts Work", sections "KDA writes corrections into a recurrent
+    matrix" and "What could go wrong").
+    Returns (o_gated [T, H, d], S_pool_new, conv_pool_new), and o~ [T, H, d] (the
+    readout before the gate) as a fourth value with return_o_tilde.
+    """
+    qp, kp, vp, conv_w, z, A, b, bl, g = map(_f64, (qp, kp, vp, conv_w, z, A, b, beta_logit, g))
+    S_pool, conv_pool = _f64(S_pool), _f64(conv_pool)
+    slot = np.asarray(slot, dtype=np.int64)
+    cu = np.asarray(cu_tokens, dtype=np.int64)
+    B = slot.shape[0]
+    T, H, d = qp.shape
+    P = S_pool.shape[0]
+    if cu.shape != (B + 1,) or B == 0 or slot.min() < 0 or slot.max() >= P:
+        raise ValueError("kda_decode_layer_tokens: slots must lie in [0, P), one per request")
+    if write_back and len(set(slot.tolist())) != B:
+        raise ValueError("kda_decode_layer_tokens: write-back needs distinct slots")
+    o = np.zeros((T, H, d))
+    o_tilde = np.zeros((T, H, d))
+    S_new, conv_new = S_pool.copy(), conv_pool.copy()
+    for r in range(B):
+        n, t0, t1 = slot[r], cu[r], cu[r + 1]
+        m = t1 - t0
+        if m == 0:
+            continue
+        win = []
+        for s, xp in enumerate((qp, kp, vp)):
+            w = np.zeros((m + 3, H, d))
+            w[0], w[1], w[2] = conv_pool[n, s, 2], conv_pool[n, s, 1], conv_pool[n, s, 0]
+            w[3:] = xp[t0:t1]
+            win.append(w)
+        zw = np.zeros((m + 3, H, d)); zw[3:] = z[t0:t1]
+        blw = np.zeros((m + 3, H)); blw[3:] = bl[t0:t1]
+        qh, kh, vv, la, beta = kda_frontend(win[0], win[1], win[2], conv_w, zw, A, b, blw,
+                                            np.array([0, m + 3], np.int32), l2_eps, n_threads)
+        ot, Sf = kda_prefill(qh[3:], kh[3:], vv[3:], la[3:], beta[3:], np.array([0, m], np.int32),
+                             S0=S_pool[n:n + 1], scale=scale, n_threads=n_threads)
+        o[t0:t1] = kda_output_gate(ot, g[t0:t1], rms_eps, n_threads)
+        o_tilde[t0:t1] = ot
+        if write_back:
+            S_new[n] = Sf[0]
+            for s in range(3):
+                for tap in range(3):
+                    conv_new[n, s, tap] = win[s][m + 2 - tap]
+    if return_o_tilde:
+        return o, S_new, conv_new, o_tilde
+    return o, S_new, conv_new

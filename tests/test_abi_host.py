@@ -266,3 +266,27 @@ def test_check_prefill_inputs_validates(kda):
     assert lib.kda_check_prefill_inputs(1, 4, 2, FAKE, 0, None, None) == 1      # no offsets
     assert lib.kda_check_prefill_inputs(1, 4, 2, FAKE + 4, 0, FAKE, None) == 1  # misaligned
     assert lib.kda_check_prefill_inputs(1, 4, 2, FAKE + 2, 1, FAKE, None) == 1  # misaligned
+
+
+def _decode_layer_tokens(lib, **kw):
+    a = dict(B=2, H=2, P=4, T=6, cu=FAKE, slot=FAKE, qp=FAKE, kp=FAKE, vp=FAKE, w=FAKE, z=FAKE,
+             A=FAKE, b=None, bl=FAKE, g=FAKE, S=FAKE, conv=FAKE + (1 << 24), wb=1, out_dt=0, o=FAKE)
+    a.update(kw)
+    return lib.kda_decode_layer_tokens(a["B"], a["H"], a["P"], a["T"], a["cu"], a["slot"], a["qp"],
+                                       a["kp"], a["vp"], a["w"], a["z"], a["A"], a["b"], a["bl"],
+                                       a["g"], a["S"], a["conv"], a["wb"], 0.1, 1e-6, 1e-6,
+                                       a["out_dt"], a["o"], None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(B=0), dict(H=0), dict(P=0), dict(T=-1), dict(wb=3), dict(out_dt=4), dict(cu=None),
+    dict(slot=FAKE + 1), dict(qp=None), dict(kp=MIS), dict(vp=None), dict(w=MIS), dict(z=None),
+    dict(A=None), dict(b=MIS), dict(bl=FAKE + 1), dict(g=None), dict(S=None), dict(conv=MIS),
+    dict(o=None), dict(conv=FAKE + 1024),  # the convolution pool inside the state pool
+])
+def test_decode_layer_tokens_rejects_bad_arguments(kda, bad):
+    assert _decode_layer_tokens(kda.library(), **bad) == 1
+
+
+def test_decode_layer_tokens_too_large_unsupported(kda):
+    assert _decode_layer_tokens(kda.library(), B=1 << 20, H=1 << 12, conv=FAKE + (1 << 40)) == 2

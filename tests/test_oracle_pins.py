@@ -554,3 +554,39 @@ def test_head_decay_is_the_scalar_gated_delta_rule():
             S = np.exp(la[t, h]) * (np.eye(d) - beta[t, h] * kk @ kk.T) @ S + beta[t, h] * kk @ v[t, h][None, :]
             np.testing.assert_allclose(o[t, h], 0.5 * S.T @ q[t, h], atol=1e-12)
         np.testing.assert_allclose(Sf[0, h], S, atol=1e-12)
+
+
+# P18 a few tokens per request through the layer core from pooled states == one
+#     decode-layer step (P15) per token, in order; verify leaves both pools as they are.
+def test_decode_layer_tokens_equals_decode_layer_steps():
+    H, d, P = 2, 8, 5
+    lens, slot = [3, 0, 1, 5], [4, 0, 2, 1]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T = int(cu[-1])
+    rng = np.random.default_rng(1000)
+    qp, kp, vp, z, g = (rng.standard_normal((T, H, d)) for _ in range(5))
+    conv_w = rng.standard_normal((3, H * d, 4)) * 0.5
+    A = rng.standard_normal(H) * 0.5
+    b = rng.standard_normal((H, d)) * 0.3
+    bl = rng.standard_normal((T, H))
+    S_pool = rng.standard_normal((P, H, d, d)) * 0.3
+    conv_pool = rng.standard_normal((P, 3, 3, H, d))
+    for wb in (False, True):
+        o, S_new, conv_new = oracle.kda_decode_layer_tokens(qp, kp, vp, conv_w, z, A, b, bl, g, cu,
+                                                            slot, S_pool, conv_pool, wb)
+        if not wb:
+            np.testing.assert_array_equal(S_new, S_pool)
+            np.testing.assert_array_equal(conv_new, conv_pool)
+        for r, n in enumerate(slot):
+            S_row, c_row = S_pool.copy(), conv_pool.copy()
+            for t in range(cu[r], cu[r + 1]):
+                sl = slice(t, t + 1)
+                ot, S_row, c_row = oracle.kda_decode_layer(qp[sl], kp[sl], vp[sl], conv_w, z[sl], A, b,
+                                                           bl[sl], g[sl], [n], S_row, c_row)
+                np.testing.assert_allclose(o[t], ot[0], atol=1e-12)
+            if wb:
+                np.testing.assert_allclose(S_new[n], S_row[n], atol=1e-12)
+                np.testing.assert_array_equal(conv_new[n], c_row[n])
+        untouched = sorted(set(range(P)) - set(slot))
+        np.testing.assert_array_equal(S_new[untouched], S_pool[untouched])
+        np.testing.assert_array_equal(conv_new[untouched], conv_pool[untouched])
