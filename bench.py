@@ -341,6 +341,35 @@ def run_ours(args, world, rank, local):
                                "kernel": "kda_prefill_head_decay"}}
     del la_head
 
+    # ---------------- the long prefill: 1 x 131,072 tokens x 96 heads, carried S0 ----------------
+    long_prefill = None
+    if not args.skip_long_prefill:
+        linp4 = synthetic.workload(4, device=dev)
+        T4 = linp4.q.shape[0]
+        o4 = torch.empty((T4, H, D), dtype=torch.bfloat16, device=dev)
+        S4 = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+
+        def long_step():
+            kda.kda_prefill(linp4.q, linp4.k, linp4.v, linp4.log_alpha, linp4.beta,
+                            linp4.cu_seqlens, linp4.S0, o=o4, S_final=S4)
+
+        l4_steps = max(1, min(args.steps, 5))
+        l4_total, l4_per = time_launches(long_step, l4_steps, args.warmup, world)
+        l4_ms = max_over_ranks(l4_total / l4_steps, world)
+        l4_launch = sum(l4_per) / len(l4_per)
+        l4_bytes = T4 * H * PREFILL_BYTES_PER_TOKEN_HEAD + 2 * H * STATE_BYTES
+        long_prefill = {"workload": "B=1 H=96 T=131072 bf16, S0 ~ N(0, 0.1), log alpha from "
+                                    "x ~ N(1, 1)", "entry_point": "kda_prefill",
+                        "ms_per_step": l4_ms, "tokens_per_s": aggregate_rate(T4, l4_ms, world),
+                        "roofline": {"bound": "hbm",
+                                     "achieved": l4_bytes / (l4_launch / 1e3) / 1e9,
+                                     "peak": hbm, "unit": "GB/s",
+                                     "frac": l4_bytes / (l4_launch / 1e3) / 1e9 / hbm,
+                                     "traffic": traffic_bytes("prefill", T4 * H),
+                                     "peak_kind": peak_kind, "kernel": "kda_prefill"}}
+        del linp4, o4, S4
+        torch.cuda.empty_cache()
+
     # ---------------- end to end through the C ABI with host buffers ----------------
     host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "log_alpha", "beta")}
     dev_bufs = {n: getattr(inp, n) for n in host}
@@ -565,6 +594,7 @@ def run_ours(args, world, rank, local):
             "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "prefill_checkpoints": checkpoints, "prefill_head_decay": head_decay,
+            "long_prefill": long_prefill,
             "decode": decode,
             "decode_layer": decode_layer, "speculative": spec, "layer_core": layer,
             "clocks": clk, "gpu_launches": args.steps,
@@ -640,6 +670,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-layer-core", action="store_true")
+    ap.add_argument("--skip-long-prefill", action="store_true",
+                    help="skip the 131,072-token prefill leg (19 GB of inputs)")
     ap.add_argument("--skip-staged-layer-core", action="store_true",
                     help="time only the fused layer core, not the three-launch composition")
     ap.add_argument("--only", choices=["prefill", "decode", "decode_layer", "decode_tokens",
