@@ -94,7 +94,8 @@ namespace {
 // kda_prefill in full: per-channel decay ([T][H][128]) or one decay per (token, head) ([T][H]).
 kda_status prefill_impl(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
                         int32_t total_tokens, int32_t num_heads, const void *q, const void *k,
-                        const void *v, const float *log_alpha, bool head_decay, const float *beta,
+                        const void *v, const float *log_alpha, bool head_decay, bool recurrent,
+                        const float *beta,
                         const float *S0, const int32_t *cu_seqlens, float scale, void *o,
                         float *S_final, void *workspace, size_t workspace_bytes,
                         int32_t ckpt_every, const int32_t *ckpt_base, float *ckpt_states,
@@ -134,9 +135,10 @@ kda_status prefill_impl(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seq
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
     a.ckpt = Checkpoints{ckpt_every, ckpt_base, ckpt_states};
     a.head_decay = head_decay ? 1 : 0;
+    a.recurrent = recurrent ? 1 : 0;
     a.status = device_status();
-    // bf16 inputs: chunked tensor-core kernel; fp32 inputs: full-precision recurrent kernel.
-    if (in_dtype == KDA_BF16)
+    // bf16 inputs: chunked tensor-core kernel; fp32 inputs (or any decay): the recurrent kernel.
+    if (in_dtype == KDA_BF16 && !recurrent)
         return from_cuda(launch_prefill_tc(a, static_cast<cudaStream_t>(stream)));
     return from_cuda(launch_prefill_recurrent(a, static_cast<cudaStream_t>(stream)));
 }
@@ -154,8 +156,8 @@ kda_status kda_prefill_with_checkpoints(kda_dtype in_dtype, kda_dtype out_dtype,
                                         int32_t ckpt_every, const int32_t *ckpt_base,
                                         float *ckpt_states, void *stream) {
     return prefill_impl(in_dtype, out_dtype, num_seqs, total_tokens, num_heads, q, k, v, log_alpha,
-                        false, beta, S0, cu_seqlens, scale, o, S_final, workspace, workspace_bytes,
-                        ckpt_every, ckpt_base, ckpt_states, stream);
+                        false, false, beta, S0, cu_seqlens, scale, o, S_final, workspace,
+                        workspace_bytes, ckpt_every, ckpt_base, ckpt_states, stream);
 }
 
 kda_status kda_prefill_head_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
@@ -166,8 +168,20 @@ kda_status kda_prefill_head_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32
                                   size_t workspace_bytes, int32_t ckpt_every,
                                   const int32_t *ckpt_base, float *ckpt_states, void *stream) {
     return prefill_impl(in_dtype, out_dtype, num_seqs, total_tokens, num_heads, q, k, v, log_alpha,
-                        true, beta, S0, cu_seqlens, scale, o, S_final, workspace, workspace_bytes,
-                        ckpt_every, ckpt_base, ckpt_states, stream);
+                        true, false, beta, S0, cu_seqlens, scale, o, S_final, workspace,
+                        workspace_bytes, ckpt_every, ckpt_base, ckpt_states, stream);
+}
+
+kda_status kda_prefill_unbounded_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
+                                       int32_t total_tokens, int32_t num_heads, const void *q,
+                                       const void *k, const void *v, const float *log_alpha,
+                                       const float *beta, const float *S0,
+                                       const int32_t *cu_seqlens, float scale, void *o,
+                                       float *S_final, void *workspace, size_t workspace_bytes,
+                                       void *stream) {
+    return prefill_impl(in_dtype, out_dtype, num_seqs, total_tokens, num_heads, q, k, v, log_alpha,
+                        false, true, beta, S0, cu_seqlens, scale, o, S_final, workspace,
+                        workspace_bytes, 0, nullptr, nullptr, stream);
 }
 
 }  // extern "C"
@@ -213,12 +227,15 @@ kda_status kda_decode_step_head_decay(kda_dtype in_dtype, kda_dtype out_dtype, i
                        S_inout, scale, o, stream);
 }
 
-kda_status kda_frontend(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
-                        const void *qp, const void *kp, const void *vp, const float *conv_w,
-                        const void *z, const float *A, const float *b, const void *beta_logit,
-                        const int32_t *cu_seqlens, float l2_eps, kda_dtype out_dtype,
-                        void *q_hat, void *k_hat, void *v_out, float *log_alpha, float *beta,
-                        void *stream) {
+}  // extern "C"
+
+namespace {
+kda_status frontend_impl(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                         const void *qp, const void *kp, const void *vp, const float *conv_w,
+                         const void *z, const float *A, const float *b, const void *beta_logit,
+                         const int32_t *cu_seqlens, float l2_eps, kda_dtype out_dtype,
+                         void *q_hat, void *k_hat, void *v_out, float *log_alpha, float *beta,
+                         bool unbounded_decay, void *stream) {
     if (!ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
     if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
     if (!ok_ptr_elem(cu_seqlens, 4) || !ok_ptr(conv_w) || !ok_ptr_elem(A, 4) || !ok_opt_ptr(b))
@@ -240,7 +257,35 @@ kda_status kda_frontend(int32_t num_seqs, int32_t total_tokens, int32_t num_head
     a.conv_w = conv_w; a.A = A; a.b = b; a.cu_seqlens = cu_seqlens; a.l2_eps = l2_eps;
     a.out_dtype = out_dtype; a.q_hat = q_hat; a.k_hat = k_hat; a.v_out = v_out;
     a.log_alpha = log_alpha; a.beta = beta;
+    a.unbounded_decay = unbounded_decay ? 1 : 0;
     return from_cuda(launch_frontend(a, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" {
+
+kda_status kda_frontend(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                        const void *qp, const void *kp, const void *vp, const float *conv_w,
+                        const void *z, const float *A, const float *b, const void *beta_logit,
+                        const int32_t *cu_seqlens, float l2_eps, kda_dtype out_dtype,
+                        void *q_hat, void *k_hat, void *v_out, float *log_alpha, float *beta,
+                        void *stream) {
+    return frontend_impl(num_seqs, total_tokens, num_heads, qp, kp, vp, conv_w, z, A, b,
+                         beta_logit, cu_seqlens, l2_eps, out_dtype, q_hat, k_hat, v_out,
+                         log_alpha, beta, false, stream);
+}
+
+kda_status kda_frontend_unbounded_decay(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                        const void *qp, const void *kp, const void *vp,
+                                        const float *conv_w, const void *z, const float *A,
+                                        const float *b, const void *beta_logit,
+                                        const int32_t *cu_seqlens, float l2_eps,
+                                        kda_dtype out_dtype, void *q_hat, void *k_hat,
+                                        void *v_out, float *log_alpha, float *beta,
+                                        void *stream) {
+    return frontend_impl(num_seqs, total_tokens, num_heads, qp, kp, vp, conv_w, z, A, b,
+                         beta_logit, cu_seqlens, l2_eps, out_dtype, q_hat, k_hat, v_out,
+                         log_alpha, beta, true, stream);
 }
 
 kda_status kda_output_gate(int64_t num_rows, kda_dtype in_dtype, const void *o_tilde,
@@ -270,12 +315,16 @@ size_t kda_layer_core_workspace_size(int32_t num_seqs, int32_t total_tokens, int
            + kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, KDA_FP32);
 }
 
-kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
-                          const void *qp, const void *kp, const void *vp, const float *conv_w,
-                          const void *z, const float *A, const float *b, const void *beta_logit,
-                          const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
-                          float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
-                          float *S_final, void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+kda_status layer_core_impl(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                           const void *qp, const void *kp, const void *vp, const float *conv_w,
+                           const void *z, const float *A, const float *b, const void *beta_logit,
+                           const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
+                           float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
+                           float *S_final, void *workspace, size_t workspace_bytes,
+                           bool unbounded_decay, void *stream) {
     if (!ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
     if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
     if (total_tokens > 0 && (!ok_ptr(g) || !ok_ptr(o_gated))) return KDA_ERR_INVALID_ARGUMENT;
@@ -295,9 +344,9 @@ kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_he
     void *pre_ws = reinterpret_cast<unsigned char *>(o_tilde) + align256(rows * kD * 4);
     const size_t pre_ws_bytes = kda_prefill_workspace_size(num_seqs, total_tokens, num_heads,
                                                            KDA_FP32);
-    kda_status st = kda_frontend(num_seqs, total_tokens, num_heads, qp, kp, vp, conv_w, z, A, b,
-                                 beta_logit, cu_seqlens, l2_eps, KDA_FP32, q_hat, k_hat, v_out,
-                                 log_alpha, beta, stream);
+    kda_status st = frontend_impl(num_seqs, total_tokens, num_heads, qp, kp, vp, conv_w, z, A, b,
+                                  beta_logit, cu_seqlens, l2_eps, KDA_FP32, q_hat, k_hat, v_out,
+                                  log_alpha, beta, unbounded_decay, stream);
     if (st != KDA_OK) return st;
     st = kda_prefill(KDA_FP32, KDA_FP32, num_seqs, total_tokens, num_heads, q_hat, k_hat, v_out,
                      log_alpha, beta, S0, cu_seqlens, scale, o_tilde, S_final, pre_ws,
@@ -305,6 +354,33 @@ kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_he
     if (st != KDA_OK) return st;
     return kda_output_gate((int64_t)rows, KDA_FP32, o_tilde, g, rms_eps, out_dtype, o_gated,
                            stream);
+}
+}  // namespace
+
+extern "C" {
+
+kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                          const void *qp, const void *kp, const void *vp, const float *conv_w,
+                          const void *z, const float *A, const float *b, const void *beta_logit,
+                          const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
+                          float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
+                          float *S_final, void *workspace, size_t workspace_bytes, void *stream) {
+    return layer_core_impl(num_seqs, total_tokens, num_heads, qp, kp, vp, conv_w, z, A, b,
+                           beta_logit, g, cu_seqlens, S0, scale, l2_eps, rms_eps, out_dtype,
+                           o_gated, S_final, workspace, workspace_bytes, false, stream);
+}
+
+kda_status kda_layer_core_unbounded_decay(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                          const void *qp, const void *kp, const void *vp,
+                                          const float *conv_w, const void *z, const float *A,
+                                          const float *b, const void *beta_logit, const void *g,
+                                          const int32_t *cu_seqlens, const float *S0, float scale,
+                                          float l2_eps, float rms_eps, kda_dtype out_dtype,
+                                          void *o_gated, float *S_final, void *workspace,
+                                          size_t workspace_bytes, void *stream) {
+    return layer_core_impl(num_seqs, total_tokens, num_heads, qp, kp, vp, conv_w, z, A, b,
+                           beta_logit, g, cu_seqlens, S0, scale, l2_eps, rms_eps, out_dtype,
+                           o_gated, S_final, workspace, workspace_bytes, true, stream);
 }
 
 kda_status kda_layer_core_fused(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,

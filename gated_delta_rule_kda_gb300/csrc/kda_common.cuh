@@ -148,6 +148,7 @@ struct PrefillArgs {
     size_t workspace_bytes;
     Checkpoints ckpt;
     int32_t head_decay;  // 1: log_alpha is [T][H], one decay per (token, head)
+    int32_t recurrent;   // 1: the token-by-token kernel whatever the input type (any decay <= 0)
     DeviceStatus status;
 };
 
@@ -160,6 +161,7 @@ struct FrontendArgs {
     kda_dtype out_dtype;
     void *q_hat, *k_hat, *v_out;
     float *log_alpha, *beta;
+    int32_t unbounded_decay;  // 1: log_alpha = -e^A softplus(z + b) instead of -5 sigmoid(e^A (z + b))
 };
 
 struct GateArgs {

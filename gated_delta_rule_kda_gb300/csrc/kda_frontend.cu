@@ -6,6 +6,9 @@
 //   x^c = SiLU( sum_{j=0..3} w[x][h*128+i][j] * x^p_{t-j} )   (zero before the sequence start)
 //   q^, k^ = x^c / sqrt(sum_i x^c^2 + l2_eps)                  (v is not normalised)
 //   log_alpha = -5 sigmoid(e^{A_h} (z + b));   beta = sigmoid(beta_logit)
+// or, with the unbounded gate of Kimi Linear ("Kimi K3's Architecture: Kimi Delta
+// Attention, Attention Residuals, and 896 Experts", section "Channel-wise decay, and the
+// floor K3 puts under it"), log_alpha = -e^{A_h} softplus(z + b), in (-inf, 0).
 // Output gate (same equation list): o^g = sigmoid(g) * o~ / sqrt(mean(o~^2) + eps).
 //
 // Both kernels give one warp to one (token, head) row of 128 channels: lane l
@@ -22,6 +25,11 @@ constexpr int kWarpsPerBlock = kThreads / 32;
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
 __device__ __forceinline__ float siluf_(float x) { return x * sigmoidf_(x); }
+// softplus(x) = log(1 + e^x); above 20 it equals x to fp32 precision.
+__device__ __forceinline__ float softplusf_(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+__device__ __forceinline__ float log_decay(float eA, float zb, bool unbounded) {
+    return unbounded ? -eA * softplusf_(zb) : -5.f * sigmoidf_(eA * zb);
+}
 
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
@@ -84,11 +92,12 @@ frontend_kernel(FrontendArgs a) {
     const float4 z = load4(a.z + (size_t)row * kD + c0);
     float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
     if (a.b != nullptr) b = *reinterpret_cast<const float4 *>(a.b + (size_t)h * kD + c0);
+    const bool ub = a.unbounded_decay != 0;
     float4 la;
-    la.x = -5.f * sigmoidf_(eA * (z.x + b.x));
-    la.y = -5.f * sigmoidf_(eA * (z.y + b.y));
-    la.z = -5.f * sigmoidf_(eA * (z.z + b.z));
-    la.w = -5.f * sigmoidf_(eA * (z.w + b.w));
+    la.x = log_decay(eA, z.x + b.x, ub);
+    la.y = log_decay(eA, z.y + b.y, ub);
+    la.z = log_decay(eA, z.z + b.z, ub);
+    la.w = log_decay(eA, z.w + b.w, ub);
     *reinterpret_cast<float4 *>(a.log_alpha + (size_t)row * kD + c0) = la;
     if (lane == 0) a.beta[row] = sigmoidf_(__bfloat162float(a.beta_logit[row]));
 }

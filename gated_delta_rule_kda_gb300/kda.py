@@ -41,12 +41,15 @@ EXPORTED = (
     "kda_prefill",
     "kda_prefill_with_checkpoints",
     "kda_prefill_head_decay",
+    "kda_prefill_unbounded_decay",
     "kda_decode_step",
     "kda_decode_step_head_decay",
     "kda_frontend",
+    "kda_frontend_unbounded_decay",
     "kda_output_gate",
     "kda_layer_core_workspace_size",
     "kda_layer_core",
+    "kda_layer_core_unbounded_decay",
     "kda_layer_core_noalloc",
     "kda_layer_core_fused",
     "kda_layer_core_fused_with_checkpoints",
@@ -88,6 +91,8 @@ def _load() -> ctypes.CDLL:
     lib.kda_prefill_with_checkpoints.restype = ctypes.c_int
     lib.kda_prefill_head_decay.argtypes = lib.kda_prefill_with_checkpoints.argtypes
     lib.kda_prefill_head_decay.restype = ctypes.c_int
+    lib.kda_prefill_unbounded_decay.argtypes = lib.kda_prefill.argtypes
+    lib.kda_prefill_unbounded_decay.restype = ctypes.c_int
     lib.kda_decode_step.argtypes = [ctypes.c_int, ctypes.c_int, I32, I32, P, P, P, P, P, P, F,
                                     P, P]
     lib.kda_decode_step.restype = ctypes.c_int
@@ -96,6 +101,8 @@ def _load() -> ctypes.CDLL:
     lib.kda_frontend.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, F, ctypes.c_int,
                                  P, P, P, P, P, P]
     lib.kda_frontend.restype = ctypes.c_int
+    lib.kda_frontend_unbounded_decay.argtypes = lib.kda_frontend.argtypes
+    lib.kda_frontend_unbounded_decay.restype = ctypes.c_int
     lib.kda_output_gate.argtypes = [I64, ctypes.c_int, P, P, F, ctypes.c_int, P, P]
     lib.kda_output_gate.restype = ctypes.c_int
     lib.kda_layer_core_workspace_size.argtypes = [I32, I32, I32]
@@ -103,6 +110,8 @@ def _load() -> ctypes.CDLL:
     lib.kda_layer_core.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, F, F, F,
                                    ctypes.c_int, P, P, P, SZ, P]
     lib.kda_layer_core.restype = ctypes.c_int
+    lib.kda_layer_core_unbounded_decay.argtypes = lib.kda_layer_core.argtypes
+    lib.kda_layer_core_unbounded_decay.restype = ctypes.c_int
     lib.kda_layer_core_noalloc.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, F, F,
                                            F, ctypes.c_int, P, P, P]
     lib.kda_layer_core_noalloc.restype = ctypes.c_int
@@ -179,7 +188,7 @@ def kda_prefill_workspace_size(num_seqs: int, total_tokens: int, num_heads: int,
 
 def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, scale=DEFAULT_SCALE, *,
                 out_dtype=None, o=None, S_final=None, want_state=True, workspace=None,
-                stream=None):
+                stream=None, _entry="kda_prefill"):
     """Packed-varlen prefill.  Returns (o, S_final or None).
 
     q, k, v [T, H, 128] (bf16 or fp32); log_alpha [T, H, 128] fp32; beta [T, H] fp32;
@@ -196,11 +205,18 @@ def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0=None, scale=DEFAULT_SCA
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = _lib.kda_prefill(_dt(q), _dtype_code(o.dtype), N, T, H, _p(q), _p(k), _p(v),
+    rc = getattr(_lib, _entry)(_dt(q), _dtype_code(o.dtype), N, T, H, _p(q), _p(k), _p(v),
                           _p(log_alpha), _p(beta), _p(S0), _p(cu_seqlens), float(scale), _p(o),
                           _p(S_final), _p(workspace), wbytes, _stream(stream))
-    _check("kda_prefill", rc)
+    _check(_entry, rc)
     return o, S_final
+
+
+def kda_prefill_unbounded_decay(q, k, v, log_alpha, beta, cu_seqlens, S0=None,
+                                scale=DEFAULT_SCALE, **kw):
+    """kda_prefill for any log_alpha <= 0 (-inf included) on the token-by-token kernel."""
+    return kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, S0, scale,
+                       _entry="kda_prefill_unbounded_decay", **kw)
 
 
 def checkpoint_offsets(cu_seqlens, every: int) -> torch.Tensor:
@@ -284,7 +300,7 @@ def kda_decode_step_head_decay(q, k, v, log_alpha, beta, S_inout, scale=DEFAULT_
 
 
 def kda_frontend(qp, kp, vp, conv_w, z, A, b, beta_logit, cu_seqlens, l2_eps=1e-6, *,
-                 out_dtype=torch.bfloat16, stream=None):
+                 out_dtype=torch.bfloat16, stream=None, _entry="kda_frontend"):
     """Returns (q_hat, k_hat, v, log_alpha, beta)."""
     T, H, _ = qp.shape
     N = cu_seqlens.shape[0] - 1
@@ -294,12 +310,19 @@ def kda_frontend(qp, kp, vp, conv_w, z, A, b, beta_logit, cu_seqlens, l2_eps=1e-
     v_out = torch.empty_like(q_hat)
     log_alpha = torch.empty((T, H, HEAD_DIM), dtype=torch.float32, device=dev)
     beta = torch.empty((T, H), dtype=torch.float32, device=dev)
-    rc = _lib.kda_frontend(N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A), _p(b),
+    rc = getattr(_lib, _entry)(N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A), _p(b),
                            _p(beta_logit), _p(cu_seqlens), float(l2_eps),
                            _dtype_code(out_dtype), _p(q_hat), _p(k_hat), _p(v_out),
                            _p(log_alpha), _p(beta), _stream(stream))
-    _check("kda_frontend", rc)
+    _check(_entry, rc)
     return q_hat, k_hat, v_out, log_alpha, beta
+
+
+def kda_frontend_unbounded_decay(qp, kp, vp, conv_w, z, A, b, beta_logit, cu_seqlens, l2_eps=1e-6,
+                                 **kw):
+    """kda_frontend with Kimi Linear's gate log_alpha = -e^A softplus(z + b)."""
+    return kda_frontend(qp, kp, vp, conv_w, z, A, b, beta_logit, cu_seqlens, l2_eps,
+                        _entry="kda_frontend_unbounded_decay", **kw)
 
 
 def kda_output_gate(o_tilde, g, eps=1e-6, *, out_dtype=torch.bfloat16, out=None, stream=None):
@@ -318,7 +341,8 @@ def kda_layer_core_workspace_size(num_seqs: int, total_tokens: int, num_heads: i
 
 def kda_layer_core(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=None,
                    scale=DEFAULT_SCALE, l2_eps=1e-6, rms_eps=1e-6, *, out_dtype=torch.bfloat16,
-                   o=None, S_final=None, want_state=True, workspace=None, stream=None):
+                   o=None, S_final=None, want_state=True, workspace=None, stream=None,
+                   _entry="kda_layer_core"):
     """Front end -> recurrence -> output gate.  Returns (o_gated, S_final or None)."""
     T, H, _ = qp.shape
     N = cu_seqlens.shape[0] - 1
@@ -330,12 +354,19 @@ def kda_layer_core(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=No
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=qp.device)
     wbytes = workspace.numel() * workspace.element_size()
-    rc = _lib.kda_layer_core(N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A), _p(b),
+    rc = getattr(_lib, _entry)(N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A), _p(b),
                              _p(beta_logit), _p(g), _p(cu_seqlens), _p(S0), float(scale),
                              float(l2_eps), float(rms_eps), _dtype_code(o.dtype), _p(o),
                              _p(S_final), _p(workspace), wbytes, _stream(stream))
-    _check("kda_layer_core", rc)
+    _check(_entry, rc)
     return o, S_final
+
+
+def kda_layer_core_unbounded_decay(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=None,
+                                   **kw):
+    """kda_layer_core with Kimi Linear's unbounded decay gate (staged, fp32 intermediates)."""
+    return kda_layer_core(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0,
+                          _entry="kda_layer_core_unbounded_decay", **kw)
 
 
 def kda_layer_core_noalloc(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=None,

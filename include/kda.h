@@ -172,6 +172,25 @@ kda_status kda_prefill_head_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32
                                   const int32_t *ckpt_base, float *ckpt_states, void *stream);
 
 /*
+ * kda_prefill_unbounded_decay - kda_prefill for decays without the floor: any
+ * log_alpha <= 0, -inf included (alpha = 0 clears the state).  Below the floor
+ * of -5 the chunk's reciprocal decays overflow, which is why Kimi Linear's
+ * unbounded gate needed a position-pair fallback inside each chunk ("Kimi K3's
+ * Architecture: Kimi Delta Attention, Attention Residuals, and 896 Experts",
+ * section "Channel-wise decay, and the floor K3 puts under it"); this call runs
+ * the token-by-token kernel for every input type instead, which has no
+ * reciprocal and is exact up to fp32 rounding.  Arguments, layouts and errors
+ * as kda_prefill.
+ */
+kda_status kda_prefill_unbounded_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
+                                       int32_t total_tokens, int32_t num_heads, const void *q,
+                                       const void *k, const void *v, const float *log_alpha,
+                                       const float *beta, const float *S0,
+                                       const int32_t *cu_seqlens, float scale, void *o,
+                                       float *S_final, void *workspace, size_t workspace_bytes,
+                                       void *stream);
+
+/*
  * kda_decode_step - one token per request, state updated in place.
  *
  * One step of the recurrence for each (request b, head h): "each step reads
@@ -233,6 +252,21 @@ kda_status kda_frontend(int32_t num_seqs, int32_t total_tokens, int32_t num_head
                         void *stream);
 
 /*
+ * kda_frontend_unbounded_decay - kda_frontend with Kimi Linear's decay gate,
+ * log_alpha = -e^{A_h} softplus(z + b), in (-inf, 0) (same section as
+ * kda_prefill_unbounded_decay), instead of K3's -5 sigmoid(e^{A_h}(z + b)).
+ * Everything else, arguments and errors included, as kda_frontend.  Its
+ * log_alpha may lie below -5: feed it to kda_prefill_unbounded_decay.
+ */
+kda_status kda_frontend_unbounded_decay(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                        const void *qp, const void *kp, const void *vp,
+                                        const float *conv_w, const void *z, const float *A,
+                                        const float *b, const void *beta_logit,
+                                        const int32_t *cu_seqlens, float l2_eps,
+                                        kda_dtype out_dtype, void *q_hat, void *k_hat,
+                                        void *v_out, float *log_alpha, float *beta, void *stream);
+
+/*
  * kda_output_gate - o^g = sigmoid(g) * RMSNorm(o~) per head over its 128
  * channels, RMSNorm(x) = x / sqrt(mean(x^2) + eps), unit weight ("Kimi K3 ·
  * KDA layer", KDA equation list).
@@ -272,6 +306,21 @@ kda_status kda_layer_core(int32_t num_seqs, int32_t total_tokens, int32_t num_he
                           const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
                           float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
                           float *S_final, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * kda_layer_core_unbounded_decay - kda_layer_core with Kimi Linear's unbounded
+ * decay gate (kda_frontend_unbounded_decay -> kda_prefill_unbounded_decay ->
+ * kda_output_gate through the same workspace, fp32 intermediates).  Arguments,
+ * workspace size and errors as kda_layer_core.
+ */
+kda_status kda_layer_core_unbounded_decay(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
+                                          const void *qp, const void *kp, const void *vp,
+                                          const float *conv_w, const void *z, const float *A,
+                                          const float *b, const void *beta_logit, const void *g,
+                                          const int32_t *cu_seqlens, const float *S0, float scale,
+                                          float l2_eps, float rms_eps, kda_dtype out_dtype,
+                                          void *o_gated, float *S_final, void *workspace,
+                                          size_t workspace_bytes, void *stream);
 
 /*
  * kda_layer_core_noalloc - kda_layer_core without a caller-provided workspace.

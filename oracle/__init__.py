@@ -327,3 +327,33 @@ def kda_decode_layer_tokens(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_token
     if return_o_tilde:
         return o, S_new, conv_new, o_tilde
     return o, S_new, conv_new
+
+
+def kimi_linear_log_decay(z, A, b):
+    """Kimi Linear's unbounded decay gate (fp64): log alpha = -e^{A_h} softplus(z + b),
+    in (-inf, 0) ("Kimi K3's Architecture: Kimi Delta Attention, Attention Residuals, and
+    896 Experts", section "Channel-wise decay, and the floor K3 puts under it").
+    z: [T, H, d]; A: [H]; b: [H, d] or None.  softplus(x) = log(1 + e^x) = logaddexp(0, x)."""
+    z = _f64(z)
+    x = z + (0.0 if b is None else _f64(b)[None])
+    return -np.exp(_f64(A))[None, :, None] * np.logaddexp(0.0, x)
+
+
+def kda_frontend_unbounded_decay(qp, kp, vp, conv_w, z, A, b, beta_logit, cu_seqlens,
+                                 l2_eps=1e-6, n_threads=None):
+    """The front end with Kimi Linear's decay gate: q^, k^, v and beta as kda_frontend,
+    log alpha from kimi_linear_log_decay."""
+    qh, kh, vv, _, beta = kda_frontend(qp, kp, vp, conv_w, z, A, b, beta_logit, cu_seqlens,
+                                       l2_eps, n_threads)
+    return qh, kh, vv, kimi_linear_log_decay(z, A, b), beta
+
+
+def kda_layer_core_unbounded_decay(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens,
+                                   S0=None, scale=None, l2_eps=1e-6, rms_eps=1e-6,
+                                   n_threads=None):
+    """The layer core with Kimi Linear's decay gate (fp64): front end, the recurrence
+    (which takes any log alpha <= 0), the output gate.  Returns (o_gated, S_final)."""
+    qh, kh, vv, la, beta = kda_frontend_unbounded_decay(qp, kp, vp, conv_w, z, A, b, beta_logit,
+                                                        cu_seqlens, l2_eps, n_threads)
+    ot, Sf = kda_prefill(qh, kh, vv, la, beta, cu_seqlens, S0, scale, n_threads)
+    return kda_output_gate(ot, g, rms_eps, n_threads), Sf

@@ -290,3 +290,20 @@ def test_decode_layer_tokens_rejects_bad_arguments(kda, bad):
 
 def test_decode_layer_tokens_too_large_unsupported(kda):
     assert _decode_layer_tokens(kda.library(), B=1 << 20, H=1 << 12, conv=FAKE + (1 << 40)) == 2
+
+
+def test_unbounded_decay_entries_validate(kda):
+    lib = kda.library()
+    a = dict(in_dt=0, out_dt=0, N=1, T=4, H=2, q=FAKE, k=FAKE, v=FAKE, la=FAKE, beta=FAKE,
+             S0=None, cu=FAKE, scale=0.1, o=FAKE, Sf=None, ws=None, wsb=0, stream=None)
+    for bad in (dict(q=None), dict(la=MIS), dict(H=0), dict(S0=FAKE, Sf=FAKE + 64)):
+        c = dict(a, **bad)
+        assert lib.kda_prefill_unbounded_decay(c["in_dt"], c["out_dt"], c["N"], c["T"], c["H"],
+                                               c["q"], c["k"], c["v"], c["la"], c["beta"], c["S0"],
+                                               c["cu"], c["scale"], c["o"], c["Sf"], c["ws"],
+                                               c["wsb"], c["stream"]) == 1
+    assert lib.kda_frontend_unbounded_decay(1, 4, 2, FAKE, FAKE, None, FAKE, FAKE, FAKE, None, FAKE,
+                                            FAKE, 1e-6, 0, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert lib.kda_layer_core_unbounded_decay(1, 4, 2, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                              FAKE, FAKE, FAKE, None, 0.1, 1e-6, 1e-6, 0, FAKE,
+                                              None, None, 0, None) == 3  # no workspace

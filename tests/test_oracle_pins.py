@@ -590,3 +590,47 @@ def test_decode_layer_tokens_equals_decode_layer_steps():
         untouched = sorted(set(range(P)) - set(slot))
         np.testing.assert_array_equal(S_new[untouched], S_pool[untouched])
         np.testing.assert_array_equal(conv_new[untouched], conv_pool[untouched])
+
+
+# P19 Kimi Linear's unbounded decay gate [Arch-K3, "Channel-wise decay, and the floor K3
+#     puts under it": g = -e^A softplus(z)]: closed forms of softplus (ln 2 at 0; x + e^-x
+#     to first order for large x; e^x for very negative x), the range (-inf, 0), per-head
+#     scaling by e^A, b added before the softplus; and decays far below K3's floor of -5
+#     (and -inf) go through the recurrence exactly as P3/P4 say.
+def test_kimi_linear_gate_closed_forms():
+    A = np.array([0.0, np.log(3.0)])
+    z = np.zeros((1, 2, 4))
+    z[0, :, 1] = 30.0
+    z[0, :, 2] = -30.0
+    z[0, :, 3] = 1.0
+    la = oracle.kimi_linear_log_decay(z, A, None)
+    for h, eA in enumerate([1.0, 3.0]):
+        np.testing.assert_allclose(la[0, h, 0], -eA * np.log(2.0), rtol=1e-15)
+        np.testing.assert_allclose(la[0, h, 1], -eA * (30.0 + np.exp(-30.0)), rtol=1e-15)
+        np.testing.assert_allclose(la[0, h, 2], -eA * np.exp(-30.0), rtol=1e-12)
+        np.testing.assert_allclose(la[0, h, 3], -eA * np.log(1.0 + np.e), rtol=1e-15)
+    b = np.full((2, 4), 0.5)
+    np.testing.assert_allclose(oracle.kimi_linear_log_decay(z - 0.5, A, b), la, rtol=1e-15)
+    zz = np.random.default_rng(1100).standard_normal((50, 2, 4)) * 10
+    assert (oracle.kimi_linear_log_decay(zz, A, None) < 0).all()
+
+
+def test_unbounded_decays_in_the_recurrence():
+    T, H, d = 6, 1, 4
+    rng = np.random.default_rng(1101)
+    q = unit(rng.standard_normal((T, H, d)))
+    k = unit(rng.standard_normal((T, H, d)))
+    v = rng.standard_normal((T, H, d))
+    beta = np.full((T, H), 0.5)
+    S0 = rng.standard_normal((1, H, d, d))
+    la = np.full((T, H, d), -40.0)   # far below the floor: e^-40 ~ 4e-18 per step
+    la[3] = -np.inf                  # a full reset at token 3
+    o, Sf = oracle.kda_prefill(q, k, v, la, beta, [0, T], S0=S0)
+    assert np.isfinite(o).all() and np.isfinite(Sf).all()
+    # after the reset only tokens 3..5 write; each earlier state is scaled by e^-40 per step
+    S = np.zeros((d, d))
+    for t in range(3, T):
+        a = 0.0 if t == 3 else np.exp(-40.0)
+        S = a * S
+        S = S + beta[t, 0] * np.outer(k[t, 0], v[t, 0] - S.T @ k[t, 0])
+    np.testing.assert_allclose(Sf[0, 0], S, atol=1e-12)
