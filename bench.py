@@ -321,6 +321,24 @@ def run_ours(args, world, rank, local):
                    "overhead_vs_prefill": ck_ms / ms_step - 1.0}
     del ck_states
 
+    # ---------------- contents checks of the prefill inputs (one pass over log alpha) ----------------
+    def check_step():
+        kda.kda_check_prefill_inputs(inp.cu_seqlens, inp.log_alpha)
+
+    ch_total, ch_per = time_launches(check_step, args.steps, args.warmup, world)
+    ch_launch = sum(ch_per) / len(ch_per)
+    check_bytes = inp.log_alpha.numel() * 4 + inp.cu_seqlens.numel() * 4
+    if kda.kda_get_device_status()[0] != 0:
+        raise RuntimeError("the contents checks flagged the bench's own inputs")
+    contents_check = {"entry_point": "kda_check_prefill_inputs",
+                      "ms_per_step": max_over_ranks(ch_total / args.steps, world),
+                      "roofline": {"bound": "hbm",
+                                   "achieved": check_bytes / (ch_launch / 1e3) / 1e9,
+                                   "peak": hbm, "unit": "GB/s",
+                                   "frac": check_bytes / (ch_launch / 1e3) / 1e9 / hbm,
+                                   "traffic": None, "peak_kind": peak_kind,
+                                   "kernel": "kda_check_prefill_inputs"}}
+
     # ---------------- the Gated DeltaNet case: one decay per (token, head) ----------------
     la_head = inp.log_alpha[:, :, 0].contiguous()  # [T, H]: one channel's draws as the head's decay
 
@@ -571,6 +589,19 @@ def run_ours(args, world, rank, local):
             layer["staged"] = {"entry_point": "kda_layer_core", "ms_per_step": s_ms,
                                "tokens_per_s": aggregate_rate(LT, s_ms, world),
                                "launches_per_step": 3}
+
+            def unbounded_step():  # Kimi Linear's gate: no decay floor, token-by-token kernel
+                kda.kda_layer_core_unbounded_decay(linp.qp, linp.kp, linp.vp, linp.conv_w, linp.z,
+                                                   linp.A, linp.b, linp.beta_logit, linp.g,
+                                                   linp.cu_seqlens, None, o=og, S_final=Sl,
+                                                   workspace=ws)
+
+            u_total, _ = time_launches(unbounded_step, 2, 1, world)
+            u_ms = max_over_ranks(u_total / 2, world)
+            layer["unbounded_decay"] = {"entry_point": "kda_layer_core_unbounded_decay",
+                                        "ms_per_step": u_ms,
+                                        "tokens_per_s": aggregate_rate(LT, u_ms, world),
+                                        "launches_per_step": 3}
             del ws
         del linp, og, Sl
         torch.cuda.empty_cache()
@@ -594,7 +625,7 @@ def run_ours(args, world, rank, local):
             "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "prefill_checkpoints": checkpoints, "prefill_head_decay": head_decay,
-            "long_prefill": long_prefill,
+            "long_prefill": long_prefill, "contents_check": contents_check,
             "decode": decode,
             "decode_layer": decode_layer, "speculative": spec, "layer_core": layer,
             "clocks": clk, "gpu_launches": args.steps,

@@ -32,13 +32,23 @@ __global__ void __launch_bounds__(kThreads) check_prefill_kernel(const CheckArgs
     const size_t per_token = (size_t)a.num_heads * (a.head_decay ? 1 : kD);
     const size_t total = (size_t)a.total_tokens * per_token;
     const size_t stride = (size_t)gridDim.x * kThreads;
-    if (!a.head_decay) {  // [T][H][128]: four values per load
+    if (!a.head_decay) {  // [T][H][128]: four values per load, four loads in flight
         const float4 *p = reinterpret_cast<const float4 *>(a.log_alpha);
-        for (size_t i = (size_t)blockIdx.x * kThreads + tid; i < total / 4; i += stride) {
-            const float4 x = __ldcs(p + i);
-            if (!(decay_ok(x.x) && decay_ok(x.y) && decay_ok(x.z) && decay_ok(x.w)))
-                record_status(a.status, KDA_ERR_DEVICE_CHECK,
-                              (2u << 28) | ((uint32_t)(4 * i / per_token) & kIndexMask));
+        const size_t n4 = total / 4;
+        for (size_t i0 = (size_t)blockIdx.x * kThreads + tid; i0 < n4; i0 += 4 * stride) {
+            float4 x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const size_t i = i0 + u * stride;
+                x[u] = i < n4 ? __ldcs(p + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const size_t i = i0 + u * stride;
+                if (!(decay_ok(x[u].x) && decay_ok(x[u].y) && decay_ok(x[u].z) && decay_ok(x[u].w)))
+                    record_status(a.status, KDA_ERR_DEVICE_CHECK,
+                                  (2u << 28) | ((uint32_t)(4 * i / per_token) & kIndexMask));
+            }
         }
     } else {  // [T][H]
         for (size_t i = (size_t)blockIdx.x * kThreads + tid; i < total; i += stride)
