@@ -175,3 +175,14 @@ def test_many_units_with_refused_and_empty_requests(kda):
         assert_close(to64(S_pool[n]), S_ref[0], TOL_BF16, f"row of request {b}")
     untouched = sorted(set(range(800)) - {int(slot[b]) for b in keep})
     assert torch.equal(S_pool[untouched], inp.S_pool[untouched])
+
+
+def test_decay_reset_minus_infinity(kda):
+    """log alpha = -inf (alpha = 0) clears the row's state at that token; decode accepts it."""
+    inp = synthetic.decode_tokens_inputs([3, 5, 2], 2, 4, torch.float32, seed=76, device="cuda")
+    inp.log_alpha[1] = -float("inf")   # request 0, token 1
+    inp.log_alpha[6, 1] = -float("inf")  # request 1, token 3, head 1
+    o, S_pool, Sf = run(kda, inp, True)
+    ref_o, ref_pool, ref_f = reference(inp, True)
+    assert_close(to64(o), ref_o, TOL_FP32, "o")
+    assert_close(to64(Sf), ref_f, TOL_FP32, "S_final")

@@ -197,3 +197,18 @@ def test_fused_many_heads_several_waves(kda):
     ref_o, ref_S, ref_ot = oracle_layer_core(inp, heads)
     assert_gated_close(to64(og[:, heads]), ref_o, ref_ot, True)
     assert_close(to64(Sf[:, heads]), ref_S, TOL_BF16, "S_final")
+
+
+def test_fused_many_short_sequences(kda):
+    """200 sequences of 0 to 50 tokens through the fused layer core (index-order CTAs, many
+    sequences shorter than the convolution or a chunk)."""
+    lens = np.random.default_rng(44).integers(0, 51, size=200).tolist()
+    inp = synthetic.layer_inputs(lens, 2, seed=45, s0_std=0.1, device="cuda")
+    og, Sf = kda.kda_layer_core_fused(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b,
+                                      inp.beta_logit, inp.g, inp.cu_seqlens, inp.S0,
+                                      out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status()[0] == 0
+    ref_o, ref_S, ref_ot = oracle_layer_core(inp)
+    assert_gated_close(to64(og), ref_o, ref_ot, False)
+    assert_close(to64(Sf), ref_S, TOL_BF16, "S_final")

@@ -187,3 +187,11 @@ def test_chunk_boundaries(kda, lens):
     the last chunk holds 31, 32 or 1 rows."""
     inp = synthetic.prefill_inputs(lens, 2, torch.bfloat16, seed=27, s0_std=0.1, device="cuda")
     check(kda, inp, TOL_BF16, torch.float32)
+
+
+def test_many_short_sequences(kda):
+    """300 sequences of 0 to 70 tokens (more than the 64 the kernel orders longest first,
+    so CTAs take sequences in index order), H=2, carried states."""
+    lens = np.random.default_rng(24).integers(0, 71, size=300).tolist()
+    inp = synthetic.prefill_inputs(lens, 2, torch.bfloat16, seed=25, s0_std=0.1, device="cuda")
+    check(kda, inp, TOL_BF16, torch.float32)
