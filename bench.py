@@ -58,10 +58,10 @@ E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the ke
 # committed ncu captures (profiles/prefill_tc_kernel_T2048_H96.md, profiles/decode_kernel_B32_H96.md),
 # taken on a smaller case and scaled by units.  Valid only for the kernel source the capture
 # was taken on: a changed kernel reports traffic null until it is captured again (a digest is
-# carried over only across comment-only edits whose compiled kernel is byte-identical).
+# carried over only across edits whose compiled kernel is byte-identical: comments, host code).
 TRAFFIC = {
     "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-                "ea5cf3c551115ce9336f4d54ee528bc3935b50e9eaa2eefbb5a62dd4c3468568",
+                "54f1d982252df742d20d69fef22148d862218645100b056bb1c76b4558481db2",
                 (252.724992e6 + 37.786880e6) / (2048 * 96)),
     "decode": ("gated_delta_rule_kda_gb300/csrc/kda_decode.cu",
                "9f1e6145572ad4787343166be5659867b8c38d020db25a2e19651c2bcc6a5657",
