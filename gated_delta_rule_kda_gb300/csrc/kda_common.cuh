@@ -1,6 +1,7 @@
 // Shared device helpers and launcher declarations of libkda (sm_103a).
 #pragma once
 
+#include <atomic>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -20,6 +21,30 @@ struct DeviceStatus {
 __device__ __forceinline__ void record_status(DeviceStatus st, uint32_t code, uint32_t detail) {
     if (st.word == nullptr) return;
     if (atomicCAS(st.word, 0u, code) == 0u) atomicExch(st.word + 1, detail);
+}
+
+// Ask L2 to fetch [p, p + bytes) ahead of its use (bytes a multiple of 16; p must lie in an
+// allocation the caller owns).  The one-CTA-per-unit decode kernels use it for the state of
+// the unit one resident wave ahead, so that HBM keeps streaming while resident CTAs compute.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Streaming multiprocessors of the current device (cached per device; a racing first call
+// stores the same value).
+inline int device_sm_count() {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    const int slot = dev >= 0 && dev < kMaxDevices ? dev : 0;
+    int sms = cache[slot].load(std::memory_order_relaxed);
+    if (sms == 0) {
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+            sms = 1;
+        cache[slot].store(sms, std::memory_order_relaxed);
+    }
+    return sms;
 }
 
 template <typename T>
@@ -72,6 +97,7 @@ struct DecodeArgs {
     const void *q, *k, *v;
     const float *log_alpha, *beta;
     int32_t head_decay;  // 1: log_alpha is [B][H], one decay per (request, head)
+    int32_t prefetch_ahead;  // units between a CTA and the one whose state it prefetches (0: none)
     float *S;
     float scale;
     void *o;
@@ -92,6 +118,7 @@ struct DecodeLayerTokensArgs {
     float scale, l2_eps, rms_eps;
     kda_dtype out_dtype;
     void *o;                                                // [T][H][128]
+    int32_t prefetch_ahead;  // units between a CTA and the one whose state it prefetches (0: none)
     DeviceStatus status;
 };
 
@@ -108,6 +135,7 @@ struct DecodeTokensArgs {
     float *S_final;                        // [B][H][128][128] or null
     float scale;
     void *o;                               // [T][H][128]
+    int32_t prefetch_ahead;  // units between a CTA and the one whose state it prefetches (0: none)
     DeviceStatus status;
 };
 
@@ -132,6 +160,7 @@ struct DecodeLayerArgs {
     float scale, l2_eps, rms_eps;
     kda_dtype out_dtype;
     void *o;                                                // [B][H][128]
+    int32_t prefetch_ahead;  // units between a CTA and the one whose state it prefetches (0: none)
     DeviceStatus status;
 };
 

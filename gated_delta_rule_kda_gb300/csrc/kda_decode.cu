@@ -33,7 +33,7 @@ template <typename Tin, typename Tout, bool kHeadDecay>
 __global__ void __launch_bounds__(kThreads, 2)
 decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
               const float *__restrict__ log_alpha, const float *__restrict__ beta,
-              float *__restrict__ S, float scale, Tout *__restrict__ o) {
+              float *__restrict__ S, float scale, Tout *__restrict__ o, int prefetch_ahead) {
     __shared__ float s_q[kD], s_k[kD], s_a[kD], s_v[kD], s_u[kD];
     __shared__ float s_red_r[kWarps][kD], s_red_p[kWarps][kD];
     __shared__ float s_kq;
@@ -41,6 +41,10 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const size_t unit = blockIdx.x;
     float *Su = S + unit * (size_t)(kD * kD);
+    // L2 prefetch of the state one resident wave ahead (HBM keeps streaming while resident
+    // CTAs compute)
+    if (tid == 0 && prefetch_ahead > 0 && unit + prefetch_ahead < gridDim.x)
+        prefetch_l2(S + (unit + prefetch_ahead) * (size_t)(kD * kD), kD * kD * sizeof(float));
 
     // 1. Issue the whole state load first: 16 x 16 B per thread in flight.
     float4 s[kRowsPerWarp];
@@ -117,7 +121,7 @@ cudaError_t launch_typed(const DecodeArgs &a, cudaStream_t stream) {
     kernel<<<(unsigned)units, kThreads, 0, stream>>>(
         static_cast<const Tin *>(a.q), static_cast<const Tin *>(a.k),
         static_cast<const Tin *>(a.v), a.log_alpha, a.beta, a.S, a.scale,
-        static_cast<Tout *>(a.o));
+        static_cast<Tout *>(a.o), 2 * device_sm_count());
     return cudaGetLastError();
 }
 

@@ -100,6 +100,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(const DecodeL
     }
     const size_t unit = (size_t)b * H + h;
     float *Su = a.S_pool + ((size_t)n * H + h) * (size_t)(kD * kD);
+    if (tid == 0 && a.prefetch_ahead > 0) {  // L2 prefetch: the state one resident wave ahead
+        const size_t u2 = blockIdx.x + (size_t)a.prefetch_ahead;
+        if (u2 < gridDim.x) {
+            const int n2 = a.slot[u2 / H];
+            if (n2 >= 0 && n2 < a.pool_size)
+                prefetch_l2(a.S_pool + ((size_t)n2 * H + u2 % H) * (size_t)(kD * kD), kD * kD * sizeof(float));
+        }
+    }
 
     // 1. The front end's few inputs first (they decide when the state work can start),
     //    then the whole state load: 16 x 16 B per thread in flight.
@@ -197,7 +205,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_kernel(const DecodeL
 
 }  // namespace
 
-cudaError_t launch_decode_layer(const DecodeLayerArgs &a, cudaStream_t stream) {
+cudaError_t launch_decode_layer(const DecodeLayerArgs &args, cudaStream_t stream) {
+    DecodeLayerArgs a = args;
+    a.prefetch_ahead = 2 * device_sm_count();  // two CTAs per SM: one resident wave
     const size_t units = (size_t)a.batch * a.num_heads;
     if (a.out_dtype == KDA_BF16)
         decode_layer_kernel<__nv_bfloat16><<<(unsigned)units, kThreads, 0, stream>>>(a);

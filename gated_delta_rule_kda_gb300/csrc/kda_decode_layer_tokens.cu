@@ -106,6 +106,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_tokens_kernel(const 
     }
     const size_t HD = (size_t)H * kD;
     float *Su = a.S_pool + ((size_t)n * H + h) * (size_t)(kD * kD);
+    if (tid == 0 && a.prefetch_ahead > 0) {  // L2 prefetch: the state one resident wave ahead
+        const size_t u2 = blockIdx.x + (size_t)a.prefetch_ahead;
+        if (u2 < gridDim.x) {
+            const int n2 = a.slot[u2 / H];
+            if (n2 >= 0 && n2 < a.pool_size)
+                prefetch_l2(a.S_pool + ((size_t)n2 * H + u2 % H) * (size_t)(kD * kD), kD * kD * sizeof(float));
+        }
+    }
     __nv_bfloat16 *cpool = a.conv_pool + (size_t)n * 9 * HD;  // [stream][tap][H][128]
     const int row0 = warp * kRowsPerWarp;
 
@@ -277,7 +285,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_tokens_kernel(const 
 
 }  // namespace
 
-cudaError_t launch_decode_layer_tokens(const DecodeLayerTokensArgs &a, cudaStream_t stream) {
+cudaError_t launch_decode_layer_tokens(const DecodeLayerTokensArgs &args, cudaStream_t stream) {
+    DecodeLayerTokensArgs a = args;
+    a.prefetch_ahead = 2 * device_sm_count();  // two CTAs per SM: one resident wave
     const size_t units = (size_t)a.batch * a.num_heads;
     const int bytes = (int)sizeof(Smem);
     if (a.out_dtype == KDA_BF16) {

@@ -24,8 +24,6 @@
 // once per batch.  Per token: decay and the two column reductions (packed fp32x2), one
 // barrier, then every warp forms u for its own columns from the partials and applies the
 // rank-1 write; lanes 0-15 of each warp write 16 columns of o~.
-#include <atomic>
-
 #include "kda_common.cuh"
 #include "tc_primitives.cuh"
 
@@ -308,24 +306,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_tokens_kernel(con
     __syncthreads();
 }
 
-// CTAs resident at once on the current device (cached per device; a racing first call
-// stores the same value).
-int resident_ctas() {
-    constexpr int kMaxDevices = 64;
-    static std::atomic<int> cache[kMaxDevices];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
-    const int slot = dev >= 0 && dev < kMaxDevices ? dev : 0;
-    int ctas = cache[slot].load(std::memory_order_relaxed);
-    if (ctas == 0) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-            sms = 1;
-        ctas = kCtasPerSm * sms;
-        cache[slot].store(ctas, std::memory_order_relaxed);
-    }
-    return ctas;
-}
+// CTAs resident at once on the current device.
+int resident_ctas() { return kCtasPerSm * device_sm_count(); }
 
 template <typename Tin, typename Tout>
 cudaError_t launch_typed(const DecodeTokensArgs &a, cudaStream_t stream) {
