@@ -64,8 +64,8 @@ TRAFFIC = {
                 "54f1d982252df742d20d69fef22148d862218645100b056bb1c76b4558481db2",
                 (252.724992e6 + 37.786880e6) / (2048 * 96)),
     "decode": ("gated_delta_rule_kda_gb300/csrc/kda_decode.cu",
-               "9f1e6145572ad4787343166be5659867b8c38d020db25a2e19651c2bcc6a5657",
-               (205.287936e6 + 142.316800e6) / (32 * 96)),
+               "4f47ecc70fd8e33c0ec569aac50f1129b3d6081242acc9ab4771f3a7c4dbd441",
+               (205.292544e6 + 141.666816e6) / (32 * 96)),
 }
 
 
