@@ -70,7 +70,7 @@ const char *kda_status_string(kda_status status) {
     return "KDA_UNKNOWN_STATUS";
 }
 
-int32_t kda_version(void) { return 100; }
+int32_t kda_version(void) { return 200; }  // 0.2.0: snapshots, multi-token decode, decay variants, checks
 
 size_t kda_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,
                                   kda_dtype in_dtype) {
