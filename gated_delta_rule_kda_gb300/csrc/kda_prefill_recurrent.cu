@@ -7,15 +7,16 @@
 //
 // Parallel decomposition.  Value columns of the state evolve independently
 // (column c only needs k, alpha, beta and v[c]), so a (sequence, head) unit is
-// split into 4 CTAs of 32 columns.  Inside a CTA, 4 adjacent lanes share one
-// column and each holds 32 of its 128 rows in registers; the two reductions
-// over rows per token are 2-step xor shuffles.  No state ever leaves registers
+// split into 4 CTAs of 32 columns.  Inside a CTA, 8 adjacent lanes share a pair
+// of columns and each holds 16 of their 128 rows in registers (so every alpha,
+// k and q value read from shared memory serves two columns); the two reductions
+// over rows per token are 3-step xor shuffles.  No state ever leaves registers
 // until the sequence ends.
 //
 // Token inputs are staged through shared memory 16 tokens at a time; the next
 // batch is fetched into registers while the current one is processed.  Vectors
-// indexed by row are stored with 4 floats of padding after every 32 rows so that
-// the 4 row-quarters of a warp read 4 different bank groups.
+// indexed by row are stored with 4 floats of padding after every 16 rows so that
+// the 8 row groups of a warp read 8 different bank groups.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -24,11 +25,11 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kCols = 32;        // value columns per CTA
 constexpr int kSplit = kD / kCols;
-constexpr int kRows = 32;        // rows per thread
+constexpr int kRows = 16;        // rows per thread (and two columns)
 constexpr int kTB = 16;          // tokens per staged batch
-constexpr int kPadRow = kD + 16; // padded vector: 4 floats after every 32 rows
+constexpr int kPadRow = kD + 32; // padded vector: 4 floats after every 16 rows
 
-__device__ __forceinline__ int prow(int row) { return row + 4 * (row >> 5); }
+__device__ __forceinline__ int prow(int row) { return row + 4 * (row >> 4); }
 
 template <typename Tin, typename Tout, bool kCkpt, bool kHeadDecay>
 __global__ void __launch_bounds__(kThreads)
@@ -45,20 +46,20 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     __shared__ __align__(16) float s_o[kTB][kCols];
 
     const int tid = threadIdx.x;
-    const int cl = tid >> 2, rq = tid & 3;
+    const int cp = tid >> 3, rq = tid & 7;  // column pair (columns 2 cp, 2 cp + 1), row group
     const int col0 = blockIdx.x * kCols;
     const int h = blockIdx.y, n = blockIdx.z;
     const int t_begin = cu_seqlens[n], t_end = cu_seqlens[n + 1];
     const size_t state_off = ((size_t)n * H + h) * (size_t)(kD * kD);
 
-    float s[kRows];
+    float2 s[kRows];  // rows kRows rq + i, columns col0 + 2 cp + {0, 1}
     if (S0 != nullptr) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
-            s[i] = S0[state_off + (size_t)(kRows * rq + i) * kD + col0 + cl];
+            s[i] = *reinterpret_cast<const float2 *>(S0 + state_off + (size_t)(kRows * rq + i) * kD + col0 + 2 * cp);
     } else {
 #pragma unroll
-        for (int i = 0; i < kRows; ++i) s[i] = 0.f;
+        for (int i = 0; i < kRows; ++i) s[i] = make_float2(0.f, 0.f);
     }
 
     // Register prefetch buffers for one batch: 16 tokens x 3 vectors x 32 quads
@@ -123,35 +124,46 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             const float *a_row = &s_a[tt][prow(kRows * rq)];
             const float *k_row = &s_k[tt][prow(kRows * rq)];
             const float *q_row = &s_q[tt][prow(kRows * rq)];
-            // decay, then the prediction r = S^T k (this thread's 32 rows)
-            float r0 = 0.f, r1 = 0.f;
+            // decay, then the prediction r = S^T k (this thread's 16 rows, both columns)
+            float2 r = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < kRows; i += 4) {
                 const float4 a4 = *reinterpret_cast<const float4 *>(a_row + i);
                 const float4 k4 = *reinterpret_cast<const float4 *>(k_row + i);
-                s[i] *= a4.x; s[i + 1] *= a4.y; s[i + 2] *= a4.z; s[i + 3] *= a4.w;
-                r0 = fmaf(s[i], k4.x, r0); r1 = fmaf(s[i + 1], k4.y, r1);
-                r0 = fmaf(s[i + 2], k4.z, r0); r1 = fmaf(s[i + 3], k4.w, r1);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    s[i + e].x *= av[e]; s[i + e].y *= av[e];
+                    r.x = fmaf(s[i + e].x, kv[e], r.x); r.y = fmaf(s[i + e].y, kv[e], r.y);
+                }
             }
-            float r = r0 + r1;
-            r += __shfl_xor_sync(0xffffffffu, r, 1);
-            r += __shfl_xor_sync(0xffffffffu, r, 2);
-            const float u = s_b[tt] * (s_v[tt][cl] - r);
+#pragma unroll
+            for (int m = 1; m < 8; m <<= 1) {
+                r.x += __shfl_xor_sync(0xffffffffu, r.x, m);
+                r.y += __shfl_xor_sync(0xffffffffu, r.y, m);
+            }
+            const float2 v2 = *reinterpret_cast<const float2 *>(&s_v[tt][2 * cp]);
+            const float bt = s_b[tt];
+            const float u0 = bt * (v2.x - r.x), u1 = bt * (v2.y - r.y);
             // delta write, then the readout of the updated state
-            float p0 = 0.f, p1 = 0.f;
+            float2 p = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < kRows; i += 4) {
                 const float4 k4 = *reinterpret_cast<const float4 *>(k_row + i);
                 const float4 q4 = *reinterpret_cast<const float4 *>(q_row + i);
-                s[i] = fmaf(k4.x, u, s[i]); s[i + 1] = fmaf(k4.y, u, s[i + 1]);
-                s[i + 2] = fmaf(k4.z, u, s[i + 2]); s[i + 3] = fmaf(k4.w, u, s[i + 3]);
-                p0 = fmaf(s[i], q4.x, p0); p1 = fmaf(s[i + 1], q4.y, p1);
-                p0 = fmaf(s[i + 2], q4.z, p0); p1 = fmaf(s[i + 3], q4.w, p1);
+                const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    s[i + e].x = fmaf(kv[e], u0, s[i + e].x); s[i + e].y = fmaf(kv[e], u1, s[i + e].y);
+                    p.x = fmaf(s[i + e].x, qv[e], p.x); p.y = fmaf(s[i + e].y, qv[e], p.y);
+                }
             }
-            float p = p0 + p1;
-            p += __shfl_xor_sync(0xffffffffu, p, 1);
-            p += __shfl_xor_sync(0xffffffffu, p, 2);
-            if (rq == 0) s_o[tt][cl] = scale * p;
+#pragma unroll
+            for (int m = 1; m < 8; m <<= 1) {
+                p.x += __shfl_xor_sync(0xffffffffu, p.x, m);
+                p.y += __shfl_xor_sync(0xffffffffu, p.y, m);
+            }
+            if (rq == 0) *reinterpret_cast<float2 *>(&s_o[tt][2 * cp]) = make_float2(scale * p.x, scale * p.y);
             if (kCkpt) {  // snapshot after every `every` tokens of the sequence
                 const int done = t0 + tt + 1 - t_begin;
                 if (done % ckpt.every == 0) {
@@ -160,7 +172,8 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                     if (kk < ckpt.base[n + 1] - base) {
                         float *dst = ckpt.states + ((size_t)(base + kk) * H + h) * (size_t)(kD * kD);
 #pragma unroll
-                        for (int i = 0; i < kRows; ++i) dst[(size_t)(kRows * rq + i) * kD + col0 + cl] = s[i];
+                        for (int i = 0; i < kRows; ++i)
+                            *reinterpret_cast<float2 *>(dst + (size_t)(kRows * rq + i) * kD + col0 + 2 * cp) = s[i];
                     }
                 }
             }
@@ -176,7 +189,7 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     if (S_final != nullptr) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
-            S_final[state_off + (size_t)(kRows * rq + i) * kD + col0 + cl] = s[i];
+            *reinterpret_cast<float2 *>(S_final + state_off + (size_t)(kRows * rq + i) * kD + col0 + 2 * cp) = s[i];
     }
 }
 
