@@ -70,8 +70,10 @@ frontend_kernel(FrontendArgs a) {
         for (int c = 0; c < 4; ++c) wt[c] = *reinterpret_cast<const float4 *>(w + 4 * c);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            if (t - j < start) break;
-            const float4 x = load4(src[s] + ((size_t)(t - j) * H + h) * kD + c0);
+            // taps before the sequence start read as zero (predicated, so all four loads of a
+            // stream are in flight at once)
+            const float4 x = t - j >= start ? load4(src[s] + ((size_t)(t - j) * H + h) * kD + c0)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
             const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
