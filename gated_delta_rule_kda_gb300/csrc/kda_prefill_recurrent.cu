@@ -126,10 +126,12 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             const float *q_row = &s_q[tt][prow(kRows * rq)];
             // decay, then the prediction r = S^T k (this thread's 16 rows, both columns)
             float2 r = make_float2(0.f, 0.f);
+            float4 kr[kRows / 4];  // this thread's k rows, used again by the delta write
 #pragma unroll
             for (int i = 0; i < kRows; i += 4) {
                 const float4 a4 = *reinterpret_cast<const float4 *>(a_row + i);
                 const float4 k4 = *reinterpret_cast<const float4 *>(k_row + i);
+                kr[i / 4] = k4;
                 const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -149,7 +151,7 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             float2 p = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < kRows; i += 4) {
-                const float4 k4 = *reinterpret_cast<const float4 *>(k_row + i);
+                const float4 k4 = kr[i / 4];
                 const float4 q4 = *reinterpret_cast<const float4 *>(q_row + i);
                 const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
