@@ -7,32 +7,67 @@
 //
 // Parallel decomposition.  Value columns of the state evolve independently
 // (column c only needs k, alpha, beta and v[c]), so a (sequence, head) unit is
-// split into 4 CTAs of 32 columns.  Inside a CTA, 8 adjacent lanes share a pair
-// of columns and each holds 16 of their 128 rows in registers (so every alpha,
-// k and q value read from shared memory serves two columns); the two reductions
-// over rows per token are 3-step xor shuffles.  No state ever leaves registers
-// until the sequence ends.
+// split into 2 CTAs of 64 columns.  Inside a CTA, 8 adjacent lanes share a quad
+// of columns and each holds 16 of their 128 rows in registers, so every alpha,
+// k and q value read from shared memory serves four columns.  The two reductions
+// over rows per token are transposed butterflies: at each of three xor steps a
+// lane sends half of the partial sums it holds and keeps the other half, so that
+// it ends with the full sum of one column (four shuffles for four columns); u is
+// gathered back to all eight lanes in three more shuffles.  No state ever leaves
+// registers until the sequence ends.
 //
-// Token inputs are staged through shared memory 16 tokens at a time; the next
+// Token inputs are staged through shared memory 8 tokens at a time; the next
 // batch is fetched into registers while the current one is processed.  Vectors
 // indexed by row are stored with 4 floats of padding after every 16 rows so that
 // the 8 row groups of a warp read 8 different bank groups.
 #include "kda_common.cuh"
+#include "tc_primitives.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kCols = 32;        // value columns per CTA
+constexpr int kCols = 64;        // value columns per CTA
 constexpr int kSplit = kD / kCols;
-constexpr int kRows = 16;        // rows per thread (and two columns)
-constexpr int kTB = 16;          // tokens per staged batch
+constexpr int kRows = 16;        // rows per thread (and four columns)
+constexpr int kTB = 8;           // tokens per staged batch
 constexpr int kPadRow = kD + 32; // padded vector: 4 floats after every 16 rows
+constexpr int kCtasPerSm = 3;
+constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ int prow(int row) { return row + 4 * (row >> 4); }
 
+// Column of its quad whose full sum a lane holds after quad_reduce (row group rq = lane & 7).
+__device__ __forceinline__ int quad_col(int rq) { return 2 * ((rq >> 2) & 1) + ((rq >> 1) & 1); }
+
+// Sum of x (one partial sum per column of the quad) over the 8 lanes of a row-group set
+// (lanes that differ in bits 0-2): the lane returns the sum for column quad_col(rq).
+__device__ __forceinline__ float quad_reduce(float4 x, int rq) {
+    const bool hi = (rq & 4) != 0;  // keeps columns 2, 3; its partner keeps 0, 1
+    float a = hi ? x.z : x.x, b = hi ? x.w : x.y;
+    const float sa = hi ? x.x : x.z, sb = hi ? x.y : x.w;
+    a += __shfl_xor_sync(kFull, sa, 4);
+    b += __shfl_xor_sync(kFull, sb, 4);
+    const bool mid = (rq & 2) != 0;  // keeps the odd column of the pair
+    float c = mid ? b : a;
+    const float sc = mid ? a : b;
+    c += __shfl_xor_sync(kFull, sc, 2);
+    c += __shfl_xor_sync(kFull, c, 1);
+    return c;
+}
+
+// The four columns' values to every lane of the row-group set, from x held for column
+// quad_col(rq) (lanes rq and rq ^ 1 hold the same column).
+__device__ __forceinline__ float4 quad_gather(float x, int rq) {
+    const float xo = __shfl_xor_sync(kFull, x, 2);  // the other column of the pair
+    const bool mid = (rq & 2) != 0;
+    const float p0 = mid ? xo : x, p1 = mid ? x : xo;  // columns 2 hi, 2 hi + 1
+    const float o0 = __shfl_xor_sync(kFull, p0, 4), o1 = __shfl_xor_sync(kFull, p1, 4);
+    return (rq & 4) ? make_float4(o0, o1, p0, p1) : make_float4(p0, p1, o0, o1);
+}
+
 template <typename Tin, typename Tout, bool kCkpt, bool kHeadDecay>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                          const Tin *__restrict__ v, const float *__restrict__ log_alpha,
                          const float *__restrict__ beta, const float *__restrict__ S0,
@@ -46,25 +81,30 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     __shared__ __align__(16) float s_o[kTB][kCols];
 
     const int tid = threadIdx.x;
-    const int cp = tid >> 3, rq = tid & 7;  // column pair (columns 2 cp, 2 cp + 1), row group
+    const int cq = tid >> 3, rq = tid & 7;  // column quad (columns 4 cq .. 4 cq + 3), row group
+    const int jc = quad_col(rq);            // the column whose reductions this lane finishes
     const int col0 = blockIdx.x * kCols;
     const int h = blockIdx.y, n = blockIdx.z;
     const int t_begin = cu_seqlens[n], t_end = cu_seqlens[n + 1];
     const size_t state_off = ((size_t)n * H + h) * (size_t)(kD * kD);
+    // this thread's part of a [128][128] state: rows kRows rq + i, columns col0 + 4 cq ..
+    const size_t my_off = (size_t)(kRows * rq) * kD + col0 + 4 * cq;
 
-    float2 s[kRows];  // rows kRows rq + i, columns col0 + 2 cp + {0, 1}
+    float4 s[kRows];
     if (S0 != nullptr) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
-            s[i] = *reinterpret_cast<const float2 *>(S0 + state_off + (size_t)(kRows * rq + i) * kD + col0 + 2 * cp);
+            s[i] = *reinterpret_cast<const float4 *>(S0 + state_off + my_off + (size_t)i * kD);
     } else {
 #pragma unroll
-        for (int i = 0; i < kRows; ++i) s[i] = make_float2(0.f, 0.f);
+        for (int i = 0; i < kRows; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
-    // Register prefetch buffers for one batch: 16 tokens x 3 vectors x 32 quads
-    // = 1536 quads -> 12 per thread; v: 16 x 8 quads -> 1 per thread; beta: 16.
-    constexpr int kQuadsPerThread = (3 * kTB * (kD / 4)) / kThreads;  // 12
+    // Register prefetch buffers for one batch: 8 tokens x 3 vectors x 32 quads = 768
+    // quads -> 6 per thread; v: 8 tokens x 16 quads -> 1 per thread; beta: 8.
+    constexpr int kQuadsPerThread = (3 * kTB * (kD / 4)) / kThreads;  // 6
+    constexpr int kVQuads = kCols / 4;                                // 16 per token
+    static_assert(kTB * kVQuads == kThreads, "one v quad per thread");
     float4 pre[kQuadsPerThread];
     float4 pre_v;
     float pre_b = 0.f;
@@ -89,7 +129,7 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             pre[m] = x;
         }
         {
-            const int tok = tid / 8, quad = tid % 8;
+            const int tok = tid / kVQuads, quad = tid % kVQuads;
             const int t = t0 + tok;
             pre_v = t < t_end ? load4(v + ((size_t)t * H + h) * kD + col0 + 4 * quad)
                               : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -109,7 +149,7 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                                   : &s_a[tok][prow(4 * quad)];
             *reinterpret_cast<float4 *>(dst) = x;
         }
-        *reinterpret_cast<float4 *>(&s_v[tid / 8][4 * (tid % 8)]) = pre_v;
+        *reinterpret_cast<float4 *>(&s_v[tid / kVQuads][4 * (tid % kVQuads)]) = pre_v;
         if (tid < kTB) s_b[tid] = pre_b;
     };
 
@@ -124,8 +164,8 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             const float *a_row = &s_a[tt][prow(kRows * rq)];
             const float *k_row = &s_k[tt][prow(kRows * rq)];
             const float *q_row = &s_q[tt][prow(kRows * rq)];
-            // decay, then the prediction r = S^T k (this thread's 16 rows, both columns)
-            float2 r = make_float2(0.f, 0.f);
+            // decay, then the prediction r = S^T k (this thread's 16 rows, four columns)
+            float2 r01 = make_float2(0.f, 0.f), r23 = r01;
             float4 kr[kRows / 4];  // this thread's k rows, used again by the delta write
 #pragma unroll
             for (int i = 0; i < kRows; i += 4) {
@@ -135,20 +175,21 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    s[i + e].x *= av[e]; s[i + e].y *= av[e];
-                    r.x = fmaf(s[i + e].x, kv[e], r.x); r.y = fmaf(s[i + e].y, kv[e], r.y);
+                    float4 &x = s[i + e];
+                    const float2 a2 = make_float2(av[e], av[e]), k2 = make_float2(kv[e], kv[e]);
+                    const float2 x01 = tc::mul2(make_float2(x.x, x.y), a2);
+                    const float2 x23 = tc::mul2(make_float2(x.z, x.w), a2);
+                    x = make_float4(x01.x, x01.y, x23.x, x23.y);
+                    r01 = tc::fma2(x01, k2, r01);
+                    r23 = tc::fma2(x23, k2, r23);
                 }
             }
-#pragma unroll
-            for (int m = 1; m < 8; m <<= 1) {
-                r.x += __shfl_xor_sync(0xffffffffu, r.x, m);
-                r.y += __shfl_xor_sync(0xffffffffu, r.y, m);
-            }
-            const float2 v2 = *reinterpret_cast<const float2 *>(&s_v[tt][2 * cp]);
-            const float bt = s_b[tt];
-            const float u0 = bt * (v2.x - r.x), u1 = bt * (v2.y - r.y);
+            const float rj = quad_reduce(make_float4(r01.x, r01.y, r23.x, r23.y), rq);
+            const float uj = s_b[tt] * (s_v[tt][4 * cq + jc] - rj);
+            const float4 u = quad_gather(uj, rq);
             // delta write, then the readout of the updated state
-            float2 p = make_float2(0.f, 0.f);
+            float2 p01 = make_float2(0.f, 0.f), p23 = p01;
+            const float2 u01 = make_float2(u.x, u.y), u23 = make_float2(u.z, u.w);
 #pragma unroll
             for (int i = 0; i < kRows; i += 4) {
                 const float4 k4 = kr[i / 4];
@@ -156,32 +197,33 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    s[i + e].x = fmaf(kv[e], u0, s[i + e].x); s[i + e].y = fmaf(kv[e], u1, s[i + e].y);
-                    p.x = fmaf(s[i + e].x, qv[e], p.x); p.y = fmaf(s[i + e].y, qv[e], p.y);
+                    float4 &x = s[i + e];
+                    const float2 k2 = make_float2(kv[e], kv[e]), q2 = make_float2(qv[e], qv[e]);
+                    const float2 x01 = tc::fma2(k2, u01, make_float2(x.x, x.y));
+                    const float2 x23 = tc::fma2(k2, u23, make_float2(x.z, x.w));
+                    x = make_float4(x01.x, x01.y, x23.x, x23.y);
+                    p01 = tc::fma2(x01, q2, p01);
+                    p23 = tc::fma2(x23, q2, p23);
                 }
             }
-#pragma unroll
-            for (int m = 1; m < 8; m <<= 1) {
-                p.x += __shfl_xor_sync(0xffffffffu, p.x, m);
-                p.y += __shfl_xor_sync(0xffffffffu, p.y, m);
-            }
-            if (rq == 0) *reinterpret_cast<float2 *>(&s_o[tt][2 * cp]) = make_float2(scale * p.x, scale * p.y);
+            const float pj = quad_reduce(make_float4(p01.x, p01.y, p23.x, p23.y), rq);
+            if ((rq & 1) == 0) s_o[tt][4 * cq + jc] = scale * pj;
             if (kCkpt) {  // snapshot after every `every` tokens of the sequence
                 const int done = t0 + tt + 1 - t_begin;
                 if (done % ckpt.every == 0) {
                     const int kk = done / ckpt.every - 1;
                     const int base = ckpt.base[n];
                     if (kk < ckpt.base[n + 1] - base) {
-                        float *dst = ckpt.states + ((size_t)(base + kk) * H + h) * (size_t)(kD * kD);
+                        float *dst = ckpt.states + ((size_t)(base + kk) * H + h) * (size_t)(kD * kD) + my_off;
 #pragma unroll
                         for (int i = 0; i < kRows; ++i)
-                            *reinterpret_cast<float2 *>(dst + (size_t)(kRows * rq + i) * kD + col0 + 2 * cp) = s[i];
+                            *reinterpret_cast<float4 *>(dst + (size_t)i * kD) = s[i];
                     }
                 }
             }
         }
         __syncthreads();
-        // write the batch's outputs: nb tokens x 32 columns
+        // write the batch's outputs: nb tokens x 64 columns
         for (int idx = tid; idx < nb * kCols; idx += kThreads) {
             const int tok = idx / kCols, c = idx % kCols;
             Elem<Tout>::store(o + ((size_t)(t0 + tok) * H + h) * kD + col0 + c, s_o[tok][c]);
@@ -191,7 +233,7 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     if (S_final != nullptr) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
-            *reinterpret_cast<float2 *>(S_final + state_off + (size_t)(kRows * rq + i) * kD + col0 + 2 * cp) = s[i];
+            *reinterpret_cast<float4 *>(S_final + state_off + my_off + (size_t)i * kD) = s[i];
     }
 }
 
