@@ -648,6 +648,18 @@ def run_only(args, local):
         fn = lambda: kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta,
                                      inp.cu_seqlens, None, o=o, S_final=Sf)
         units = T
+    elif args.only == "prefill_fp32":
+        # the token-by-token kernel (fp32 inputs): 8 sequences x 1024 tokens (--small) or
+        # 16 x 8192, 96 heads
+        lens = [1024] * 8 if args.small else [8192] * 16
+        inp = synthetic.prefill_inputs(lens, 96, torch.float32, seed=synthetic.BASE_SEED + 1,
+                                       device=dev)
+        T = inp.q.shape[0]
+        o = torch.empty((T, 96, D), dtype=torch.float32, device=dev)
+        Sf = torch.empty((len(lens), 96, D, D), dtype=torch.float32, device=dev)
+        fn = lambda: kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta,
+                                     inp.cu_seqlens, None, o=o, S_final=Sf)
+        units = T
     elif args.only == "layer":
         lens = [2048] if args.small else synthetic.varlen_lengths(seed=synthetic.BASE_SEED + 5)
         linp = synthetic.layer_inputs(lens, 96, seed=synthetic.BASE_SEED + 5, device=dev)
@@ -705,8 +717,8 @@ def main():
                     help="skip the 131,072-token prefill leg (19 GB of inputs)")
     ap.add_argument("--skip-staged-layer-core", action="store_true",
                     help="time only the fused layer core, not the three-launch composition")
-    ap.add_argument("--only", choices=["prefill", "decode", "decode_layer", "decode_tokens",
-                                       "decode_layer_tokens", "layer"],
+    ap.add_argument("--only", choices=["prefill", "prefill_fp32", "decode", "decode_layer",
+                                       "decode_tokens", "decode_layer_tokens", "layer"],
                     default=None,
                     help="profiling aid: run just this kernel (no baseline, no e2e)")
     ap.add_argument("--small", action="store_true",

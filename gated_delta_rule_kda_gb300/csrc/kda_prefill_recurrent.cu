@@ -73,11 +73,12 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                          const float *__restrict__ beta, const float *__restrict__ S0,
                          const int32_t *__restrict__ cu_seqlens, int H, float scale,
                          Tout *__restrict__ o, float *__restrict__ S_final, const Checkpoints ckpt) {
-    __shared__ __align__(16) float s_q[kTB][kPadRow];
-    __shared__ __align__(16) float s_k[kTB][kPadRow];
-    __shared__ __align__(16) float s_a[kTB][kPadRow];
-    __shared__ __align__(16) float s_v[kTB][kCols];
-    __shared__ float s_b[kTB];
+    // Staged token inputs, double-buffered: the last token of a batch already reads the
+    // decay and key of the next batch's first token.
+    struct Batch {
+        float q[kTB][kPadRow], k[kTB][kPadRow], a[kTB][kPadRow], v[kTB][kCols], b[kTB];
+    };
+    __shared__ __align__(16) Batch sb[2];
     __shared__ __align__(16) float s_o[kTB][kCols];
 
     const int tid = threadIdx.x;
@@ -136,7 +137,7 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         }
         if (tid < kTB) pre_b = (t0 + tid < t_end) ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
     };
-    auto stash = [&]() {
+    auto stash = [&](Batch &B) {
 #pragma unroll
         for (int m = 0; m < kQuadsPerThread; ++m) {
             const int idx = tid + kThreads * m;
@@ -144,29 +145,34 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             const int tok = rem / 32, quad = rem % 32;
             float4 x = pre[m];
             if (arr == 2) x = make_float4(expf(x.x), expf(x.y), expf(x.z), expf(x.w));
-            float *dst = arr == 0 ? &s_q[tok][prow(4 * quad)]
-                       : arr == 1 ? &s_k[tok][prow(4 * quad)]
-                                  : &s_a[tok][prow(4 * quad)];
+            float *dst = arr == 0 ? &B.q[tok][prow(4 * quad)]
+                       : arr == 1 ? &B.k[tok][prow(4 * quad)]
+                                  : &B.a[tok][prow(4 * quad)];
             *reinterpret_cast<float4 *>(dst) = x;
         }
-        *reinterpret_cast<float4 *>(&s_v[tid / kVQuads][4 * (tid % kVQuads)]) = pre_v;
-        if (tid < kTB) s_b[tid] = pre_b;
+        *reinterpret_cast<float4 *>(&B.v[tid / kVQuads][4 * (tid % kVQuads)]) = pre_v;
+        if (tid < kTB) B.b[tid] = pre_b;
     };
 
-    if (t_begin < t_end) fetch(t_begin);
-    for (int t0 = t_begin; t0 < t_end; t0 += kTB) {
-        __syncthreads();  // previous batch fully consumed
-        stash();
+    // Tokens are processed in one pass over the state each: the delta write and readout of
+    // token t, then the decay and prediction of token t + 1, so the two reductions of a step
+    // run side by side.  Rows past the sequence end are staged as zeros (alpha = 1, k = 0,
+    // beta = 0), which leaves the state as it is after the last token.
+    float4 kr[kRows / 4];  // this thread's rows of the current token's k
+    float4 u = make_float4(0.f, 0.f, 0.f, 0.f);  // the current token's u, all four columns
+    // u of column jc from its prediction r (held for column jc) and token (B, tn)
+    auto u_of = [&](const Batch &B, int tn, float rj) {
+        return quad_gather(B.b[tn] * (B.v[tn][4 * cq + jc] - rj), rq);
+    };
+    if (t_begin < t_end) {
+        fetch(t_begin);
+        stash(sb[0]);
+        fetch(t_begin + kTB);
         __syncthreads();
-        if (t0 + kTB < t_end) fetch(t0 + kTB);
-        const int nb = min(kTB, t_end - t0);
-        for (int tt = 0; tt < nb; ++tt) {
-            const float *a_row = &s_a[tt][prow(kRows * rq)];
-            const float *k_row = &s_k[tt][prow(kRows * rq)];
-            const float *q_row = &s_q[tt][prow(kRows * rq)];
-            // decay, then the prediction r = S^T k (this thread's 16 rows, four columns)
+        {  // the first token: decay and prediction
+            const float *a_row = &sb[0].a[0][prow(kRows * rq)];
+            const float *k_row = &sb[0].k[0][prow(kRows * rq)];
             float2 r01 = make_float2(0.f, 0.f), r23 = r01;
-            float4 kr[kRows / 4];  // this thread's k rows, used again by the delta write
 #pragma unroll
             for (int i = 0; i < kRows; i += 4) {
                 const float4 a4 = *reinterpret_cast<const float4 *>(a_row + i);
@@ -184,19 +190,46 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                     r23 = tc::fma2(x23, k2, r23);
                 }
             }
-            const float rj = quad_reduce(make_float4(r01.x, r01.y, r23.x, r23.y), rq);
-            const float uj = s_b[tt] * (s_v[tt][4 * cq + jc] - rj);
-            const float4 u = quad_gather(uj, rq);
-            // delta write, then the readout of the updated state
-            float2 p01 = make_float2(0.f, 0.f), p23 = p01;
+            u = u_of(sb[0], 0, quad_reduce(make_float4(r01.x, r01.y, r23.x, r23.y), rq));
+        }
+    }
+    int cur = 0;
+    for (int t0 = t_begin; t0 < t_end; t0 += kTB, cur ^= 1) {
+        __syncthreads();  // the other buffer (the previous batch) and s_o are no longer read
+        stash(sb[cur ^ 1]);
+        __syncthreads();
+        fetch(t0 + 2 * kTB);
+        const int nb = min(kTB, t_end - t0);
+        for (int tt = 0; tt < nb; ++tt) {
+            const Batch &B = sb[cur];
+            const Batch &N = tt + 1 < kTB ? sb[cur] : sb[cur ^ 1];  // the next token's batch
+            const int tn = tt + 1 < kTB ? tt + 1 : 0;
+            const float *q_row = &B.q[tt][prow(kRows * rq)];
+            const float *a_row = &N.a[tn][prow(kRows * rq)];
+            const float *k_row = &N.k[tn][prow(kRows * rq)];
+            float *snap = nullptr;  // snapshot after every `every` tokens of the sequence
+            if constexpr (kCkpt) {
+                const int done = t0 + tt + 1 - t_begin;
+                if (done % ckpt.every == 0) {
+                    const int kk = done / ckpt.every - 1;
+                    const int base = ckpt.base[n];
+                    if (kk < ckpt.base[n + 1] - base)
+                        snap = ckpt.states + ((size_t)(base + kk) * H + h) * (size_t)(kD * kD) + my_off;
+                }
+            }
+            float2 p01 = make_float2(0.f, 0.f), p23 = p01, r01 = p01, r23 = p01;
             const float2 u01 = make_float2(u.x, u.y), u23 = make_float2(u.z, u.w);
 #pragma unroll
             for (int i = 0; i < kRows; i += 4) {
                 const float4 k4 = kr[i / 4];
                 const float4 q4 = *reinterpret_cast<const float4 *>(q_row + i);
+                const float4 a4 = *reinterpret_cast<const float4 *>(a_row + i);
+                const float4 n4 = *reinterpret_cast<const float4 *>(k_row + i);
+                kr[i / 4] = n4;
                 const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w}, nv[4] = {n4.x, n4.y, n4.z, n4.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
+                for (int e = 0; e < 4; ++e) {  // delta write and readout of token t
                     float4 &x = s[i + e];
                     const float2 k2 = make_float2(kv[e], kv[e]), q2 = make_float2(qv[e], qv[e]);
                     const float2 x01 = tc::fma2(k2, u01, make_float2(x.x, x.y));
@@ -205,22 +238,26 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                     p01 = tc::fma2(x01, q2, p01);
                     p23 = tc::fma2(x23, q2, p23);
                 }
-            }
-            const float pj = quad_reduce(make_float4(p01.x, p01.y, p23.x, p23.y), rq);
-            if ((rq & 1) == 0) s_o[tt][4 * cq + jc] = scale * pj;
-            if (kCkpt) {  // snapshot after every `every` tokens of the sequence
-                const int done = t0 + tt + 1 - t_begin;
-                if (done % ckpt.every == 0) {
-                    const int kk = done / ckpt.every - 1;
-                    const int base = ckpt.base[n];
-                    if (kk < ckpt.base[n + 1] - base) {
-                        float *dst = ckpt.states + ((size_t)(base + kk) * H + h) * (size_t)(kD * kD) + my_off;
+                if (kCkpt && snap != nullptr) {
 #pragma unroll
-                        for (int i = 0; i < kRows; ++i)
-                            *reinterpret_cast<float4 *>(dst + (size_t)i * kD) = s[i];
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        *reinterpret_cast<float4 *>(snap + (size_t)(i + e) * kD) = s[i + e];
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {  // decay and prediction of token t + 1
+                    float4 &x = s[i + e];
+                    const float2 a2 = make_float2(av[e], av[e]), n2 = make_float2(nv[e], nv[e]);
+                    const float2 x01 = tc::mul2(make_float2(x.x, x.y), a2);
+                    const float2 x23 = tc::mul2(make_float2(x.z, x.w), a2);
+                    x = make_float4(x01.x, x01.y, x23.x, x23.y);
+                    r01 = tc::fma2(x01, n2, r01);
+                    r23 = tc::fma2(x23, n2, r23);
                 }
             }
+            const float pj = quad_reduce(make_float4(p01.x, p01.y, p23.x, p23.y), rq);
+            const float rj = quad_reduce(make_float4(r01.x, r01.y, r23.x, r23.y), rq);
+            if ((rq & 1) == 0) s_o[tt][4 * cq + jc] = scale * pj;
+            u = u_of(N, tn, rj);
         }
         __syncthreads();
         // write the batch's outputs: nb tokens x 64 columns
