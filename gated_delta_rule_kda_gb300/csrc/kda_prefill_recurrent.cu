@@ -16,8 +16,11 @@
 // gathered back to all eight lanes in three more shuffles.  No state ever leaves
 // registers until the sequence ends.
 //
-// Token inputs are staged through shared memory 8 tokens at a time; the next
-// batch is fetched into registers while the current one is processed.  Vectors
+// Each token costs one pass over the state: the delta write and readout of
+// token t, then the decay and prediction of token t + 1.  Token inputs are
+// staged through shared memory 8 tokens at a time in two buffers (the last
+// token of a batch reads the next batch's first decay and key); the batch after
+// that is fetched into registers while the current one is processed.  Vectors
 // indexed by row are stored with 4 floats of padding after every 16 rows so that
 // the 8 row groups of a warp read 8 different bank groups.
 #include "kda_common.cuh"
