@@ -46,6 +46,16 @@ def test_oracle_scale_fp32(kda):
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_fp32_staging_batch_boundaries(kda, out_dtype):
+    """fp32 inputs (the token-by-token kernel) in one packed call over sequences of 1..17,
+    23, 24, 25 and 64 tokens: the last token falls at every position of the kernel's
+    8-token staging batches, including a last batch that ends exactly on a boundary."""
+    lens = list(range(1, 18)) + [23, 24, 25, 64]
+    inp = synthetic.prefill_inputs(lens, 3, torch.float32, seed=23, s0_std=0.1, device="cuda")
+    check(kda, inp, TOL_FP32, out_dtype)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 def test_bf16_varlen_ragged(kda, out_dtype):
     inp = synthetic.prefill_inputs([229, 64, 1, 0, 130], 4, torch.bfloat16, seed=21,
                                    s0_std=0.1, device="cuda")
