@@ -13,7 +13,8 @@
 //
 // In host code the array's name is only a host-side stand-in for the device
 // object, so the device address is obtained with cudaGetSymbolAddress, once per
-// device, on the first call made with that device current.
+// device, on the first call made with that device current.  The address is cached
+// for the life of the process and is not looked up again after a device reset.
 #include <atomic>
 
 #include "kda_common.cuh"

@@ -345,7 +345,10 @@ kda_status kda_layer_core_unbounded_decay(int32_t num_seqs, int32_t total_tokens
  *     other's results, so serialise them.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: after cudaDeviceReset (or any other teardown of the device's
+ *     primary context) it no longer names live memory, so a process that
+ *     resets a device must not call this entry point on it again.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 kda_status kda_layer_core_noalloc(int32_t num_seqs, int32_t total_tokens, int32_t num_heads,

@@ -38,3 +38,12 @@ def assert_close(gpu, ref, tol, what, out_is_bf16=False):
     assert np.isfinite(np.asarray(gpu, np.float64)).all(), f"{what}: non-finite values"
     assert e <= tol, f"{what}: max-abs/rms error {e:.3e} > {tol:.1e}"
     return e
+
+
+def assert_gated_close(gpu, ref, out_is_bf16, what="o_gated"):
+    """The gated output o^g = sigma(g) RMSNorm(o~) against the oracle with the plain bound:
+    max |gpu - oracle| / rms(oracle) <= 2e-3 over the whole tensor (plus the bf16 half-ulp
+    per element when the output is bf16).  RMSNorm divides each (token, head) row by its own
+    RMS, which could in principle magnify an error of o~ on rows of small norm; measured, the
+    errors of o~ scale with the row's own size, so no per-row allowance is needed."""
+    return assert_close(gpu, ref, TOL_BF16, what, out_is_bf16)

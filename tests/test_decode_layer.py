@@ -1,7 +1,6 @@
 """GPU decode step of the layer core over pooled states vs the fp64 oracle.
 
-The gated output is checked with the row-conditioned bound of the layer-core tests
-(RMSNorm divides each row by its own RMS); the state rows with the plain 2e-3 bound;
+The gated output and the state rows are checked with the plain 2e-3 max-abs/rms bound;
 the convolution state is bit-exact (it only moves bf16 inputs); rows of the pools
 that no request names are untouched.
 """
@@ -11,8 +10,7 @@ import torch
 
 import oracle
 from gated_delta_rule_kda_gb300 import synthetic
-from tests._parity import TOL_BF16, assert_close, to64
-from tests.test_layer_core import assert_gated_close
+from tests._parity import TOL_BF16, assert_close, assert_gated_close, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -37,26 +35,8 @@ def oracle_step(inp, heads=None):
         to64(sel(inp.qp)), to64(sel(inp.kp)), to64(sel(inp.vp)), conv_w, to64(sel(inp.z)),
         to64(inp.A)[hs], to64(inp.b)[hs], to64(sel(inp.beta_logit)), to64(sel(inp.g)), slot,
         S_pool, conv_pool)
-    # the oracle's own o~ (before the gate) for the row-conditioned bound
     return o, S_new, conv_new
 
-
-def oracle_o_tilde(inp, S_new, heads=None):
-    """o~ = S_new^T q^ / sqrt(128) per request; q^ from the oracle front end of the window."""
-    sel = (lambda t: t) if heads is None else (lambda t: t[:, heads])
-    H_all = inp.qp.shape[1]
-    hs = list(range(H_all)) if heads is None else heads
-    B = inp.qp.shape[0]
-    slot = inp.slot.cpu().numpy()
-    conv_w = to64(inp.conv_w).reshape(3, H_all, 128, 4)[:, hs].reshape(3, len(hs) * 128, 4)
-    cp = to64(inp.conv_pool)[:, :, :, hs]
-    w = np.zeros((B, 4, len(hs), 128))
-    w[:, 0], w[:, 1], w[:, 2], w[:, 3] = cp[slot, 0, 2], cp[slot, 0, 1], cp[slot, 0, 0], to64(sel(inp.qp))
-    zeros = np.zeros((4 * B, len(hs), 128))
-    qh = oracle.kda_frontend(w.reshape(4 * B, len(hs), 128), zeros, zeros, conv_w, zeros,
-                             to64(inp.A)[hs], to64(inp.b)[hs], np.zeros((4 * B, len(hs))),
-                             np.arange(0, 4 * B + 1, 4, dtype=np.int32))[0][3::4]
-    return np.einsum("bhjc,bhj->bhc", S_new[slot], qh) / np.sqrt(128.0)
 
 
 def run(kda, inp, out_dtype=torch.float32):
@@ -75,8 +55,7 @@ def test_decode_layer_small_pool(kda, out_dtype):
     o, S_pool, conv_pool = run(kda, inp, out_dtype)
     assert kda.kda_get_device_status()[0] == 0
     ref_o, ref_S, ref_conv = oracle_step(inp)
-    ot = oracle_o_tilde(inp, ref_S)
-    assert_gated_close(to64(o), ref_o, ot, out_dtype == torch.bfloat16)
+    assert_gated_close(to64(o), ref_o, out_dtype == torch.bfloat16)
     slot = inp.slot.cpu().numpy()
     assert_close(to64(S_pool)[slot], ref_S[slot], TOL_BF16, "S_pool rows")
     assert torch.equal(conv_pool.float().cpu(), torch.from_numpy(ref_conv).float()), "conv_pool"
@@ -92,8 +71,7 @@ def test_decode_layer_full_batch_sampled_heads(kda):
     assert kda.kda_get_device_status()[0] == 0
     heads = [0, 47, 95]
     ref_o, ref_S, ref_conv = oracle_step(inp, heads)
-    ot = oracle_o_tilde(inp, ref_S, heads)
-    assert_gated_close(to64(o[:, heads]), ref_o, ot, True)
+    assert_gated_close(to64(o[:, heads]), ref_o, True)
     slot = inp.slot.cpu().numpy()
     assert_close(to64(S_pool[:, heads])[slot], ref_S[slot], TOL_BF16, "S_pool rows")
     assert torch.equal(conv_pool[:, :, :, heads].float().cpu(), torch.from_numpy(ref_conv).float())
@@ -136,15 +114,9 @@ def test_decode_layer_continues_the_fused_prefill(kda):
     ref_o, ref_S = oracle.kda_layer_core(to64(inp.qp), to64(inp.kp), to64(inp.vp), to64(inp.conv_w),
                                          to64(inp.z), to64(inp.A), to64(inp.b), to64(inp.beta_logit),
                                          to64(inp.g), inp.cu_seqlens.cpu().numpy(), S0=to64(inp.S0))
-    qh, kh, vv, la, beta = oracle.kda_frontend(to64(inp.qp), to64(inp.kp), to64(inp.vp),
-                                               to64(inp.conv_w), to64(inp.z), to64(inp.A),
-                                               to64(inp.b), to64(inp.beta_logit),
-                                               inp.cu_seqlens.cpu().numpy())
-    ref_ot, _ = oracle.kda_prefill(qh, kh, vv, la, beta, inp.cu_seqlens.cpu().numpy(), S0=to64(inp.S0))
     gpu = np.stack([to64(x) for x in outs], 1)          # [2, steps, H, 128]
     want = np.stack([ref_o[cu[n] + T0[n]:cu[n] + T0[n] + steps] for n in range(2)])
-    want_ot = np.stack([ref_ot[cu[n] + T0[n]:cu[n] + T0[n] + steps] for n in range(2)])
-    assert_gated_close(gpu, want, want_ot, False)
+    assert_gated_close(gpu, want, False)
     for n in range(2):
         if T0[n] + steps == lens[n]:
             assert_close(to64(S_pool[rows[n]]), ref_S[n], TOL_BF16, "S after the last token")

@@ -1,8 +1,7 @@
 """GPU layer core for a few tokens per request from pooled states (layer-level speculative
 verify and replay) vs the fp64 oracle, through the C ABI.
 
-Gated outputs use the row-conditioned bound of the layer-core tests; state rows the plain
-2e-3 bound; convolution-state rows are bit-exact (they only move bf16 inputs); rows that no
+Gated outputs and state rows are checked with the plain 2e-3 max-abs/rms bound; convolution-state rows are bit-exact (they only move bf16 inputs); rows that no
 request advances stay bit-identical.
 """
 import numpy as np
@@ -11,8 +10,7 @@ import torch
 
 import oracle
 from gated_delta_rule_kda_gb300 import synthetic
-from tests._parity import TOL_BF16, assert_close, to64
-from tests.test_layer_core import assert_gated_close
+from tests._parity import TOL_BF16, assert_close, assert_gated_close, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +32,7 @@ def reference(inp, write_back, heads=None):
         sel(inp.qp), sel(inp.kp), sel(inp.vp), conv_w, sel(inp.z), to64(inp.A)[hs],
         to64(inp.b)[hs], sel(inp.beta_logit), sel(inp.g), inp.cu_tokens.cpu().numpy(),
         inp.slot.cpu().numpy(), to64(inp.S_pool)[:, hs], to64(inp.conv_pool)[:, :, :, hs],
-        write_back, return_o_tilde=True)
+        write_back)
 
 
 def run(kda, inp, write_back, out_dtype=torch.float32):
@@ -53,8 +51,8 @@ def test_ragged_requests_shuffled_pools(kda, out_dtype, write_back):
     inp = synthetic.decode_layer_tokens_inputs([3, 0, 1, 16, 5, 2], 3, 9, seed=91, device="cuda")
     o, S_pool, conv_pool = run(kda, inp, write_back, out_dtype)
     assert kda.kda_get_device_status()[0] == 0
-    ref_o, ref_S, ref_conv, ref_ot = reference(inp, write_back)
-    assert_gated_close(to64(o), ref_o, ref_ot, out_dtype == torch.bfloat16)
+    ref_o, ref_S, ref_conv = reference(inp, write_back)
+    assert_gated_close(to64(o), ref_o, out_dtype == torch.bfloat16)
     slot = inp.slot.cpu().numpy()
     if write_back:
         assert_close(to64(S_pool)[slot], ref_S[slot], TOL_BF16, "S_pool rows")
@@ -71,8 +69,8 @@ def test_verify_may_share_rows(kda):
     inp.slot[:] = 1
     o, S_pool, conv_pool = run(kda, inp, False)
     assert kda.kda_get_device_status()[0] == 0
-    ref_o, _, _, ref_ot = reference(inp, False)
-    assert_gated_close(to64(o), ref_o, ref_ot, False)
+    ref_o, _, _ = reference(inp, False)
+    assert_gated_close(to64(o), ref_o, False)
     assert torch.equal(S_pool, inp.S_pool) and torch.equal(conv_pool, inp.conv_pool)
 
 
@@ -127,14 +125,9 @@ def test_continues_the_fused_prefill_in_drafts(kda):
     ref_o, ref_S = oracle.kda_layer_core(to64(inp.qp), to64(inp.kp), to64(inp.vp), to64(inp.conv_w),
                                          to64(inp.z), to64(inp.A), to64(inp.b), to64(inp.beta_logit),
                                          to64(inp.g), inp.cu_seqlens.cpu().numpy(), S0=to64(inp.S0))
-    qh, kh, vv, la, beta = oracle.kda_frontend(to64(inp.qp), to64(inp.kp), to64(inp.vp),
-                                               to64(inp.conv_w), to64(inp.z), to64(inp.A),
-                                               to64(inp.b), to64(inp.beta_logit),
-                                               inp.cu_seqlens.cpu().numpy())
-    ref_ot, _ = oracle.kda_prefill(qh, kh, vv, la, beta, inp.cu_seqlens.cpu().numpy(), S0=to64(inp.S0))
     ts = sorted(got)
     gpu = np.stack([to64(got[t]) for t in ts])
-    assert_gated_close(gpu, ref_o[ts], ref_ot[ts], False)
+    assert_gated_close(gpu, ref_o[ts], False)
     for n in range(2):
         assert_close(to64(S_pool[rows[n]]), ref_S[n], TOL_BF16, "row after the last token")
 
@@ -145,8 +138,8 @@ def test_full_batch_sampled_heads(kda):
     o, S_pool, conv_pool = run(kda, inp, True, torch.bfloat16)
     assert kda.kda_get_device_status()[0] == 0
     heads = [0, 47, 95]
-    ref_o, ref_S, ref_conv, ref_ot = reference(inp, True, heads)
-    assert_gated_close(to64(o[:, heads]), ref_o, ref_ot, True)
+    ref_o, ref_S, ref_conv = reference(inp, True, heads)
+    assert_gated_close(to64(o[:, heads]), ref_o, True)
     slot = inp.slot.cpu().numpy()
     assert_close(to64(S_pool[:, heads])[slot], ref_S[slot], TOL_BF16, "S_pool rows")
     assert torch.equal(conv_pool[:, :, :, heads].float().cpu(), torch.from_numpy(ref_conv).float())
