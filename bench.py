@@ -55,18 +55,33 @@ E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the ke
 
 
 # DRAM traffic per unit (token-head for the prefill, request-head for decode) from the
-# committed ncu captures (profiles/prefill_tc_kernel_T2048_H96.md, profiles/decode_kernel_B32_H96.md),
-# taken on a smaller case and scaled by units.  Valid only for the kernel source the capture
-# was taken on: a changed kernel reports traffic null until it is captured again (a digest is
-# carried over only across edits whose compiled kernel is byte-identical: comments, host code).
+# committed ncu captures (profiles/prefill_tc_kernel_T2048_H96.md,
+# profiles/decode_traffic_B64_B128_H96.md), taken on a smaller case and scaled by units.
+# Valid only for the kernel source the capture was taken on: a changed kernel reports traffic
+# null until it is captured again (a digest is carried over only across edits whose compiled
+# kernel is byte-identical: comments, host code).
 TRAFFIC = {
     "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
                 "54f1d982252df742d20d69fef22148d862218645100b056bb1c76b4558481db2",
                 (252.724992e6 + 37.786880e6) / (2048 * 96)),
+    # decode kernels: the difference of captures at 128 and 64 requests (both above L2), so
+    # that the written lines still in L2 at the end of a launch cancel
+    # (profiles/decode_traffic_B64_B128_H96.md)
     "decode": ("gated_delta_rule_kda_gb300/csrc/kda_decode.cu",
                "4f47ecc70fd8e33c0ec569aac50f1129b3d6081242acc9ab4771f3a7c4dbd441",
-               (205.292544e6 + 141.666816e6) / (32 * 96)),
+               ((821180416 - 410643456) + (747280896 - 343196928)) / (64 * 96)),
+    "decode_layer": ("gated_delta_rule_kda_gb300/csrc/kda_decode_layer.cu",
+                     "ddc9ce806309fbe1eccc963b5e42462607fb2f0ef96d742145ab25207c53c72c",
+                     ((857602560 - 431563008) + (775423232 - 357278464)) / (64 * 96)),
+    # the layer mode of the tensor-core kernel (profiles/layer_core_kernel_T2048_H96.md)
+    "layer": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
+              "54f1d982252df742d20d69fef22148d862218645100b056bb1c76b4558481db2",
+              (252.8e6 + 37.8e6) / (2048 * 96)),
 }
+# GB300's nominal HBM3e bandwidth (NVIDIA's product figure), reported beside the measured copy
+# bandwidth: a kernel that streams a little faster than torch's copy_ reads above 1.0 of the
+# measured figure but stays below the nominal one.
+HBM_NOMINAL_GBS = 7900.0
 
 
 def traffic_bytes(kind, units):
@@ -79,6 +94,19 @@ def traffic_bytes(kind, units):
     except OSError:
         return None
     return per_unit * units
+
+
+def hbm_roofline(bytes_, launch_ms, hbm, peak_kind, kernel, traffic=None):
+    """Roofline object of an HBM-bound kernel: algorithmic bytes per launch over the mean
+    CUDA-event launch time, against the measured copy bandwidth (frac) and the nominal one."""
+    ach = bytes_ / (launch_ms / 1e3) / 1e9
+    r = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+         "traffic": traffic, "peak_kind": peak_kind, "kernel": kernel,
+         "nominal_peak": HBM_NOMINAL_GBS, "frac_of_nominal": ach / HBM_NOMINAL_GBS}
+    if ach > hbm:
+        r["note"] = ("above 1.0 of the measured peak: that peak is torch's copy_, which this "
+                     "kernel outstreams; frac_of_nominal is against the datasheet figure")
+    return r
 
 
 def peaks():
@@ -212,13 +240,13 @@ def time_launches(fn, steps, warmup, world):
     return total_ms, per
 
 
-def cpu_baseline_prefill(inp, heads, tokens):
+def cpu_baseline_prefill(inp, heads, tokens, n_threads=None):
     """The fp64 oracle as it stands, on a bounded sample of the prefill workload."""
     import numpy as np
     import oracle
     f = lambda t: t[:tokens, heads].double().cpu().numpy()
     args = [f(inp.q), f(inp.k), f(inp.v), f(inp.log_alpha), f(inp.beta)]
-    cores = oracle.default_threads()
+    cores = n_threads or oracle.default_threads()
     t = time.perf_counter()
     oracle.kda_prefill(*args, np.array([0, tokens], np.int32), n_threads=cores)
     dt = time.perf_counter() - t
@@ -468,12 +496,9 @@ def run_ours(args, world, rank, local):
     d_launch = sum(d_per) / len(d_per)
     units = 256 * 96
     d_bytes = units * DECODE_BYTES_PER_UNIT
-    d_ach = d_bytes / (d_launch / 1e3) / 1e9
     decode = {"tokens_per_s": aggregate_rate(256, d_ms, world), "ms_per_step": d_ms,
-              "roofline": {"bound": "hbm", "achieved": d_ach, "peak": hbm, "unit": "GB/s",
-                           "frac": d_ach / hbm, "traffic": traffic_bytes("decode", units),
-                           "peak_kind": peak_kind,
-                           "kernel": "kda_decode_step"}}
+              "roofline": hbm_roofline(d_bytes, d_launch, hbm, peak_kind, "kda_decode_step",
+                                       traffic_bytes("decode", units))}
     del dinp, od
     torch.cuda.empty_cache()
 
@@ -490,14 +515,13 @@ def run_ours(args, world, rank, local):
     dl_ms = max_over_ranks(dl_total / args.steps, world)
     dl_launch = sum(dl_per) / len(dl_per)
     dl_bytes = 256 * 96 * DECODE_LAYER_BYTES_PER_UNIT + 96 * DECODE_LAYER_BYTES_PER_HEAD
-    dl_ach = dl_bytes / (dl_launch / 1e3) / 1e9
     decode_layer = {"tokens_per_s": aggregate_rate(256, dl_ms, world), "ms_per_step": dl_ms,
                     "entry_point": "kda_decode_layer",
                     "workload": "256 requests x 96 heads in shuffled rows of 256-row state and "
                                 "convolution pools; front end + recurrence + gate",
-                    "roofline": {"bound": "hbm", "achieved": dl_ach, "peak": hbm, "unit": "GB/s",
-                                 "frac": dl_ach / hbm, "traffic": None, "peak_kind": peak_kind,
-                                 "kernel": "kda_decode_layer"}}
+                    "roofline": hbm_roofline(dl_bytes, dl_launch, hbm, peak_kind,
+                                             "kda_decode_layer",
+                                             traffic_bytes("decode_layer", 256 * 96))}
     del linp1, odl
     torch.cuda.empty_cache()
 
@@ -516,12 +540,11 @@ def run_ours(args, world, rank, local):
         t_ms = max_over_ranks(t_total / args.steps, world)
         t_launch = sum(t_per) / len(t_per)
         t_bytes = 256 * 96 * ((2 if wb else 1) * STATE_BYTES + ntok * DECODE_TOKENS_BYTES_PER_TOKEN)
-        t_ach = t_bytes / (t_launch / 1e3) / 1e9
         spec[mode] = {"tokens_per_s": aggregate_rate(256 * ntok, t_ms, world), "ms_per_step": t_ms,
                       "write_back": wb,
-                      "roofline": {"bound": "hbm", "achieved": t_ach, "peak": hbm, "unit": "GB/s",
-                                   "frac": t_ach / hbm, "traffic": None, "peak_kind": peak_kind,
-                                   "kernel": "kda_decode_tokens"}}
+                      "roofline": hbm_roofline(t_bytes, t_launch, hbm, peak_kind,
+                                               "kda_decode_tokens",
+                                               traffic_bytes("decode_tokens_" + mode, 256 * 96))}
     del tinp, ot
     torch.cuda.empty_cache()
 
@@ -543,13 +566,12 @@ def run_ours(args, world, rank, local):
         t_launch = sum(t_per) / len(t_per)
         per_unit = (2 if wb else 1) * (STATE_BYTES + 9 * D * 2) + ntok * LAYER_BYTES_PER_TOKEN_HEAD
         t_bytes = 256 * 96 * per_unit + 96 * DECODE_LAYER_BYTES_PER_HEAD
-        t_ach = t_bytes / (t_launch / 1e3) / 1e9
         spec_layer[mode] = {"tokens_per_s": aggregate_rate(256 * ntok, t_ms, world),
                             "ms_per_step": t_ms, "write_back": wb,
-                            "roofline": {"bound": "hbm", "achieved": t_ach, "peak": hbm,
-                                         "unit": "GB/s", "frac": t_ach / hbm, "traffic": None,
-                                         "peak_kind": peak_kind,
-                                         "kernel": "kda_decode_layer_tokens"}}
+                            "roofline": hbm_roofline(t_bytes, t_launch, hbm, peak_kind,
+                                                     "kda_decode_layer_tokens",
+                                                     traffic_bytes("decode_layer_tokens_" + mode,
+                                                                   256 * 96))}
     spec["layer"] = spec_layer
     del linp2, og2
     torch.cuda.empty_cache()
@@ -568,13 +590,20 @@ def run_ours(args, world, rank, local):
                                      o=og, S_final=Sl)
 
         l_steps = max(1, min(args.steps, 10))
-        l_total, _ = time_launches(fused_step, l_steps, args.warmup, world)
+        l_total, l_per = time_launches(fused_step, l_steps, args.warmup, world)
         l_ms = max_over_ranks(l_total / l_steps, world)
+        l_launch = sum(l_per) / len(l_per)
+        # q^p, k^p, v^p, z, g, beta_logit in, o^g out per (token, head); S_final per (sequence,
+        # head); the convolution weights and gate parameters once per head
+        l_bytes = (LT * 96 * LAYER_BYTES_PER_TOKEN_HEAD + 16 * 96 * STATE_BYTES
+                   + 96 * DECODE_LAYER_BYTES_PER_HEAD)
         layer = {"tokens_per_s": aggregate_rate(LT, l_ms, world), "ms_per_step": l_ms,
                  "tokens": LT, "workload": "16 sequences, lengths log-uniform in [1K, 64K], "
                                            "96 heads, front end + recurrence + gate",
                  "entry_point": "kda_layer_core_fused", "launches_per_step": 1,
-                 "hbm_bytes_per_token_head": LAYER_BYTES_PER_TOKEN_HEAD}
+                 "hbm_bytes_per_token_head": LAYER_BYTES_PER_TOKEN_HEAD,
+                 "roofline": hbm_roofline(l_bytes, l_launch, hbm, peak_kind,
+                                          "kda_layer_core_fused", traffic_bytes("layer", LT * 96))}
         if not args.skip_staged_layer_core:
             ws = torch.empty(kda.kda_layer_core_workspace_size(16, LT, 96), dtype=torch.uint8,
                              device=dev)
@@ -612,10 +641,15 @@ def run_ours(args, world, rank, local):
         from gated_delta_rule_kda_gb300 import synthetic as syn
         cinp = syn.workload(2, device="cpu")
         dt, head_tokens, cores = cpu_baseline_prefill(cinp, list(range(96)), 8192)
+        # one core: 12 of the 96 heads over all 8192 tokens on one thread, scaled per head
+        dt1, head_tokens1, _ = cpu_baseline_prefill(cinp, list(range(12)), 8192, n_threads=1)
         cpu = {"value": head_tokens / dt / 96.0, "unit": UNIT, "cores": cores,
                "kind": "oracle",
                "sample": f"the whole prefill workload (96 heads x 8192 tokens), {dt:.1f} s wall "
-                         f"on {cores} threads"}
+                         f"on {cores} threads",
+               "one_core": {"value": head_tokens1 / dt1 / 96.0, "unit": UNIT, "cores": 1,
+                            "sample": f"12 heads x 8192 tokens on one thread ({dt1:.1f} s), "
+                                      f"scaled to 96-head tokens"}}
 
     if rank == 0:
         line = {
@@ -669,8 +703,22 @@ def run_only(args, local):
                                               linp.A, linp.b, linp.beta_logit, linp.g,
                                               linp.cu_seqlens, None, o=og, want_state=False)
         units = LT
+    elif args.only == "staged_layer":
+        # front end -> token-by-token prefill -> gate through a workspace (kda_layer_core):
+        # 2 x 2048 tokens (--small) or workload 5's lengths, 96 heads
+        lens = [2048, 2048] if args.small else synthetic.varlen_lengths(seed=synthetic.BASE_SEED + 5)
+        linp = synthetic.layer_inputs(lens, 96, seed=synthetic.BASE_SEED + 5, device=dev)
+        LT = linp.qp.shape[0]
+        og = torch.empty((LT, 96, D), dtype=torch.bfloat16, device=dev)
+        Sl = torch.empty((len(lens), 96, D, D), dtype=torch.float32, device=dev)
+        ws = torch.empty(kda.kda_layer_core_workspace_size(len(lens), LT, 96), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: kda.kda_layer_core(linp.qp, linp.kp, linp.vp, linp.conv_w, linp.z, linp.A,
+                                        linp.b, linp.beta_logit, linp.g, linp.cu_seqlens, None,
+                                        o=og, S_final=Sl, workspace=ws)
+        units = LT
     elif args.only == "decode_layer":
-        B = 32 if args.small else 256
+        B = args.batch or (32 if args.small else 256)
         linp1 = synthetic.decode_layer_inputs(B, 96, B, device=dev)
         odl = torch.empty((B, 96, D), dtype=torch.bfloat16, device=dev)
         fn = lambda: kda.kda_decode_layer(linp1.qp, linp1.kp, linp1.vp, linp1.conv_w, linp1.z,
@@ -678,23 +726,25 @@ def run_only(args, local):
                                           linp1.S_pool, linp1.conv_pool, o=odl)
         units = B
     elif args.only == "decode_layer_tokens":
-        B = 32 if args.small else 256
+        B = args.batch or (32 if args.small else 256)
         linp2 = synthetic.decode_layer_tokens_inputs([4] * B, 96, B, device=dev)
         og2 = torch.empty((4 * B, 96, D), dtype=torch.bfloat16, device=dev)
         fn = lambda: kda.kda_decode_layer_tokens(linp2.qp, linp2.kp, linp2.vp, linp2.conv_w,
                                                  linp2.z, linp2.A, linp2.b, linp2.beta_logit,
                                                  linp2.g, linp2.cu_tokens, linp2.slot,
-                                                 linp2.S_pool, linp2.conv_pool, True, o=og2)
+                                                 linp2.S_pool, linp2.conv_pool,
+                                                 bool(args.write_back), o=og2)
         units = B
     elif args.only == "decode_tokens":
-        B = 32 if args.small else 256
+        B = args.batch or (32 if args.small else 256)
         tinp = synthetic.decode_tokens_inputs([4] * B, 96, B, device=dev)
         ot = torch.empty((4 * B, 96, D), dtype=torch.bfloat16, device=dev)
         fn = lambda: kda.kda_decode_tokens(tinp.q, tinp.k, tinp.v, tinp.log_alpha, tinp.beta,
-                                           tinp.cu_tokens, tinp.slot, tinp.S_pool, True, o=ot)
+                                           tinp.cu_tokens, tinp.slot, tinp.S_pool,
+                                           bool(args.write_back), o=ot)
         units = B
     else:
-        B = 32 if args.small else 256
+        B = args.batch or (32 if args.small else 256)
         dinp = synthetic.decode_inputs(B, 96, torch.bfloat16, device=dev)
         od = torch.empty((B, 96, D), dtype=torch.bfloat16, device=dev)
         fn = lambda: kda.kda_decode_step(dinp.q, dinp.k, dinp.v, dinp.log_alpha, dinp.beta,
@@ -718,11 +768,16 @@ def main():
     ap.add_argument("--skip-staged-layer-core", action="store_true",
                     help="time only the fused layer core, not the three-launch composition")
     ap.add_argument("--only", choices=["prefill", "prefill_fp32", "decode", "decode_layer",
-                                       "decode_tokens", "decode_layer_tokens", "layer"],
+                                       "decode_tokens", "decode_layer_tokens", "layer",
+                                       "staged_layer"],
                     default=None,
                     help="profiling aid: run just this kernel (no baseline, no e2e)")
     ap.add_argument("--small", action="store_true",
                     help="with --only: a smaller case sized for ncu captures")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="with --only and a decode kind: this many requests")
+    ap.add_argument("--write-back", type=int, default=1,
+                    help="with --only decode_tokens / decode_layer_tokens: 0 verify, 1 replay")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
