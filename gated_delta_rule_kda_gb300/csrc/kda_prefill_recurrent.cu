@@ -23,6 +23,7 @@
 // that is fetched into registers while the current one is processed.  Vectors
 // indexed by row are stored with 4 floats of padding after every 16 rows so that
 // the 8 row groups of a warp read 8 different bank groups.
+#include "kda_column_quads.cuh"
 #include "kda_common.cuh"
 #include "tc_primitives.cuh"
 
@@ -34,40 +35,12 @@ constexpr int kCols = 64;        // value columns per CTA
 constexpr int kSplit = kD / kCols;
 constexpr int kRows = 16;        // rows per thread (and four columns)
 constexpr int kTB = 8;           // tokens per staged batch
-constexpr int kPadRow = kD + 32; // padded vector: 4 floats after every 16 rows
 constexpr int kCtasPerSm = 3;
-constexpr unsigned kFull = 0xffffffffu;
-
-__device__ __forceinline__ int prow(int row) { return row + 4 * (row >> 4); }
-
-// Column of its quad whose full sum a lane holds after quad_reduce (row group rq = lane & 7).
-__device__ __forceinline__ int quad_col(int rq) { return 2 * ((rq >> 2) & 1) + ((rq >> 1) & 1); }
-
-// Sum of x (one partial sum per column of the quad) over the 8 lanes of a row-group set
-// (lanes that differ in bits 0-2): the lane returns the sum for column quad_col(rq).
-__device__ __forceinline__ float quad_reduce(float4 x, int rq) {
-    const bool hi = (rq & 4) != 0;  // keeps columns 2, 3; its partner keeps 0, 1
-    float a = hi ? x.z : x.x, b = hi ? x.w : x.y;
-    const float sa = hi ? x.x : x.z, sb = hi ? x.y : x.w;
-    a += __shfl_xor_sync(kFull, sa, 4);
-    b += __shfl_xor_sync(kFull, sb, 4);
-    const bool mid = (rq & 2) != 0;  // keeps the odd column of the pair
-    float c = mid ? b : a;
-    const float sc = mid ? a : b;
-    c += __shfl_xor_sync(kFull, sc, 2);
-    c += __shfl_xor_sync(kFull, c, 1);
-    return c;
-}
-
-// The four columns' values to every lane of the row-group set, from x held for column
-// quad_col(rq) (lanes rq and rq ^ 1 hold the same column).
-__device__ __forceinline__ float4 quad_gather(float x, int rq) {
-    const float xo = __shfl_xor_sync(kFull, x, 2);  // the other column of the pair
-    const bool mid = (rq & 2) != 0;
-    const float p0 = mid ? xo : x, p1 = mid ? x : xo;  // columns 2 hi, 2 hi + 1
-    const float o0 = __shfl_xor_sync(kFull, p0, 4), o1 = __shfl_xor_sync(kFull, p1, 4);
-    return (rq & 4) ? make_float4(o0, o1, p0, p1) : make_float4(p0, p1, o0, o1);
-}
+using quads::kPadRow;
+using quads::prow;
+using quads::quad_col;
+using quads::quad_gather;
+using quads::quad_reduce;
 
 template <typename Tin, typename Tout, bool kCkpt, bool kHeadDecay>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
