@@ -66,6 +66,7 @@
 // -5 sigmoid(e^A (z + b)) and beta = sigmoid(beta_logit).  v is then fp32, so it
 // enters M2 as hi + lo like every other operand.  The chain group's readout
 // applies the output gate sigmoid(g) * RMSNorm(o~) per (token, head) row.
+#include <atomic>
 #include <cuda.h>
 #include <cstring>
 #include <cudaTypedefs.h>
@@ -166,6 +167,10 @@ struct Params {
     const float *conv_w, *A, *b;
     float l2_eps, rms_eps;
     Checkpoints ckpt;  // read only by the instantiation that takes snapshots
+    // Test-only fault injection, read only by the debug library (KDA_DEBUG): the prep group
+    // skips its first "slot full" hand-off, and every wait gives up after wait_ns.
+    int32_t skip_first_full;
+    uint64_t wait_ns;
 };
 
 // 1 / (1 + 2^(-x log2 e)) on the SFU: ex2.approx and rcp.approx, each within about
@@ -231,10 +236,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 // Bounded wait by one thread; a timeout is recorded with `where`.
-__device__ __forceinline__ bool wait_one(uint64_t *bar, uint32_t parity, DeviceStatus st,
+__device__ __forceinline__ bool wait_one(uint64_t *bar, uint32_t parity, const Params &p,
                                          uint32_t where) {
-    const bool ok = mbar_wait_bounded(bar, parity, kWaitNs);
-    if (!ok) record_status(st, KDA_ERR_DEVICE_TIMEOUT, where);
+#ifdef KDA_DEBUG
+    const uint64_t limit = p.wait_ns;
+#else
+    const uint64_t limit = kWaitNs;
+#endif
+    const bool ok = mbar_wait_bounded(bar, parity, limit);
+    if (!ok) record_status(p.status, KDA_ERR_DEVICE_TIMEOUT, where);
     return ok;
 }
 // Operand writes (generic-proxy smem stores and tcgen05.st) -> visible to an MMA
@@ -385,8 +395,8 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         {
             bool ok = true;
             if (tid == kPA && c >= 2)
-                ok = wait_one(bar + B_EMPTY + s, ((c >> 1) - 1) & 1, p.status, 10);
-            if (tid == kTmaThread) ok = wait_one(bar + B_TQKV + s, (c >> 1) & 1, p.status, 11);
+                ok = wait_one(bar + B_EMPTY + s, ((c >> 1) - 1) & 1, p, 10);
+            if (tid == kTmaThread) ok = wait_one(bar + B_TQKV + s, (c >> 1) & 1, p, 11);
             if (pt < kC) cp_async_wait_all();
             if constexpr (kLayer) {  // beta = sigmoid(beta_logit); rows past the end write nothing
                 if (pt < kC)
@@ -624,7 +634,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         if (c + 1 < nchunks) {  // stage chunk c+1 into slot s^1 once chunk c-1 no longer needs it
             bool ok = true;
             if (tid == kTmaThread && c >= 1)
-                ok = wait_one(bar + B_VFREE + (s ^ 1), ((c - 1) >> 1) & 1, p.status, 12);
+                ok = wait_one(bar + B_VFREE + (s ^ 1), ((c - 1) >> 1) & 1, p, 12);
             alive = group_and(kPrepBar, ok);
             if (!alive) break;
             issue_loads<kLayer>(p, sm, bar, s ^ 1, t0 + kC, min(kC, t_end - t0 - kC), h, tid, true);
@@ -702,7 +712,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         {
             bool ok = true;
             if (tid == kPA || tid == kPB)
-                ok = wait_one(bar + (tid == kPA ? B_PA : B_PB), ph & 1, p.status, 13);
+                ok = wait_one(bar + (tid == kPA ? B_PA : B_PB), ph & 1, p, 13);
             ++ph;
             alive = group_and(kPrepBar, ok);
             fence_after_sync();
@@ -804,7 +814,11 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         }
         fence_proxy_async_smem();  // wq, P and Tb are MMA operands of the chain group
         group_sync(kPrepBar);
+#ifdef KDA_DEBUG
+        if (tid == kPA && !(p.skip_first_full && c == 0)) mbar_arrive(bar + B_FULL + s);
+#else
         if (tid == kPA) mbar_arrive(bar + B_FULL + s);
+#endif
     }
 
     if (pt < kC) cp_async_wait_all();  // nothing may still be in flight into shared memory
@@ -911,7 +925,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
         // ---- the prep group has filled slot s ----
         {
             bool ok = true;
-            if (tid == 0) ok = wait_one(bar + B_FULL + s, (c >> 1) & 1, p.status, 20);
+            if (tid == 0) ok = wait_one(bar + B_FULL + s, (c >> 1) & 1, p, 20);
             alive = group_and(kChainBar, ok);
             fence_after_sync();
             if (!alive) break;
@@ -966,7 +980,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
                     if (part == 1 && (tid == kCA || tid == kCB)) {
-                        m2_ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p.status, 24);
+                        m2_ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p, 24);
                         if (m2_ok && tid == kCA) mbar_arrive(bar + B_VFREE + s);
                     }
                     const int j0 = 32 * part;
@@ -1057,7 +1071,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
         {
             bool ok = true;
             if (tid == kCA || tid == kCB)
-                ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p.status, 21);
+                ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p, 21);
             ++ph;
             alive = group_and(kChainBar, ok);
             fence_after_sync();
@@ -1115,7 +1129,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
         {
             bool ok = true;
             if (tid == kCA || tid == kCB)
-                ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p.status, 22);
+                ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p, 22);
             ++ph;
             fence_before_sync();
             alive = group_and(kChainBar, ok);
@@ -1148,7 +1162,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                 float *gate = reinterpret_cast<float *>(sm + S_GATE);
                 gate[warp * 32 + (c_lane & 31)] = b[0];
                 bool ok = true;
-                if (tid == 0) ok = wait_one(bar + B_TG, c & 1, p.status, 25);  // chunk c's g tile
+                if (tid == 0) ok = wait_one(bar + B_TG, c & 1, p, 25);  // chunk c's g tile
                 ok = group_and(kChainBar, ok);
                 if (!ok) {
                     alive = false;
@@ -1332,10 +1346,22 @@ cudaError_t launch_params(const Params &p, int num_seqs, int num_heads, cudaStre
     return launch_kernel<Tout, kLayer, false, kHeadDecay>(p, num_seqs, num_heads, stream);
 }
 
+#ifdef KDA_DEBUG
+// Armed by kda_debug_inject_handoff_timeout, consumed by the next prefill launch.
+std::atomic<int> g_inject_handoff_timeout{0};
+#endif
+
 template <typename Tout>
 cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
     Params p;
     memset(&p, 0, sizeof(p));
+    p.wait_ns = kWaitNs;
+#ifdef KDA_DEBUG
+    if (g_inject_handoff_timeout.exchange(0) != 0) {
+        p.skip_first_full = 1;
+        p.wait_ns = 1000000ull;  // 1 ms
+    }
+#endif
     if (a.total_tokens > 0) {
         const int T = a.total_tokens, H = a.num_heads;
         if (!encode_bf16_tiles(&p.tm_q, a.q, T, H, kC) || !encode_bf16_tiles(&p.tm_k, a.k, T, H, kC) ||
@@ -1360,6 +1386,7 @@ template <typename Tout>
 cudaError_t launch_layer_typed(const LayerArgs &a, cudaStream_t stream) {
     Params p;
     memset(&p, 0, sizeof(p));
+    p.wait_ns = kWaitNs;
     if (a.total_tokens > 0) {
         const int T = a.total_tokens, H = a.num_heads;
         if (!encode_bf16_tiles(&p.tm_q, a.qp, T, H, kC) || !encode_bf16_tiles(&p.tm_k, a.kp, T, H, kC) ||
@@ -1401,3 +1428,12 @@ cudaError_t launch_layer_tc(const LayerArgs &a, cudaStream_t stream) {
 }
 
 }  // namespace kda
+
+extern "C" kda_status kda_debug_inject_handoff_timeout(void) {
+#ifdef KDA_DEBUG
+    kda::g_inject_handoff_timeout.store(1);
+    return KDA_OK;
+#else
+    return KDA_ERR_UNSUPPORTED;
+#endif
+}

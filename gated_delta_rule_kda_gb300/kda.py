@@ -58,6 +58,7 @@ EXPORTED = (
     "kda_decode_layer_tokens",
     "kda_check_prefill_inputs",
     "kda_get_device_status",
+    "kda_debug_inject_handoff_timeout",
 )
 
 # Capacity of the fixed scratch array behind kda_layer_core_noalloc (include/kda.h).
@@ -135,6 +136,8 @@ def _load() -> ctypes.CDLL:
     lib.kda_check_prefill_inputs.restype = ctypes.c_int
     lib.kda_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
     lib.kda_get_device_status.restype = ctypes.c_int
+    lib.kda_debug_inject_handoff_timeout.argtypes = []
+    lib.kda_debug_inject_handoff_timeout.restype = ctypes.c_int
     return lib
 
 

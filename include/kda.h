@@ -575,6 +575,28 @@ kda_status kda_check_prefill_inputs(int32_t num_seqs, int32_t total_tokens, int3
  */
 kda_status kda_get_device_status(void *stream, uint32_t *detail);
 
+/*
+ * kda_debug_inject_handoff_timeout - test-only fault injection that lets a test
+ * check, on a GPU, that a device-side wait which runs out is reported through
+ * the status word and leaves the context usable.  The pages have no counterpart:
+ * this is failure-detection plumbing.
+ *
+ * In a library built with KDA_DEBUG defined it arms the NEXT launch of the
+ * tensor-core prefill (kda_prefill, kda_prefill_with_checkpoints and
+ * kda_prefill_head_decay with bf16 inputs).  In that launch the warps that build
+ * each chunk's operands skip their first "chunk ready" hand-off (nothing has been
+ * issued into that chunk's slot by then), and every wait of the launch gives up
+ * after 1 ms instead of 2 s.  The warps that consume the chunk give up waiting
+ * for it, the launch leaves without writing its results, and
+ * kda_get_device_status reports KDA_ERR_DEVICE_TIMEOUT with detail 20 (the wait
+ * for a ready chunk).  A sequence of two chunks (33 to 64 tokens) keeps that the
+ * only wait that runs out.  Later launches are unaffected.
+ * The normal library arms nothing and returns KDA_ERR_UNSUPPORTED.  The armed
+ * state is shared by the process: do not call it while other threads launch
+ * prefills.
+ */
+kda_status kda_debug_inject_handoff_timeout(void);
+
 #ifdef __cplusplus
 }
 #endif
