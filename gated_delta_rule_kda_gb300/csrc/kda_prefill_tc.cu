@@ -977,15 +977,22 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             const float *e31p = vec + 2 * kD + s * kD;
             auto f4 = [&](auto with_snapshot, float *snap) {
                 constexpr bool kSnap = decltype(with_snapshot)::value;
+                // the state's columns 32 part .. 32 part + 31; the next part's load is in flight
+                // while this part is split and stored
+                uint32_t sr[2][32];
+                tmem_ld32_async(tl + TM_ST, sr[0]);
+                tmem_ld_wait32(sr[0]);
 #pragma unroll
                 for (int part = 0; part < 4; ++part) {
+                    if (part < 3) tmem_ld32_async(tl + TM_ST + 32 * (part + 1), sr[(part + 1) & 1]);
                     if (part == 1 && (tid == kCA || tid == kCB)) {
                         m2_ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p, 24);
                         if (m2_ok && tid == kCA) mbar_arrive(bar + B_VFREE + s);
                     }
                     const int j0 = 32 * part;
                     float sv[32];
-                    tmem_ld32(tl + TM_ST + j0, sv);
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) sv[jj] = __uint_as_float(sr[part & 1][jj]);
                     uint32_t hw[16], lw[16], yv[32];
 #pragma unroll
                     for (int jj = 0; jj < 32; jj += 4) {
@@ -1010,6 +1017,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                     tmem_st16u(tl + TM_OPS + (j0 >> 1), hw);
                     tmem_st16u(tl + TM_OPS + 64 + (j0 >> 1), lw);
                     tmem_st32(tl + TM_ST + j0, yv);
+                    if (part < 3) tmem_ld_wait32(sr[(part + 1) & 1]);
                 }
             };
             // The entering state S0 is the state after kC c tokens: a snapshot when that is a
