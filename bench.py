@@ -62,8 +62,8 @@ E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the ke
 # kernel is byte-identical: comments, host code).
 TRAFFIC = {
     "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-                "54f1d982252df742d20d69fef22148d862218645100b056bb1c76b4558481db2",
-                (252.724992e6 + 37.786880e6) / (2048 * 96)),
+                "d6becad1ebccd60a22b30ba7e9e1a4baf5c0fc38899fd7e4dc44d633e73e8f7a",
+                (252.5568e6 + 37.706752e6) / (2048 * 96)),
     # decode kernels: the difference of captures at 128 and 64 requests (both above L2), so
     # that the written lines still in L2 at the end of a launch cancel
     # (profiles/decode_traffic_B64_B128_H96.md)
@@ -73,10 +73,24 @@ TRAFFIC = {
     "decode_layer": ("gated_delta_rule_kda_gb300/csrc/kda_decode_layer.cu",
                      "ddc9ce806309fbe1eccc963b5e42462607fb2f0ef96d742145ab25207c53c72c",
                      ((857602560 - 431563008) + (775423232 - 357278464)) / (64 * 96)),
+    # a few tokens per request (4, the bench leg's draft), same difference method
+    # (profiles/decode_tokens_traffic_B64_B128_H96.md)
+    "decode_tokens_verify": ("gated_delta_rule_kda_gb300/csrc/kda_decode_tokens.cu",
+                             "85e8a08ee610b59f11a965b8d2397b2e6fe9844ffd3524b82120926693c439d2",
+                             ((868478464 - 434237952) + (14044416 - 7197952)) / (64 * 96)),
+    "decode_tokens_replay": ("gated_delta_rule_kda_gb300/csrc/kda_decode_tokens.cu",
+                             "85e8a08ee610b59f11a965b8d2397b2e6fe9844ffd3524b82120926693c439d2",
+                             ((868482304 - 434240768) + (755365120 - 346715392)) / (64 * 96)),
+    "decode_layer_tokens_verify": ("gated_delta_rule_kda_gb300/csrc/kda_decode_layer_tokens.cu",
+                                   "e83fc7ca81254769df6bb07fa8f05a1b7e38552aa3dd2833214bb34876169960",
+                                   ((897444352 - 449020160) + (12886016 - 5880064)) / (64 * 96)),
+    "decode_layer_tokens_replay": ("gated_delta_rule_kda_gb300/csrc/kda_decode_layer_tokens.cu",
+                                   "e83fc7ca81254769df6bb07fa8f05a1b7e38552aa3dd2833214bb34876169960",
+                                   ((903500288 - 451118336) + (784547584 - 361533952)) / (64 * 96)),
     # the layer mode of the tensor-core kernel (profiles/layer_core_kernel_T2048_H96.md)
     "layer": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-              "54f1d982252df742d20d69fef22148d862218645100b056bb1c76b4558481db2",
-              (252.8e6 + 37.8e6) / (2048 * 96)),
+              "d6becad1ebccd60a22b30ba7e9e1a4baf5c0fc38899fd7e4dc44d633e73e8f7a",
+              (253.040896e6 + 37.804544e6) / (2048 * 96)),
 }
 # GB300's nominal HBM3e bandwidth (NVIDIA's product figure), reported beside the measured copy
 # bandwidth: a kernel that streams a little faster than torch's copy_ reads above 1.0 of the
