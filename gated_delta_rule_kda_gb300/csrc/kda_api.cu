@@ -94,7 +94,7 @@ namespace {
 // kda_prefill in full: per-channel decay ([T][H][128]) or one decay per (token, head) ([T][H]).
 kda_status prefill_impl(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
                         int32_t total_tokens, int32_t num_heads, const void *q, const void *k,
-                        const void *v, const float *log_alpha, bool head_decay, bool recurrent,
+                        const void *v, const float *log_alpha, bool head_decay, bool unbounded,
                         const float *beta,
                         const float *S0, const int32_t *cu_seqlens, float scale, void *o,
                         float *S_final, void *workspace, size_t workspace_bytes,
@@ -119,8 +119,8 @@ kda_status prefill_impl(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seq
         return KDA_ERR_WORKSPACE;
 
 #ifdef KDA_DEBUG
-    // debug builds: the contents checks run before every prefill
-    {
+    // debug builds: the contents checks run before every prefill with the decay floor
+    if (!unbounded) {
         CheckArgs c{num_seqs, total_tokens, num_heads, head_decay ? 1 : 0,
                     total_tokens > 0 ? log_alpha : nullptr, cu_seqlens, device_status()};
         if (launch_check_prefill(c, static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -135,10 +135,11 @@ kda_status prefill_impl(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seq
     a.workspace = workspace; a.workspace_bytes = workspace_bytes;
     a.ckpt = Checkpoints{ckpt_every, ckpt_base, ckpt_states};
     a.head_decay = head_decay ? 1 : 0;
-    a.recurrent = recurrent ? 1 : 0;
+    a.unbounded = unbounded ? 1 : 0;
     a.status = device_status();
-    // bf16 inputs: chunked tensor-core kernel; fp32 inputs (or any decay): the recurrent kernel.
-    if (in_dtype == KDA_BF16 && !recurrent)
+    // bf16 inputs: chunked tensor-core kernel (without the floor, chunks out of its range run
+    // token by token inside it); fp32 inputs: the token-by-token kernel, exact for any decay.
+    if (in_dtype == KDA_BF16)
         return from_cuda(launch_prefill_tc(a, static_cast<cudaStream_t>(stream)));
     return from_cuda(launch_prefill_recurrent(a, static_cast<cudaStream_t>(stream)));
 }
@@ -348,9 +349,10 @@ kda_status layer_core_impl(int32_t num_seqs, int32_t total_tokens, int32_t num_h
                                   beta_logit, cu_seqlens, l2_eps, KDA_FP32, q_hat, k_hat, v_out,
                                   log_alpha, beta, unbounded_decay, stream);
     if (st != KDA_OK) return st;
-    st = kda_prefill(KDA_FP32, KDA_FP32, num_seqs, total_tokens, num_heads, q_hat, k_hat, v_out,
-                     log_alpha, beta, S0, cu_seqlens, scale, o_tilde, S_final, pre_ws,
-                     pre_ws_bytes, stream);
+    // (the unbounded gate has no decay floor: its prefill skips the debug contents checks)
+    st = (unbounded_decay ? kda_prefill_unbounded_decay : kda_prefill)(
+        KDA_FP32, KDA_FP32, num_seqs, total_tokens, num_heads, q_hat, k_hat, v_out, log_alpha,
+        beta, S0, cu_seqlens, scale, o_tilde, S_final, pre_ws, pre_ws_bytes, stream);
     if (st != KDA_OK) return st;
     return kda_output_gate((int64_t)rows, KDA_FP32, o_tilde, g, rms_eps, out_dtype, o_gated,
                            stream);
@@ -396,12 +398,13 @@ kda_status kda_layer_core_fused(int32_t num_seqs, int32_t total_tokens, int32_t 
                                                  0, nullptr, nullptr, stream);
 }
 
-kda_status kda_layer_core_fused_with_checkpoints(
+static kda_status layer_core_fused_impl(
     int32_t num_seqs, int32_t total_tokens, int32_t num_heads, const void *qp, const void *kp,
     const void *vp, const float *conv_w, const void *z, const float *A, const float *b,
     const void *beta_logit, const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
     float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated, float *S_final,
-    int32_t ckpt_every, const int32_t *ckpt_base, float *ckpt_states, void *stream) {
+    int32_t ckpt_every, const int32_t *ckpt_base, float *ckpt_states, bool unbounded,
+    void *stream) {
     if (!ok_dtype(out_dtype)) return KDA_ERR_INVALID_ARGUMENT;
     if (!ok_checkpoints(ckpt_every, ckpt_base, ckpt_states)) return KDA_ERR_INVALID_ARGUMENT;
     if (num_seqs < 1 || total_tokens < 0 || num_heads < 1) return KDA_ERR_INVALID_ARGUMENT;
@@ -429,8 +432,31 @@ kda_status kda_layer_core_fused_with_checkpoints(
     a.scale = scale; a.l2_eps = l2_eps; a.rms_eps = rms_eps;
     a.out_dtype = out_dtype; a.o = o_gated; a.S_final = S_final;
     a.ckpt = Checkpoints{ckpt_every, ckpt_base, ckpt_states};
+    a.unbounded_decay = unbounded ? 1 : 0;
     a.status = device_status();
     return from_cuda(launch_layer_tc(a, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status kda_layer_core_fused_with_checkpoints(
+    int32_t num_seqs, int32_t total_tokens, int32_t num_heads, const void *qp, const void *kp,
+    const void *vp, const float *conv_w, const void *z, const float *A, const float *b,
+    const void *beta_logit, const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
+    float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated, float *S_final,
+    int32_t ckpt_every, const int32_t *ckpt_base, float *ckpt_states, void *stream) {
+    return layer_core_fused_impl(num_seqs, total_tokens, num_heads, qp, kp, vp, conv_w, z, A, b,
+                                 beta_logit, g, cu_seqlens, S0, scale, l2_eps, rms_eps, out_dtype,
+                                 o_gated, S_final, ckpt_every, ckpt_base, ckpt_states, false,
+                                 stream);
+}
+
+kda_status kda_layer_core_fused_unbounded_decay(
+    int32_t num_seqs, int32_t total_tokens, int32_t num_heads, const void *qp, const void *kp,
+    const void *vp, const float *conv_w, const void *z, const float *A, const float *b,
+    const void *beta_logit, const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
+    float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated, float *S_final, void *stream) {
+    return layer_core_fused_impl(num_seqs, total_tokens, num_heads, qp, kp, vp, conv_w, z, A, b,
+                                 beta_logit, g, cu_seqlens, S0, scale, l2_eps, rms_eps, out_dtype,
+                                 o_gated, S_final, 0, nullptr, nullptr, true, stream);
 }
 
 kda_status kda_decode_layer(int32_t batch, int32_t num_heads, int32_t pool_size,

@@ -177,7 +177,8 @@ struct PrefillArgs {
     size_t workspace_bytes;
     Checkpoints ckpt;
     int32_t head_decay;  // 1: log_alpha is [T][H], one decay per (token, head)
-    int32_t recurrent;   // 1: the token-by-token kernel whatever the input type (any decay <= 0)
+    int32_t unbounded;   // 1: any decay <= 0 (no -5 floor): chunks out of the tensor-core range
+                         //    run token by token; fp32 inputs run the token-by-token kernel
     DeviceStatus status;
 };
 
@@ -213,6 +214,7 @@ struct LayerArgs {
     void *o;
     float *S_final;
     Checkpoints ckpt;
+    int32_t unbounded_decay;  // 1: log_alpha = -e^A softplus(z + b) (no floor), chunk fallback
     DeviceStatus status;
 };
 

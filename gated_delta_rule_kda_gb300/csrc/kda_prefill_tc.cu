@@ -181,6 +181,8 @@ __device__ __forceinline__ float sigmoid_(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
     return r;
 }
+// log(1 + e^x); above 20 it equals x to fp32 precision (Kimi Linear's decay gate).
+__device__ __forceinline__ float softplus_(float x) { return x > 20.f ? x : log1pf(expf(x)); }
 __device__ __forceinline__ void bf16x4_to_f32(uint2 u, float (&x)[4]) {
     x[0] = __uint_as_float(u.x << 16);
     x[1] = __uint_as_float(u.x & 0xFFFF0000u);
@@ -342,7 +344,7 @@ __device__ __forceinline__ void load_gate_inputs(const Params &p, int t0, int nr
 // ============================================================================
 // Prep group (warps 4-11, 256 threads): operands of every chunk, in order.
 // ============================================================================
-template <bool kLayer, bool kHeadDecay>
+template <bool kLayer, bool kHeadDecay, bool kUnb>
 __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, uint32_t tb,
                                            int h, int t_begin, int t_end, int nchunks) {
     const int tid = threadIdx.x, pt = tid - 128, lane = tid & 31;
@@ -390,6 +392,9 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         unsigned char *pp = sm + S_P + s * P_SIZE;
         float *em_s = vec + s * kD, *e31p_s = vec + 2 * kD + s * kD, *e31_s = vec + 4 * kD + s * kD;
         float *sT = sT_base + s * (32 * kLdT);
+        // kUnb: the chunk takes the tensor-core form (every decay factor in range) or is handed
+        // to the chain group to run token by token
+        bool fast = true;
 
         // ---- slot s free again (chunk c-2 finished); chunk c's inputs landed ----
         {
@@ -505,16 +510,24 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                     *reinterpret_cast<uint2 *>(qkvw + VO + tile_chunk(32, r, cc) + hb) = h2;
                     *reinterpret_cast<uint2 *>(qkvw + QO + tile_chunk(32, r, cc) + hb) = l2;
                 }
-                // ---- log alpha = -5 sigmoid(e^A (z + b)) (rows past the end: 0) ----
+                // ---- log alpha = -5 sigmoid(e^A (z + b)), or with kUnb Kimi Linear's
+                //      -e^A softplus(z + b) (rows past the end: 0) ----
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     float zf[4];
                     bf16x4_to_f32(zr[k], zf);
                     const bool in = 4 * rg + k < nrow;
-                    la[k].x = in ? -5.f * sigmoid_(eA * (zf[0] + bb.x)) : 0.f;
-                    la[k].y = in ? -5.f * sigmoid_(eA * (zf[1] + bb.y)) : 0.f;
-                    la[k].z = in ? -5.f * sigmoid_(eA * (zf[2] + bb.z)) : 0.f;
-                    la[k].w = in ? -5.f * sigmoid_(eA * (zf[3] + bb.w)) : 0.f;
+                    if constexpr (kUnb) {
+                        la[k].x = in ? -eA * softplus_(zf[0] + bb.x) : 0.f;
+                        la[k].y = in ? -eA * softplus_(zf[1] + bb.y) : 0.f;
+                        la[k].z = in ? -eA * softplus_(zf[2] + bb.z) : 0.f;
+                        la[k].w = in ? -eA * softplus_(zf[3] + bb.w) : 0.f;
+                    } else {
+                        la[k].x = in ? -5.f * sigmoid_(eA * (zf[0] + bb.x)) : 0.f;
+                        la[k].y = in ? -5.f * sigmoid_(eA * (zf[1] + bb.y)) : 0.f;
+                        la[k].z = in ? -5.f * sigmoid_(eA * (zf[2] + bb.z)) : 0.f;
+                        la[k].w = in ? -5.f * sigmoid_(eA * (zf[3] + bb.w)) : 0.f;
+                    }
                 }
             }
             const float kL2E = 1.4426950408889634f;
@@ -557,9 +570,23 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             base.w = incl.w - acc.w - (rg < 4 ? mid.w : 0.f);
             const float em4[4] = {ex2_approx(mid.x), ex2_approx(mid.y), ex2_approx(mid.z),
                                   ex2_approx(mid.w)};
+            if constexpr (kUnb) {
+                // Without the decay floor the chunk takes the tensor-core form only when every
+                // factor 2^{+-D} stays inside 2^115 (about e^80, the range the floor guarantees);
+                // otherwise (a decay of -inf included) the chain group runs it token by token.
+                bool ok = true;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    ok = ok && fabsf(base.x + pre[k].x) <= 115.f && fabsf(base.y + pre[k].y) <= 115.f &&
+                         fabsf(base.z + pre[k].z) <= 115.f && fabsf(base.w + pre[k].w) <= 115.f;
+                fast = group_and(kPrepBar, ok);
+            }
+            const float4 e31_entering = e31_prev;  // rows of row group 0 hold the true value
             if (rg == 0) {
-                const float4 e31 = make_float4(ex2_approx(last.x), ex2_approx(last.y),
-                                               ex2_approx(last.z), ex2_approx(last.w));
+                // a chunk run token by token leaves the state unscaled: e31 = 1
+                const float4 e31 = fast ? make_float4(ex2_approx(last.x), ex2_approx(last.y),
+                                                      ex2_approx(last.z), ex2_approx(last.w))
+                                        : make_float4(1.f, 1.f, 1.f, 1.f);
                 *reinterpret_cast<float4 *>(em_s + 4 * q4) =
                     make_float4(em4[0], em4[1], em4[2], em4[3]);
                 *reinterpret_cast<float4 *>(e31p_s + 4 * q4) = e31_prev;
@@ -569,6 +596,37 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             // Row order: threads with bit 1 of rg set take their rows in the order 2, 3, 0, 1,
             // so that the four rows a half-warp stores at once (8-byte accesses are served a
             // half-warp at a time) fall in four distinct 32-byte bank groups of the swizzled tile.
+            if (kUnb && !fast) {
+                // Out of range: raw k, q (fp32) into slot s's [W ; Q~] tile and alpha (fp32; row 0
+                // times the entering state's scale e31) into its R tile, [32][128] each, for the
+                // chain group's token-by-token pass.  Nothing else of the chunk is built.
+                float *kf = reinterpret_cast<float *>(wq), *qf = kf + kC * kD;
+                float *af = reinterpret_cast<float *>(rr);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 4 * rg + k;
+                    float kv[4], qv[4];
+                    if constexpr (kLayer) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            kv[e] = kh[k][e];
+                            qv[e] = qh[k][e];
+                        }
+                    } else {
+                        bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + KO + tile_chunk(32, r, cc) + hb), kv);
+                        bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + QO + tile_chunk(32, r, cc) + hb), qv);
+                    }
+                    float4 al4 = make_float4(ex2_approx(la[k].x * kL2E), ex2_approx(la[k].y * kL2E),
+                                             ex2_approx(la[k].z * kL2E), ex2_approx(la[k].w * kL2E));
+                    if (r == 0) {
+                        al4.x *= e31_entering.x; al4.y *= e31_entering.y;
+                        al4.z *= e31_entering.z; al4.w *= e31_entering.w;
+                    }
+                    *reinterpret_cast<float4 *>(kf + r * kD + 4 * q4) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+                    *reinterpret_cast<float4 *>(qf + r * kD + 4 * q4) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+                    *reinterpret_cast<float4 *>(af + r * kD + 4 * q4) = al4;
+                }
+            } else {
             float kT[4][4];  // bf16 inputs: k E by channel t and loop step k
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -625,6 +683,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                     store_t4(wq, 4 * q4 + t, 4 * rg, v);
                 }
             }
+            }
         }
         if (c + 1 < nchunks) {
             if constexpr (kLayer) load_gate_inputs(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, pt, zr, bl);
@@ -640,177 +699,183 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             issue_loads<kLayer>(p, sm, bar, s ^ 1, t0 + kC, min(kC, t_end - t0 - kC), h, tid, true);
             issued = c + 2;
         }
-        if (tid == kPA || tid == kPB) {  // M1: Gram, K steps split over the two issuers
-            // M = 64 ([k E ; q E] has 64 rows): D row m lands in TMEM lane 32 (m / 16) + m % 16
-            const uint32_t id = idesc_bf16_f32(64, 32);
-            const int s0 = tid == kPA ? 0 : 4;
-            const uint32_t d = tb + (tid == kPA ? TM_DG : TM_DU);
-            const uint32_t xh = smem_u32(wx), xl = xh + 16384;
-            const uint32_t rh = smem_u32(rr), rl = rh + 8192;
+        // Gram, solve and Tb: the tensor-core form only (a chunk run token by token needs none)
+        if (!kUnb || fast) {
+            if (tid == kPA || tid == kPB) {  // M1: Gram, K steps split over the two issuers
+                // M = 64 ([k E ; q E] has 64 rows): D row m lands in TMEM lane 32 (m / 16) + m % 16
+                const uint32_t id = idesc_bf16_f32(64, 32);
+                const int s0 = tid == kPA ? 0 : 4;
+                const uint32_t d = tb + (tid == kPA ? TM_DG : TM_DU);
+                const uint32_t xh = smem_u32(wx), xl = xh + 16384;
+                const uint32_t rh = smem_u32(rr), rl = rh + 8192;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(d, sw128_desc_k(xh, 64, s0 + k), sw128_desc_k(rh, 32, s0 + k), id, k > 0);
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(d, sw128_desc_k(xh, 64, s0 + k), sw128_desc_k(rh, 32, s0 + k), id, k > 0);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(d, sw128_desc_k(xh, 64, s0 + k), sw128_desc_k(rl, 32, s0 + k), id, 1);
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(d, sw128_desc_k(xh, 64, s0 + k), sw128_desc_k(rl, 32, s0 + k), id, 1);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                mma_bf16(d, sw128_desc_k(xl, 64, s0 + k), sw128_desc_k(rh, 32, s0 + k), id, 1);
-            mma_commit(bar + (tid == kPA ? B_PA : B_PB));
-        }
-        // ---- while M1 runs: Q~ = (q E) em, rebuilt from its hi + lo in wx (the Gram only reads
-        //      wx) -> wq elements 32 + r of rows j; layer mode also (k E)^T -> elements r of rows
-        //      j (M2b's A operand), the hi and lo words of wx's k rows transposed 4 x 4 ----
-        {
-            const int cc = q4 >> 1, hb = (q4 & 1) * 8;
-            const float4 em4 = *reinterpret_cast<const float4 *>(em_s + 4 * q4);
-            float qT[4][4];  // Q~ by channel t and loop step k (row 4 rg + (k ^ (rg & 2)))
-            uint2 kw[2][4];  // k E hi / lo words by loop step k
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int r = 4 * rg + (k ^ (rg & 2));  // the row order of F2/F3
-                const uint32_t oq = tile_chunk(64, 32 + r, cc) + hb;
-                const uint32_t ok2 = tile_chunk(64, r, cc) + hb;
-                if constexpr (kLayer) {
-                    kw[0][k] = *reinterpret_cast<const uint2 *>(wx + ok2);
-                    kw[1][k] = *reinterpret_cast<const uint2 *>(wx + 16384 + ok2);
-                }
-                float qh4[4], ql4[4];
-                bf16x4_to_f32(*reinterpret_cast<const uint2 *>(wx + oq), qh4);
-                bf16x4_to_f32(*reinterpret_cast<const uint2 *>(wx + 16384 + oq), ql4);
-                qT[0][k] = (qh4[0] + ql4[0]) * em4.x;
-                qT[1][k] = (qh4[1] + ql4[1]) * em4.y;
-                qT[2][k] = (qh4[2] + ql4[2]) * em4.z;
-                qT[3][k] = (qh4[3] + ql4[3]) * em4.w;
+                for (int k = 0; k < 4; ++k)
+                    mma_bf16(d, sw128_desc_k(xl, 64, s0 + k), sw128_desc_k(rh, 32, s0 + k), id, 1);
+                mma_commit(bar + (tid == kPA ? B_PA : B_PB));
             }
+            // ---- while M1 runs: Q~ = (q E) em, rebuilt from its hi + lo in wx (the Gram only reads
+            //      wx) -> wq elements 32 + r of rows j; layer mode also (k E)^T -> elements r of rows
+            //      j (M2b's A operand), the hi and lo words of wx's k rows transposed 4 x 4 ----
+            {
+                const int cc = q4 >> 1, hb = (q4 & 1) * 8;
+                const float4 em4 = *reinterpret_cast<const float4 *>(em_s + 4 * q4);
+                float qT[4][4];  // Q~ by channel t and loop step k (row 4 rg + (k ^ (rg & 2)))
+                uint2 kw[2][4];  // k E hi / lo words by loop step k
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const bool sw = (rg & 2) != 0;
-                const float v[4] = {sw ? qT[t][2] : qT[t][0], sw ? qT[t][3] : qT[t][1],
-                                    sw ? qT[t][0] : qT[t][2], sw ? qT[t][1] : qT[t][3]};
-                store_t4(wq, 4 * q4 + t, 32 + 4 * rg, v);
-            }
-            const bool sw = (rg & 2) != 0;
-#pragma unroll
-            for (int hl = 0; hl < (kLayer ? 2 : 0); ++hl) {
-                // rows 4 rg .. 4 rg + 3 in order
-                const uint2 a = sw ? kw[hl][2] : kw[hl][0], b = sw ? kw[hl][3] : kw[hl][1];
-                const uint2 c2 = sw ? kw[hl][0] : kw[hl][2], d = sw ? kw[hl][1] : kw[hl][3];
-                const int e0 = 4 * rg;
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {  // channel 4 q4 + t: 16-bit half t & 1 of word t >> 1
-                    const uint32_t sel = (t & 1) ? 0x7632u : 0x5410u;
-                    const uint32_t wa = (t >> 1) ? a.y : a.x, wb = (t >> 1) ? b.y : b.x;
-                    const uint32_t wc = (t >> 1) ? c2.y : c2.x, wd = (t >> 1) ? d.y : d.x;
-                    const int j = 4 * q4 + t;
-                    const uint32_t o = (uint32_t)(j * 128 + ((((e0 >> 3) ^ (j & 7))) << 4) + (e0 & 4) * 2);
-                    *reinterpret_cast<uint2 *>(wq + 16384 * hl + o) =
-                        make_uint2(__byte_perm(wa, wb, sel), __byte_perm(wc, wd, sel));
-                }
-            }
-        }
-        {
-            bool ok = true;
-            if (tid == kPA || tid == kPB)
-                ok = wait_one(bar + (tid == kPA ? B_PA : B_PB), ph & 1, p, 13);
-            ++ph;
-            alive = group_and(kPrepBar, ok);
-            fence_after_sync();
-            if (!alive) break;
-        }
-
-        // ---- F5: A (k rows, scaled by beta, strictly lower; stored column-major) and
-        //      P (q rows, lower).  The M = 64 Gram holds its rows in lanes 0-15 of each lane
-        //      quarter: quarters 0-1 the k rows 0-15 / 16-31, quarters 2-3 the q rows; each of
-        //      the two warps of a quarter takes 16 columns ----
-        {
-            float g[16], g2[16];
-            tmem_ld16(tl + TM_DG + 16 * half, g);
-            tmem_ld16(tl + TM_DU + 16 * half, g2);
-            const int r = 16 * (quarter & 1) + lane;
-            if (lane >= 16) {
-                // lanes 16-31 of each quarter hold no Gram rows
-            } else if (quarter < 2) {
-                const float br = beta_s[r];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int i = 16 * half + e;
-                    sAt[i * 32 + r] = i < r ? br * (g[e] + g2[e]) : 0.f;
-                }
-            } else {
-#pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int i = 16 * half + 8 * c2 + e;
-                        x[e] = i <= r ? g[8 * c2 + e] + g2[8 * c2 + e] : 0.f;
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 4 * rg + (k ^ (rg & 2));  // the row order of F2/F3
+                    const uint32_t oq = tile_chunk(64, 32 + r, cc) + hb;
+                    const uint32_t ok2 = tile_chunk(64, r, cc) + hb;
+                    if constexpr (kLayer) {
+                        kw[0][k] = *reinterpret_cast<const uint2 *>(wx + ok2);
+                        kw[1][k] = *reinterpret_cast<const uint2 *>(wx + 16384 + ok2);
                     }
-                    store_split_chunk(pp + sw128_chunk_offset(32, r, 2 * half + c2),
-                                      pp + sw128_chunk_offset(32, r, 4 + 2 * half + c2), x);
+                    float qh4[4], ql4[4];
+                    bf16x4_to_f32(*reinterpret_cast<const uint2 *>(wx + oq), qh4);
+                    bf16x4_to_f32(*reinterpret_cast<const uint2 *>(wx + 16384 + oq), ql4);
+                    qT[0][k] = (qh4[0] + ql4[0]) * em4.x;
+                    qT[1][k] = (qh4[1] + ql4[1]) * em4.y;
+                    qT[2][k] = (qh4[2] + ql4[2]) * em4.z;
+                    qT[3][k] = (qh4[3] + ql4[3]) * em4.w;
+                }
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const bool sw = (rg & 2) != 0;
+                    const float v[4] = {sw ? qT[t][2] : qT[t][0], sw ? qT[t][3] : qT[t][1],
+                                        sw ? qT[t][0] : qT[t][2], sw ? qT[t][1] : qT[t][3]};
+                    store_t4(wq, 4 * q4 + t, 32 + 4 * rg, v);
+                }
+                const bool sw = (rg & 2) != 0;
+#pragma unroll
+                for (int hl = 0; hl < (kLayer ? 2 : 0); ++hl) {
+                    // rows 4 rg .. 4 rg + 3 in order
+                    const uint2 a = sw ? kw[hl][2] : kw[hl][0], b = sw ? kw[hl][3] : kw[hl][1];
+                    const uint2 c2 = sw ? kw[hl][0] : kw[hl][2], d = sw ? kw[hl][1] : kw[hl][3];
+                    const int e0 = 4 * rg;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {  // channel 4 q4 + t: 16-bit half t & 1 of word t >> 1
+                        const uint32_t sel = (t & 1) ? 0x7632u : 0x5410u;
+                        const uint32_t wa = (t >> 1) ? a.y : a.x, wb = (t >> 1) ? b.y : b.x;
+                        const uint32_t wc = (t >> 1) ? c2.y : c2.x, wd = (t >> 1) ? d.y : d.x;
+                        const int j = 4 * q4 + t;
+                        const uint32_t o = (uint32_t)(j * 128 + ((((e0 >> 3) ^ (j & 7))) << 4) + (e0 & 4) * 2);
+                        *reinterpret_cast<uint2 *>(wq + 16384 * hl + o) =
+                            make_uint2(__byte_perm(wa, wb, sel), __byte_perm(wc, wd, sel));
+                    }
                 }
             }
-        }
-        group_sync(kPrepBar);
+            {
+                bool ok = true;
+                if (tid == kPA || tid == kPB)
+                    ok = wait_one(bar + (tid == kPA ? B_PA : B_PB), ph & 1, p, 13);
+                ++ph;
+                alive = group_and(kPrepBar, ok);
+                fence_after_sync();
+                if (!alive) break;
+            }
 
-        // ---- F6: T = (I + A)^-1.  One warp inverts both 16 x 16 diagonal blocks by
-        //      forward substitution (lane = column: lanes 0-15 the upper block, 16-31 the
-        //      lower), then T_10 = -T_11 (A_10 T_00) with one entry per thread, then
-        //      T goes to slot s for the chain group ----
-        if (pt < 32) {
-            const int o = 16 * (lane >> 4), j = lane & 15;
-            float x[16];
+            // ---- F5: A (k rows, scaled by beta, strictly lower; stored column-major) and
+            //      P (q rows, lower).  The M = 64 Gram holds its rows in lanes 0-15 of each lane
+            //      quarter: quarters 0-1 the k rows 0-15 / 16-31, quarters 2-3 the q rows; each of
+            //      the two warps of a quarter takes 16 columns ----
+            {
+                float g[16], g2[16];
+                tmem_ld16(tl + TM_DG + 16 * half, g);
+                tmem_ld16(tl + TM_DU + 16 * half, g2);
+                const int r = 16 * (quarter & 1) + lane;
+                if (lane >= 16) {
+                    // lanes 16-31 of each quarter hold no Gram rows
+                } else if (quarter < 2) {
+                    const float br = beta_s[r];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) x[m] = m == j ? 1.f : 0.f;
+                    for (int e = 0; e < 16; ++e) {
+                        const int i = 16 * half + e;
+                        sAt[i * 32 + r] = i < r ? br * (g[e] + g2[e]) : 0.f;
+                    }
+                } else {
 #pragma unroll
-            for (int i = 0; i < 15; ++i) {
-                float a[16];  // column o + i of A, rows o .. o + 15
+                    for (int c2 = 0; c2 < 2; ++c2) {
+                        float x[8];
 #pragma unroll
-                for (int q = (i + 1) >> 2; q < 4; ++q) {
-                    const float4 v = *reinterpret_cast<const float4 *>(sAt + (o + i) * 32 + o + 4 * q);
-                    a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+                        for (int e = 0; e < 8; ++e) {
+                            const int i = 16 * half + 8 * c2 + e;
+                            x[e] = i <= r ? g[8 * c2 + e] + g2[8 * c2 + e] : 0.f;
+                        }
+                        store_split_chunk(pp + sw128_chunk_offset(32, r, 2 * half + c2),
+                                          pp + sw128_chunk_offset(32, r, 4 + 2 * half + c2), x);
+                    }
+                }
+            }
+            group_sync(kPrepBar);
+
+            // ---- F6: T = (I + A)^-1.  One warp inverts both 16 x 16 diagonal blocks by
+            //      forward substitution (lane = column: lanes 0-15 the upper block, 16-31 the
+            //      lower), then T_10 = -T_11 (A_10 T_00) with one entry per thread, then
+            //      T goes to slot s for the chain group ----
+            if (pt < 32) {
+                const int o = 16 * (lane >> 4), j = lane & 15;
+                float x[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) x[m] = m == j ? 1.f : 0.f;
+#pragma unroll
+                for (int i = 0; i < 15; ++i) {
+                    float a[16];  // column o + i of A, rows o .. o + 15
+#pragma unroll
+                    for (int q = (i + 1) >> 2; q < 4; ++q) {
+                        const float4 v = *reinterpret_cast<const float4 *>(sAt + (o + i) * 32 + o + 4 * q);
+                        a[4 * q] = v.x; a[4 * q + 1] = v.y; a[4 * q + 2] = v.z; a[4 * q + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int m = i + 1; m < 16; ++m) x[m] = fmaf(-a[m], x[i], x[m]);
                 }
 #pragma unroll
-                for (int m = i + 1; m < 16; ++m) x[m] = fmaf(-a[m], x[i], x[m]);
+                for (int m = 0; m < 16; ++m) sT[(o + m) * kLdT + o + j] = x[m];
             }
-#pragma unroll
-            for (int m = 0; m < 16; ++m) sT[(o + m) * kLdT + o + j] = x[m];
-        }
-        group_sync(kPrepBar);
-        {  // 32 x 32: T_10 = -T_11 (A_10 T_00), one entry per thread (row 16 + r, column i)
-            const int r = pt >> 4, i = pt & 15;
-            float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; m += 2) {
-                x0 = fmaf(sAt[m * 32 + 16 + r], sT[m * kLdT + i], x0);
-                x1 = fmaf(sAt[(m + 1) * 32 + 16 + r], sT[(m + 1) * kLdT + i], x1);
-            }
-            // X = A_10 T_00 (row r, column i) goes to T's upper-right block, which T never uses
-            sT[r * kLdT + 16 + i] = x0 + x1;
             group_sync(kPrepBar);
-            float y0 = 0.f, y1 = 0.f;
+            {  // 32 x 32: T_10 = -T_11 (A_10 T_00), one entry per thread (row 16 + r, column i)
+                const int r = pt >> 4, i = pt & 15;
+                float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; m += 2) {
-                y0 = fmaf(sT[(16 + r) * kLdT + 16 + m], sT[m * kLdT + 16 + i], y0);
-                y1 = fmaf(sT[(16 + r) * kLdT + 17 + m], sT[(m + 1) * kLdT + 16 + i], y1);
+                for (int m = 0; m < 16; m += 2) {
+                    x0 = fmaf(sAt[m * 32 + 16 + r], sT[m * kLdT + i], x0);
+                    x1 = fmaf(sAt[(m + 1) * 32 + 16 + r], sT[(m + 1) * kLdT + i], x1);
+                }
+                // X = A_10 T_00 (row r, column i) goes to T's upper-right block, which T never uses
+                sT[r * kLdT + 16 + i] = x0 + x1;
+                group_sync(kPrepBar);
+                float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; m += 2) {
+                    y0 = fmaf(sT[(16 + r) * kLdT + 16 + m], sT[m * kLdT + 16 + i], y0);
+                    y1 = fmaf(sT[(16 + r) * kLdT + 17 + m], sT[(m + 1) * kLdT + 16 + i], y1);
+                }
+                sT[(16 + r) * kLdT + i] = -(y0 + y1);
             }
-            sT[(16 + r) * kLdT + i] = -(y0 + y1);
+            group_sync(kPrepBar);
+            // ---- Tb = T diag(beta) (32 rows x K 32) -> slot s: one 16-byte chunk per thread ----
+            if (pt < 128) {
+                const int r = pt >> 2, cc = pt & 3;
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = 8 * cc + e;
+                    x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
+                }
+                // a quarter-warp holds rows r and r + 1: odd rows store their lo chunk first, so
+                // that each instruction's 8 chunks fall in 8 distinct 16-byte bank groups
+                unsigned char *tbs = sm + S_TB + s * TB_SIZE;
+                store_split_chunk(tbs + sw128_chunk_offset(32, r, cc), tbs + sw128_chunk_offset(32, r, 4 + cc),
+                                  x, (r & 1) != 0);
+            }
         }
-        group_sync(kPrepBar);
-        // ---- Tb = T diag(beta) (32 rows x K 32) -> slot s: one 16-byte chunk per thread ----
-        if (pt < 128) {
-            const int r = pt >> 2, cc = pt & 3;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int i = 8 * cc + e;
-                x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
-            }
-            // a quarter-warp holds rows r and r + 1: odd rows store their lo chunk first, so
-            // that each instruction's 8 chunks fall in 8 distinct 16-byte bank groups
-            unsigned char *tbs = sm + S_TB + s * TB_SIZE;
-            store_split_chunk(tbs + sw128_chunk_offset(32, r, cc), tbs + sw128_chunk_offset(32, r, 4 + cc),
-                              x, (r & 1) != 0);
+        if constexpr (kUnb) {
+            if (tid == kPA) reinterpret_cast<int *>(sm + S_TSLOT + 8)[s] = fast ? 0 : 1;
         }
         fence_proxy_async_smem();  // wq, P and Tb are MMA operands of the chain group
         group_sync(kPrepBar);
@@ -847,7 +912,7 @@ __device__ __forceinline__ float *snapshot_dst(const Params &p, int base, int co
     return p.ckpt.states + ((size_t)(base + k) * p.H + h) * (size_t)(kD * kD);
 }
 
-template <typename Tout, bool kLayer, bool kCkpt>
+template <typename Tout, bool kLayer, bool kCkpt, bool kUnb>
 __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, uint32_t tb,
                                             int h, int n, int t_begin, int t_end, int nchunks) {
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -931,6 +996,89 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             if (!alive) break;
         }
 
+        // kUnb: a chunk out of the tensor-core range runs token by token on the state in TMEM
+        const bool fb = kUnb && reinterpret_cast<const int *>(sm + S_TSLOT + 8)[s] != 0;
+        if (fb) {
+            // The recurrence itself, token by token, on column c_lane of the state (TMEM lane
+            // c_lane): S <- Diag(alpha_t) S, r = S^T k_t, u = beta_t (v_t - r), S <- S + k_t u,
+            // o~ = scale S^T q_t.  The prep group left raw k, q and alpha (fp32, [32][128]) in the
+            // slot's [W ; Q~] and R tiles, alpha of row 0 times the entering state's scale, so the
+            // state comes out unscaled (the prep group set this chunk's e31 to 1).  Exact for any
+            // decay, alpha = 0 included.  Each token's S^T q_t goes to the readout accumulator's
+            // TMEM column (its partner columns zero), so the readout below serves both forms.
+            if constexpr (sizeof(Tout) == 2 && !kLayer) copy_out();  // the previous chunk's rows
+            {
+                uint32_t zero[32];
+#pragma unroll
+                for (int r = 0; r < 32; ++r) zero[r] = 0u;
+                tmem_st32(tl + TM_D3A + 32, zero);
+                tmem_st32(tl + TM_D3B + 32, zero);
+            }
+            const float *kf = reinterpret_cast<const float *>(wq), *qf = kf + kC * kD;
+            const float *af = reinterpret_cast<const float *>(rr);
+            const float *beta_c = reinterpret_cast<const float *>(sm + S_BETA + 128 * s);
+            for (int t = 0; t < nrow; ++t) {
+                const float *at = af + t * kD, *kt = kf + t * kD, *qt = qf + t * kD;
+                // v_t[c] (bf16 tile; layer mode: hi in the v^p tile, lo in the q^p tile's place)
+                const uint32_t vo = tile_chunk(32, t, c_lane >> 3) + (c_lane & 7) * 2;
+                float vc = __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short *>(qkv + VO + vo) << 16);
+                if constexpr (kLayer)
+                    vc += __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short *>(qkv + QO + vo) << 16);
+                float r4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int part = 0; part < 4; ++part) {  // decay and prediction
+                    float sv[32];
+                    uint32_t st[32];
+                    tmem_ld32(tl + TM_ST + 32 * part, sv);
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(at + 32 * part + jj);
+                        const float4 k4 = *reinterpret_cast<const float4 *>(kt + 32 * part + jj);
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x = sv[jj + e] * av[e];
+                            r4[e] = fmaf(x, kv[e], r4[e]);
+                            st[jj + e] = __float_as_uint(x);
+                        }
+                    }
+                    tmem_st32(tl + TM_ST + 32 * part, st);
+                }
+                tmem_wait_st();
+                const float u = beta_c[t] * (vc - ((r4[0] + r4[1]) + (r4[2] + r4[3])));
+                float o4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int part = 0; part < 4; ++part) {  // delta write and readout
+                    float sv[32];
+                    uint32_t st[32];
+                    tmem_ld32(tl + TM_ST + 32 * part, sv);
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 4) {
+                        const float4 k4 = *reinterpret_cast<const float4 *>(kt + 32 * part + jj);
+                        const float4 q4 = *reinterpret_cast<const float4 *>(qt + 32 * part + jj);
+                        const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x = fmaf(kv[e], u, sv[jj + e]);
+                            o4[e] = fmaf(x, qv[e], o4[e]);
+                            st[jj + e] = __float_as_uint(x);
+                        }
+                    }
+                    tmem_st32(tl + TM_ST + 32 * part, st);
+                }
+                tmem_st1u(tl + TM_D3A + 32 + t,
+                          __float_as_uint((o4[0] + o4[1]) + (o4[2] + o4[3])));
+                tmem_wait_st();
+            }
+            // every thread is done with slot s: its v tile and its operand tiles go back
+            fence_before_sync();
+            group_sync(kChainBar);
+            fence_after_sync();
+            if (tid == 0) {
+                mbar_arrive(bar + B_VFREE + s);
+                mbar_arrive(bar + B_EMPTY + s);
+            }
+        } else {
         // (Tb, W's k E and Q~ came with the slot: the prep group published them)
         if (tid == kCA) {  // M2: U~^T = V^T Tb^T  (V read MN-major: exact bf16, or hi + lo)
             const uint32_t th = smem_u32(sm + S_TB + s * TB_SIZE);
@@ -1145,6 +1293,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             if (!alive) break;
             if (tid == 0) mbar_arrive(bar + B_EMPTY + s);
         }
+        }  // the tensor-core form
         {
             float a[32], b[32];
             tmem_ld32(tl + TM_D3A + 32, a);
@@ -1250,7 +1399,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
     }
 }
 
-template <typename Tout, bool kLayer, bool kCkpt, bool kHeadDecay>
+template <typename Tout, bool kLayer, bool kCkpt, bool kHeadDecay, bool kUnb>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -1293,9 +1442,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int nchunks = t_end > t_begin ? (t_end - t_begin + kC - 1) / kC : 0;
 
     if (warp >= 4)
-        prep_group<kLayer, kHeadDecay>(p, sm, tb, h, t_begin, t_end, nchunks);
+        prep_group<kLayer, kHeadDecay, kUnb>(p, sm, tb, h, t_begin, t_end, nchunks);
     else
-        chain_group<Tout, kLayer, kCkpt>(p, sm, tb, h, n, t_begin, t_end, nchunks);
+        chain_group<Tout, kLayer, kCkpt, kUnb>(p, sm, tb, h, n, t_begin, t_end, nchunks);
 
     fence_before_sync();
     __syncthreads();
@@ -1335,13 +1484,13 @@ bool encode_bf16_tiles(CUtensorMap *m, const void *base, int T, int H, int box_r
                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <typename Tout, bool kLayer, bool kCkpt, bool kHeadDecay>
+template <typename Tout, bool kLayer, bool kCkpt, bool kHeadDecay, bool kUnb = false>
 cudaError_t launch_kernel(const Params &p, int num_seqs, int num_heads, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<Tout, kLayer, kCkpt, kHeadDecay>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<Tout, kLayer, kCkpt, kHeadDecay, kUnb>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM_DYN);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)num_seqs * (unsigned)num_heads;
-    prefill_tc_kernel<Tout, kLayer, kCkpt, kHeadDecay><<<grid, kThreads, SM_DYN, stream>>>(p);
+    prefill_tc_kernel<Tout, kLayer, kCkpt, kHeadDecay, kUnb><<<grid, kThreads, SM_DYN, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -1386,6 +1535,8 @@ cudaError_t launch_typed(const PrefillArgs &a, cudaStream_t stream) {
     p.S_final = a.S_final;
     p.ckpt = a.ckpt;
     p.status = a.status;
+    if (a.unbounded)  // no decay floor: chunks out of the tensor-core range run token by token
+        return launch_kernel<Tout, false, false, false, true>(p, a.num_seqs, a.num_heads, stream);
     if (a.head_decay) return launch_params<Tout, false, true>(p, a.num_seqs, a.num_heads, stream);
     return launch_params<Tout, false, false>(p, a.num_seqs, a.num_heads, stream);
 }
@@ -1420,6 +1571,8 @@ cudaError_t launch_layer_typed(const LayerArgs &a, cudaStream_t stream) {
     p.b = a.b;
     p.l2_eps = a.l2_eps;
     p.rms_eps = a.rms_eps;
+    if (a.unbounded_decay)
+        return launch_kernel<Tout, true, false, false, true>(p, a.num_seqs, a.num_heads, stream);
     return launch_params<Tout, true, false>(p, a.num_seqs, a.num_heads, stream);
 }
 

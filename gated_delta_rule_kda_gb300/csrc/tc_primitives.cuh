@@ -326,6 +326,10 @@ __device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[1
         "r"(v[15])
         : "memory");
 }
+__device__ __forceinline__ void tmem_st1u(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v)
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_st8u(uint32_t taddr, const uint32_t (&v)[8]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),

@@ -52,6 +52,7 @@ EXPORTED = (
     "kda_layer_core_unbounded_decay",
     "kda_layer_core_noalloc",
     "kda_layer_core_fused",
+    "kda_layer_core_fused_unbounded_decay",
     "kda_layer_core_fused_with_checkpoints",
     "kda_decode_layer",
     "kda_decode_tokens",
@@ -119,6 +120,8 @@ def _load() -> ctypes.CDLL:
     lib.kda_layer_core_fused.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, F, F,
                                          F, ctypes.c_int, P, P, P]
     lib.kda_layer_core_fused.restype = ctypes.c_int
+    lib.kda_layer_core_fused_unbounded_decay.argtypes = lib.kda_layer_core_fused.argtypes
+    lib.kda_layer_core_fused_unbounded_decay.restype = ctypes.c_int
     lib.kda_layer_core_fused_with_checkpoints.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P,
                                                           P, P, P, F, F, F, ctypes.c_int, P, P,
                                                           I32, P, P, P]
@@ -392,7 +395,7 @@ def kda_layer_core_noalloc(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlen
 def kda_layer_core_fused(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0=None,
                          scale=DEFAULT_SCALE, l2_eps=1e-6, rms_eps=1e-6, *,
                          out_dtype=torch.bfloat16, o=None, S_final=None, want_state=True,
-                         stream=None):
+                         stream=None, _entry="kda_layer_core_fused"):
     """The layer core in one tensor-core kernel.  Returns (o_gated, S_final or None)."""
     T, H, _ = qp.shape
     N = cu_seqlens.shape[0] - 1
@@ -400,12 +403,23 @@ def kda_layer_core_fused(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens,
         o = torch.empty((T, H, HEAD_DIM), dtype=out_dtype, device=qp.device)
     if S_final is None and want_state:
         S_final = torch.empty((N, H, HEAD_DIM, HEAD_DIM), dtype=torch.float32, device=qp.device)
-    rc = _lib.kda_layer_core_fused(N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A),
-                                   _p(b), _p(beta_logit), _p(g), _p(cu_seqlens), _p(S0),
-                                   float(scale), float(l2_eps), float(rms_eps),
-                                   _dtype_code(o.dtype), _p(o), _p(S_final), _stream(stream))
-    _check("kda_layer_core_fused", rc)
+    rc = getattr(_lib, _entry)(N, T, H, _p(qp), _p(kp), _p(vp), _p(conv_w), _p(z), _p(A),
+                               _p(b), _p(beta_logit), _p(g), _p(cu_seqlens), _p(S0),
+                               float(scale), float(l2_eps), float(rms_eps),
+                               _dtype_code(o.dtype), _p(o), _p(S_final), _stream(stream))
+    _check(_entry, rc)
     return o, S_final
+
+
+def kda_layer_core_fused_unbounded_decay(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens,
+                                         S0=None, scale=DEFAULT_SCALE, l2_eps=1e-6, rms_eps=1e-6,
+                                         *, out_dtype=torch.bfloat16, o=None, S_final=None,
+                                         want_state=True, stream=None):
+    """kda_layer_core_fused with Kimi Linear's decay gate -e^A softplus(z + b) (no floor)."""
+    return kda_layer_core_fused(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens, S0,
+                                scale, l2_eps, rms_eps, out_dtype=out_dtype, o=o,
+                                S_final=S_final, want_state=want_state, stream=stream,
+                                _entry="kda_layer_core_fused_unbounded_decay")
 
 
 def kda_layer_core_fused_with_checkpoints(qp, kp, vp, conv_w, z, A, b, beta_logit, g, cu_seqlens,

@@ -177,10 +177,13 @@ kda_status kda_prefill_head_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32
  * of -5 the chunk's reciprocal decays overflow, which is why Kimi Linear's
  * unbounded gate needed a position-pair fallback inside each chunk ("Kimi K3's
  * Architecture: Kimi Delta Attention, Attention Residuals, and 896 Experts",
- * section "Channel-wise decay, and the floor K3 puts under it"); this call runs
- * the token-by-token kernel for every input type instead, which has no
- * reciprocal and is exact up to fp32 rounding.  Arguments, layouts and errors
- * as kda_prefill.
+ * section "Channel-wise decay, and the floor K3 puts under it").  Here bf16
+ * inputs run the tensor-core kernel chunk by chunk: a 32-token chunk whose decay
+ * factors all lie within the range the floor would guarantee (about e^{+-80}
+ * around the chunk's middle) takes the tensor-core form, any other chunk runs
+ * token by token on the state inside the same kernel, exact for any decay.
+ * fp32 inputs run the token-by-token kernel, which has no reciprocal and is
+ * exact up to fp32 rounding.  Arguments, layouts and errors as kda_prefill.
  */
 kda_status kda_prefill_unbounded_decay(kda_dtype in_dtype, kda_dtype out_dtype, int32_t num_seqs,
                                        int32_t total_tokens, int32_t num_heads, const void *q,
@@ -387,6 +390,25 @@ kda_status kda_layer_core_fused(int32_t num_seqs, int32_t total_tokens, int32_t 
                                 const int32_t *cu_seqlens, const float *S0, float scale,
                                 float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated,
                                 float *S_final, void *stream);
+
+/*
+ * kda_layer_core_fused_unbounded_decay - kda_layer_core_fused with Kimi Linear's decay
+ * gate log alpha = -e^{A_h} softplus(z + b), which has no floor ("Kimi K3's
+ * Architecture: Kimi Delta Attention, Attention Residuals, and 896 Experts", section
+ * "Channel-wise decay, and the floor K3 puts under it": K3 bounds the decay so that the
+ * chunk's reciprocal decays stay in range; Kimi Linear did not).  Arguments, results and
+ * errors are those of kda_layer_core_fused.
+ * Each 32-token chunk takes the tensor-core form when every one of its decay factors lies
+ * within the range that the -5 floor would guarantee (about e^{+-80} around the chunk's
+ * middle), and otherwise runs token by token on the state inside the same kernel, exactly
+ * for any decay (log alpha = -inf included).  On inputs like the 16-sequence layer workload
+ * (A ~ N(0, 0.5), z ~ N(0, 1)) about one chunk in 10^5 takes the token-by-token form.
+ */
+kda_status kda_layer_core_fused_unbounded_decay(
+    int32_t num_seqs, int32_t total_tokens, int32_t num_heads, const void *qp, const void *kp,
+    const void *vp, const float *conv_w, const void *z, const float *A, const float *b,
+    const void *beta_logit, const void *g, const int32_t *cu_seqlens, const float *S0, float scale,
+    float l2_eps, float rms_eps, kda_dtype out_dtype, void *o_gated, float *S_final, void *stream);
 
 /*
  * kda_layer_core_fused_with_checkpoints - kda_layer_core_fused that also leaves
