@@ -401,6 +401,34 @@ def run_ours(args, world, rank, local):
                                "kernel": "kda_prefill_head_decay"}}
     del la_head
 
+    # ---------------- no decay floor (Kimi Linear): kda_prefill_unbounded_decay ----------------
+    def unbounded_step():
+        kda.kda_prefill_unbounded_decay(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta,
+                                        inp.cu_seqlens, None, o=o, S_final=Sf)
+
+    ub_total, _ = time_launches(unbounded_step, args.steps, args.warmup, world)
+    ub_ms = max_over_ranks(ub_total / args.steps, world)
+    la_strong = -40.0 * torch.rand(inp.log_alpha.shape, generator=torch.Generator(device=dev)
+                                   .manual_seed(7), device=dev)
+
+    def strong_step():
+        kda.kda_prefill_unbounded_decay(inp.q, inp.k, inp.v, la_strong, inp.beta,
+                                        inp.cu_seqlens, None, o=o, S_final=Sf)
+
+    st_steps = max(1, min(args.steps, 3))
+    st_total, _ = time_launches(strong_step, st_steps, args.warmup, world)
+    st_ms = max_over_ranks(st_total / st_steps, world)
+    del la_strong
+    prefill_unbounded = {"entry_point": "kda_prefill_unbounded_decay",
+                         "in_range": {"decays": "the bench step's (every chunk takes the "
+                                                "tensor-core form)", "ms_per_step": ub_ms,
+                                      "tokens_per_s": aggregate_rate(tokens_per_step, ub_ms, world)},
+                         "strong_decay": {"decays": "log alpha uniform in [-40, 0] (every chunk "
+                                                    "runs token by token in the kernel)",
+                                          "ms_per_step": st_ms,
+                                          "tokens_per_s": aggregate_rate(tokens_per_step, st_ms,
+                                                                         world)}}
+
     # ---------------- the long prefill: 1 x 131,072 tokens x 96 heads, carried S0 ----------------
     long_prefill = None
     if not args.skip_long_prefill:
@@ -646,6 +674,20 @@ def run_ours(args, world, rank, local):
                                         "tokens_per_s": aggregate_rate(LT, u_ms, world),
                                         "launches_per_step": 3}
             del ws
+
+        def unbounded_fused_step():  # the same gate in the tensor-core kernel (chunk fallback)
+            kda.kda_layer_core_fused_unbounded_decay(linp.qp, linp.kp, linp.vp, linp.conv_w,
+                                                     linp.z, linp.A, linp.b, linp.beta_logit,
+                                                     linp.g, linp.cu_seqlens, None, o=og,
+                                                     S_final=Sl)
+
+        uf_total, _ = time_launches(unbounded_fused_step, l_steps, args.warmup, world)
+        uf_ms = max_over_ranks(uf_total / l_steps, world)
+        layer["unbounded_decay_fused"] = {"entry_point": "kda_layer_core_fused_unbounded_decay",
+                                          "ms_per_step": uf_ms,
+                                          "tokens_per_s": aggregate_rate(LT, uf_ms, world),
+                                          "vs_bounded_fused": uf_ms / l_ms,
+                                          "launches_per_step": 1}
         del linp, og, Sl
         torch.cuda.empty_cache()
 
@@ -673,6 +715,7 @@ def run_ours(args, world, rank, local):
             "dtype": "bf16", "data": "synthetic", "config": workload_config(world),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "prefill_checkpoints": checkpoints, "prefill_head_decay": head_decay,
+            "prefill_unbounded_decay": prefill_unbounded,
             "long_prefill": long_prefill, "contents_check": contents_check,
             "decode": decode,
             "decode_layer": decode_layer, "speculative": spec, "layer_core": layer,
