@@ -181,8 +181,15 @@ __device__ __forceinline__ float sigmoid_(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
     return r;
 }
-// log(1 + e^x); above 20 it equals x to fp32 precision (Kimi Linear's decay gate).
-__device__ __forceinline__ float softplus_(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+// log(1 + e^x) on the SFU (ex2.approx, lg2.approx: about 2^-22 relative); above 20 it equals x to
+// fp32 precision, and where e^x is below half an ulp of 1 it returns 0 (alpha = 1 to within
+// 6e-8).  Kimi Linear's decay gate.
+__device__ __forceinline__ float softplus_(float x) {
+    if (x > 20.f) return x;
+    float l;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l) : "f"(1.f + ex2_approx(1.4426950408889634f * x)));
+    return 0.6931471805599453f * l;
+}
 __device__ __forceinline__ void bf16x4_to_f32(uint2 u, float (&x)[4]) {
     x[0] = __uint_as_float(u.x << 16);
     x[1] = __uint_as_float(u.x & 0xFFFF0000u);
@@ -394,7 +401,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
         float *sT = sT_base + s * (32 * kLdT);
         // kUnb: the chunk takes the tensor-core form (every decay factor in range) or is handed
         // to the chain group to run token by token
-        bool fast = true;
+        bool fast = true, in_range = true;
 
         // ---- slot s free again (chunk c-2 finished); chunk c's inputs landed ----
         {
@@ -574,14 +581,15 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 // Without the decay floor the chunk takes the tensor-core form only when every
                 // factor 2^{+-D} stays inside 2^115 (about e^80, the range the floor guarantees);
                 // otherwise (a decay of -inf included) the chain group runs it token by token.
-                bool ok = true;
+                // Layer mode votes here, while the thread still holds q^, k^; with bf16 inputs
+                // the vote rides on the operand pass's closing barrier instead.
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    ok = ok && fabsf(base.x + pre[k].x) <= 115.f && fabsf(base.y + pre[k].y) <= 115.f &&
-                         fabsf(base.z + pre[k].z) <= 115.f && fabsf(base.w + pre[k].w) <= 115.f;
-                fast = group_and(kPrepBar, ok);
+                    in_range = in_range && fabsf(base.x + pre[k].x) <= 115.f &&
+                               fabsf(base.y + pre[k].y) <= 115.f && fabsf(base.z + pre[k].z) <= 115.f &&
+                               fabsf(base.w + pre[k].w) <= 115.f;
+                if constexpr (kLayer) fast = group_and(kPrepBar, in_range);
             }
-            const float4 e31_entering = e31_prev;  // rows of row group 0 hold the true value
             if (rg == 0) {
                 // a chunk run token by token leaves the state unscaled: e31 = 1
                 const float4 e31 = fast ? make_float4(ex2_approx(last.x), ex2_approx(last.y),
@@ -596,31 +604,27 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             // Row order: threads with bit 1 of rg set take their rows in the order 2, 3, 0, 1,
             // so that the four rows a half-warp stores at once (8-byte accesses are served a
             // half-warp at a time) fall in four distinct 32-byte bank groups of the swizzled tile.
-            if (kUnb && !fast) {
-                // Out of range: raw k, q (fp32) into slot s's [W ; Q~] tile and alpha (fp32; row 0
-                // times the entering state's scale e31) into its R tile, [32][128] each, for the
-                // chain group's token-by-token pass.  Nothing else of the chunk is built.
+            if (kUnb && kLayer && !fast) {
+                // Out of range (layer mode): raw q^, k^ (fp32) into slot s's [W ; Q~] tile and
+                // alpha (fp32; row 0 times the entering state's scale e31) into its R tile,
+                // [32][128] each, for the chain group's token-by-token pass.  Nothing else of the
+                // chunk is built.  (bf16 inputs write the same after the pass's closing vote.)
                 float *kf = reinterpret_cast<float *>(wq), *qf = kf + kC * kD;
                 float *af = reinterpret_cast<float *>(rr);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int r = 4 * rg + k;
                     float kv[4], qv[4];
-                    if constexpr (kLayer) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            kv[e] = kh[k][e];
-                            qv[e] = qh[k][e];
-                        }
-                    } else {
-                        bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + KO + tile_chunk(32, r, cc) + hb), kv);
-                        bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + QO + tile_chunk(32, r, cc) + hb), qv);
+                    for (int e = 0; e < 4; ++e) {
+                        kv[e] = kh[k][e];
+                        qv[e] = qh[k][e];
                     }
                     float4 al4 = make_float4(ex2_approx(la[k].x * kL2E), ex2_approx(la[k].y * kL2E),
                                              ex2_approx(la[k].z * kL2E), ex2_approx(la[k].w * kL2E));
-                    if (r == 0) {
-                        al4.x *= e31_entering.x; al4.y *= e31_entering.y;
-                        al4.z *= e31_entering.z; al4.w *= e31_entering.w;
+                    if (r == 0) {  // the entering state's scale, stored above by this thread
+                        const float4 ep = *reinterpret_cast<const float4 *>(e31p_s + 4 * q4);
+                        al4.x *= ep.x; al4.y *= ep.y; al4.z *= ep.z; al4.w *= ep.w;
                     }
                     *reinterpret_cast<float4 *>(kf + r * kD + 4 * q4) = make_float4(kv[0], kv[1], kv[2], kv[3]);
                     *reinterpret_cast<float4 *>(qf + r * kD + 4 * q4) = make_float4(qv[0], qv[1], qv[2], qv[3]);
@@ -653,7 +657,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                     xk[t] = kv[t] * E;    // k E
                     xq[t] = qv[t] * E;    // q E
                     xr[t] = kv[t] * EI;   // k E^-1
-                    if constexpr (!kLayer) kT[t][k] = xk[t];
+                    if constexpr (!kLayer && !kUnb) kT[t][k] = xk[t];
                 }
                 uint2 h2, l2;
                 split2(xk[0], xk[1], h2.x, l2.x);
@@ -672,9 +676,10 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 *reinterpret_cast<uint2 *>(dst) = h2;
                 *reinterpret_cast<uint2 *>(dst + 8192) = l2;
             }
-            if constexpr (!kLayer) {
+            if constexpr (!kLayer && !kUnb) {
                 // (k E)^T -> wq elements 4 rg .. 4 rg + 3 of rows j = 4 q4 + t (M2b's A operand;
-                // layer mode writes it during the Gram instead, where it costs no registers here)
+                // layer mode and the unbounded variant write it during the Gram instead, where it
+                // costs no registers here)
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     const bool sw = (rg & 2) != 0;
@@ -689,7 +694,43 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
             if constexpr (kLayer) load_gate_inputs(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, pt, zr, bl);
             else load_log_alpha<kHeadDecay>(p, t0 + kC, min(kC, t_end - t0 - kC), h, q4, rg, la);
         }
-        publish(kPrepBar);
+        if constexpr (kUnb && !kLayer) {
+            // the range vote on the closing barrier; an out-of-range chunk then replaces what the
+            // pass wrote for the tensor-core form by raw k, q and alpha (log alpha read again)
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            fence_before_sync();
+            fast = group_and(kPrepBar, in_range);
+            fence_after_sync();
+            if (!fast) {
+                const int cc = q4 >> 1, hb = (q4 & 1) * 8;
+                float4 lac[4];
+                load_log_alpha<false>(p, t0, nrow, h, q4, rg, lac);
+                float *kf = reinterpret_cast<float *>(wq), *qf = kf + kC * kD;
+                float *af = reinterpret_cast<float *>(rr);
+                const float4 ep = *reinterpret_cast<const float4 *>(e31p_s + 4 * q4);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 4 * rg + k;
+                    float kv[4], qv[4];
+                    bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + KO + tile_chunk(32, r, cc) + hb), kv);
+                    bf16x4_to_f32(*reinterpret_cast<const uint2 *>(qkv + QO + tile_chunk(32, r, cc) + hb), qv);
+                    const float kL2E = 1.4426950408889634f;
+                    float4 al4 = make_float4(ex2_approx(lac[k].x * kL2E), ex2_approx(lac[k].y * kL2E),
+                                             ex2_approx(lac[k].z * kL2E), ex2_approx(lac[k].w * kL2E));
+                    if (r == 0) { al4.x *= ep.x; al4.y *= ep.y; al4.z *= ep.z; al4.w *= ep.w; }
+                    *reinterpret_cast<float4 *>(kf + r * kD + 4 * q4) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+                    *reinterpret_cast<float4 *>(qf + r * kD + 4 * q4) = make_float4(qv[0], qv[1], qv[2], qv[3]);
+                    *reinterpret_cast<float4 *>(af + r * kD + 4 * q4) = al4;
+                }
+                if (rg == 0) {  // the chunk leaves the state unscaled
+                    *reinterpret_cast<float4 *>(e31_s + 4 * q4) = make_float4(1.f, 1.f, 1.f, 1.f);
+                    e31_prev = make_float4(1.f, 1.f, 1.f, 1.f);
+                }
+            }
+        } else {
+            publish(kPrepBar);
+        }
         if (c + 1 < nchunks) {  // stage chunk c+1 into slot s^1 once chunk c-1 no longer needs it
             bool ok = true;
             if (tid == kTmaThread && c >= 1)
@@ -732,7 +773,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                     const int r = 4 * rg + (k ^ (rg & 2));  // the row order of F2/F3
                     const uint32_t oq = tile_chunk(64, 32 + r, cc) + hb;
                     const uint32_t ok2 = tile_chunk(64, r, cc) + hb;
-                    if constexpr (kLayer) {
+                    if constexpr (kLayer || kUnb) {
                         kw[0][k] = *reinterpret_cast<const uint2 *>(wx + ok2);
                         kw[1][k] = *reinterpret_cast<const uint2 *>(wx + 16384 + ok2);
                     }
@@ -753,7 +794,7 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 }
                 const bool sw = (rg & 2) != 0;
 #pragma unroll
-                for (int hl = 0; hl < (kLayer ? 2 : 0); ++hl) {
+                for (int hl = 0; hl < ((kLayer || kUnb) ? 2 : 0); ++hl) {
                     // rows 4 rg .. 4 rg + 3 in order
                     const uint2 a = sw ? kw[hl][2] : kw[hl][0], b = sw ? kw[hl][3] : kw[hl][1];
                     const uint2 c2 = sw ? kw[hl][0] : kw[hl][2], d = sw ? kw[hl][1] : kw[hl][3];
@@ -912,6 +953,73 @@ __device__ __forceinline__ float *snapshot_dst(const Params &p, int base, int co
     return p.ckpt.states + ((size_t)(base + k) * p.H + h) * (size_t)(kD * kD);
 }
 
+// A chunk out of the tensor-core range (kUnb), run token by token on column c_lane of the
+// state (TMEM lane c_lane): S <- Diag(alpha_t) S, r = S^T k_t, u = beta_t (v_t - r),
+// S <- S + k_t u, then S^T q_t (unscaled) into the readout accumulator's TMEM column t.  Out of
+// line, so that the tensor-core loop keeps its code size.
+template <bool kLayer>
+__device__ __noinline__ void token_by_token_chunk(unsigned char *sm, uint32_t tl, int s, int nrow,
+                                                   int c_lane) {
+    const unsigned char *wq = sm + S_WQ + s * WQ_SIZE, *rr = sm + S_R + s * R_SIZE;
+    const unsigned char *qkv = sm + S_QKV + s * QKV_SIZE;
+    const float *kf = reinterpret_cast<const float *>(wq), *qf = kf + kC * kD;
+    const float *af = reinterpret_cast<const float *>(rr);
+    const float *beta_c = reinterpret_cast<const float *>(sm + S_BETA + 128 * s);
+    for (int t = 0; t < nrow; ++t) {
+        const float *at = af + t * kD, *kt = kf + t * kD, *qt = qf + t * kD;
+        // v_t[c] (bf16 tile; layer mode: hi in the v^p tile, lo in the q^p tile's place)
+        const uint32_t vo = tile_chunk(32, t, c_lane >> 3) + (c_lane & 7) * 2;
+        float vc = __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short *>(qkv + VO + vo) << 16);
+        if constexpr (kLayer)
+            vc += __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short *>(qkv + QO + vo) << 16);
+        float r4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {  // decay and prediction
+            float sv[32];
+            uint32_t st[32];
+            tmem_ld32(tl + TM_ST + 32 * part, sv);
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(at + 32 * part + jj);
+                const float4 k4 = *reinterpret_cast<const float4 *>(kt + 32 * part + jj);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x = sv[jj + e] * av[e];
+                    r4[e] = fmaf(x, kv[e], r4[e]);
+                    st[jj + e] = __float_as_uint(x);
+                }
+            }
+            tmem_st32(tl + TM_ST + 32 * part, st);
+        }
+        tmem_wait_st();
+        const float u = beta_c[t] * (vc - ((r4[0] + r4[1]) + (r4[2] + r4[3])));
+        float o4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int part = 0; part < 4; ++part) {  // delta write and readout
+            float sv[32];
+            uint32_t st[32];
+            tmem_ld32(tl + TM_ST + 32 * part, sv);
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 4) {
+                const float4 k4 = *reinterpret_cast<const float4 *>(kt + 32 * part + jj);
+                const float4 q4 = *reinterpret_cast<const float4 *>(qt + 32 * part + jj);
+                const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x = fmaf(kv[e], u, sv[jj + e]);
+                    o4[e] = fmaf(x, qv[e], o4[e]);
+                    st[jj + e] = __float_as_uint(x);
+                }
+            }
+            tmem_st32(tl + TM_ST + 32 * part, st);
+        }
+        tmem_st1u(tl + TM_D3A + 32 + t,
+                  __float_as_uint((o4[0] + o4[1]) + (o4[2] + o4[3])));
+        tmem_wait_st();
+    }
+}
+
 template <typename Tout, bool kLayer, bool kCkpt, bool kUnb>
 __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, uint32_t tb,
                                             int h, int n, int t_begin, int t_end, int nchunks) {
@@ -1014,62 +1122,7 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                 tmem_st32(tl + TM_D3A + 32, zero);
                 tmem_st32(tl + TM_D3B + 32, zero);
             }
-            const float *kf = reinterpret_cast<const float *>(wq), *qf = kf + kC * kD;
-            const float *af = reinterpret_cast<const float *>(rr);
-            const float *beta_c = reinterpret_cast<const float *>(sm + S_BETA + 128 * s);
-            for (int t = 0; t < nrow; ++t) {
-                const float *at = af + t * kD, *kt = kf + t * kD, *qt = qf + t * kD;
-                // v_t[c] (bf16 tile; layer mode: hi in the v^p tile, lo in the q^p tile's place)
-                const uint32_t vo = tile_chunk(32, t, c_lane >> 3) + (c_lane & 7) * 2;
-                float vc = __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short *>(qkv + VO + vo) << 16);
-                if constexpr (kLayer)
-                    vc += __uint_as_float((uint32_t)*reinterpret_cast<const unsigned short *>(qkv + QO + vo) << 16);
-                float r4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int part = 0; part < 4; ++part) {  // decay and prediction
-                    float sv[32];
-                    uint32_t st[32];
-                    tmem_ld32(tl + TM_ST + 32 * part, sv);
-#pragma unroll
-                    for (int jj = 0; jj < 32; jj += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(at + 32 * part + jj);
-                        const float4 k4 = *reinterpret_cast<const float4 *>(kt + 32 * part + jj);
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float x = sv[jj + e] * av[e];
-                            r4[e] = fmaf(x, kv[e], r4[e]);
-                            st[jj + e] = __float_as_uint(x);
-                        }
-                    }
-                    tmem_st32(tl + TM_ST + 32 * part, st);
-                }
-                tmem_wait_st();
-                const float u = beta_c[t] * (vc - ((r4[0] + r4[1]) + (r4[2] + r4[3])));
-                float o4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int part = 0; part < 4; ++part) {  // delta write and readout
-                    float sv[32];
-                    uint32_t st[32];
-                    tmem_ld32(tl + TM_ST + 32 * part, sv);
-#pragma unroll
-                    for (int jj = 0; jj < 32; jj += 4) {
-                        const float4 k4 = *reinterpret_cast<const float4 *>(kt + 32 * part + jj);
-                        const float4 q4 = *reinterpret_cast<const float4 *>(qt + 32 * part + jj);
-                        const float kv[4] = {k4.x, k4.y, k4.z, k4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float x = fmaf(kv[e], u, sv[jj + e]);
-                            o4[e] = fmaf(x, qv[e], o4[e]);
-                            st[jj + e] = __float_as_uint(x);
-                        }
-                    }
-                    tmem_st32(tl + TM_ST + 32 * part, st);
-                }
-                tmem_st1u(tl + TM_D3A + 32 + t,
-                          __float_as_uint((o4[0] + o4[1]) + (o4[2] + o4[3])));
-                tmem_wait_st();
-            }
+            token_by_token_chunk<kLayer>(sm, tl, s, nrow, c_lane);
             // every thread is done with slot s: its v tile and its operand tiles go back
             fence_before_sync();
             group_sync(kChainBar);
