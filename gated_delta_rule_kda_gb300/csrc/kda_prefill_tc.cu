@@ -1221,15 +1221,63 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                     if (part < 3) tmem_ld_wait32(sr[(part + 1) & 1]);
                 }
             };
+            // Layer mode keeps this loop rolled: its larger code (the front end) makes
+            // instruction fetch the tighter limit there (measured: 45.2 ms against 46.0 ms per
+            // step on the layer workload); the prefill unrolls it and keeps the next part's TMEM
+            // load in flight (1.14 ms against 1.22 ms).
+            auto f4_rolled = [&](auto with_snapshot, float *snap) {
+                constexpr bool kSnap = decltype(with_snapshot)::value;
+#pragma unroll 1
+                for (int part = 0; part < 4; ++part) {
+                    if (part == 1 && (tid == kCA || tid == kCB)) {
+                        m2_ok = wait_one(bar + (tid == kCA ? B_CA : B_CB), ph & 1, p, 24);
+                        if (m2_ok && tid == kCA) mbar_arrive(bar + B_VFREE + s);
+                    }
+                    const int j0 = 32 * part;
+                    float sv[32];
+                    tmem_ld32(tl + TM_ST + j0, sv);
+                    uint32_t hw[16], lw[16], yv[32];
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj += 4) {
+                        const float4 ep = *reinterpret_cast<const float4 *>(e31p + j0 + jj);
+                        const float4 mm = *reinterpret_cast<const float4 *>(em + j0 + jj);
+                        const float2 a = mul2(make_float2(sv[jj], sv[jj + 1]), make_float2(ep.x, ep.y));
+                        const float2 b =
+                            mul2(make_float2(sv[jj + 2], sv[jj + 3]), make_float2(ep.z, ep.w));
+                        split2(a.x, a.y, hw[jj >> 1], lw[jj >> 1]);
+                        split2(b.x, b.y, hw[(jj >> 1) + 1], lw[(jj >> 1) + 1]);
+                        if constexpr (kSnap) {
+                            float *d = snap + (size_t)(j0 + jj) * kD + c_lane;
+                            d[0] = a.x; d[kD] = a.y; d[2 * kD] = b.x; d[3 * kD] = b.y;
+                        }
+                        const float2 ya = mul2(a, make_float2(mm.x, mm.y));
+                        const float2 yb = mul2(b, make_float2(mm.z, mm.w));
+                        yv[jj] = __float_as_uint(ya.x);
+                        yv[jj + 1] = __float_as_uint(ya.y);
+                        yv[jj + 2] = __float_as_uint(yb.x);
+                        yv[jj + 3] = __float_as_uint(yb.y);
+                    }
+                    tmem_st16u(tl + TM_OPS + (j0 >> 1), hw);
+                    tmem_st16u(tl + TM_OPS + 64 + (j0 >> 1), lw);
+                    tmem_st32(tl + TM_ST + j0, yv);
+                }
+            };
             // The entering state S0 is the state after kC c tokens: a snapshot when that is a
             // multiple of the interval (F4 computes S0 in fp32 anyway).  Chunks without one
             // run the loop without the stores.
             float *snap = nullptr;
             if constexpr (kCkpt) snap = snapshot_dst(p, snap_base, snap_count, h, kC * c);
-            if (kCkpt && snap != nullptr)
-                f4(BoolTag<true>{}, snap);
-            else
-                f4(BoolTag<false>{}, nullptr);
+            if constexpr (kLayer) {
+                if (kCkpt && snap != nullptr)
+                    f4_rolled(BoolTag<true>{}, snap);
+                else
+                    f4_rolled(BoolTag<false>{}, nullptr);
+            } else {
+                if (kCkpt && snap != nullptr)
+                    f4(BoolTag<true>{}, snap);
+                else
+                    f4(BoolTag<false>{}, nullptr);
+            }
         }
         // ---- M2 and M2b done (W'^T is read next) ----
         {
