@@ -79,6 +79,43 @@ def test_edge_cases(kda, case):
     check(kda, inp, TOL_BF16, torch.float32)
 
 
+@pytest.mark.parametrize("case", ["la_zero", "la_floor", "beta_one", "beta_zero", "T1", "T9"])
+def test_fp32_edge_cases(kda, case):
+    """fp32 inputs (the token-by-token kernel, eight tokens staged per batch): at the decay
+    floor, without decay, with beta 0 or 1, one token, and a batch plus one token."""
+    lens = [1] if case == "T1" else [9] if case == "T9" else [150]
+    inp = synthetic.prefill_inputs(lens, 3, torch.float32, seed=22, s0_std=0.1, device="cuda")
+    if case == "la_zero":
+        inp.log_alpha.zero_()
+    elif case == "la_floor":
+        inp.log_alpha.fill_(-5.0)
+    elif case == "beta_one":
+        inp.beta.fill_(1.0)
+    elif case == "beta_zero":
+        inp.beta.zero_()
+        inp.log_alpha.mul_(0.02)
+    check(kda, inp, TOL_FP32, torch.float32)
+
+
+def test_fp32_varlen_bit_exact_packing(kda):
+    """fp32 inputs: a sequence gives the same bits alone or packed with others (its staged
+    batches start at its own first token)."""
+    lens = [77, 200, 5, 64, 0, 129]
+    inp = synthetic.prefill_inputs(lens, 3, torch.float32, seed=25, s0_std=0.1, device="cuda")
+    o, Sf = kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.cu_seqlens,
+                            inp.S0, out_dtype=torch.float32)
+    cu = inp.cu_seqlens.tolist()
+    for n, L in enumerate(lens):
+        a, b = cu[n], cu[n + 1]
+        solo_cu = torch.tensor([0, L], dtype=torch.int32, device="cuda")
+        o_n, S_n = kda.kda_prefill(inp.q[a:b], inp.k[a:b], inp.v[a:b], inp.log_alpha[a:b],
+                                   inp.beta[a:b], solo_cu, inp.S0[n:n + 1].contiguous(),
+                                   out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert torch.equal(o_n, o[a:b]), f"sequence {n} output differs when run alone"
+        assert torch.equal(S_n[0], Sf[n]), f"sequence {n} state differs when run alone"
+
+
 def test_zero_tokens_keeps_state(kda):
     inp = synthetic.prefill_inputs([0, 0], 2, torch.bfloat16, seed=23, s0_std=0.3, device="cuda")
     o, Sf = kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta, inp.cu_seqlens,
