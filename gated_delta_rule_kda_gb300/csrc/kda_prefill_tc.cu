@@ -1503,8 +1503,11 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
 template <typename Tout, bool kLayer, bool kCkpt, bool kHeadDecay, bool kUnb>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ Params p) {
     extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // The map starts at the first 1024-byte boundary of the dynamic window (the swizzled
+    // tiles need it).  The offset is added to the array itself, not through an integer
+    // round trip, so that the compiler keeps every access in the shared address space
+    // (32-bit shared loads and stores instead of generic ones).
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + S_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + S_TSLOT);
     const int tid = threadIdx.x, warp = tid >> 5;
