@@ -62,8 +62,8 @@ E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the ke
 # kernel is byte-identical: comments, host code).
 TRAFFIC = {
     "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-                "eb65d12c9d4f46b55e0e5a7251f643b1ba2cea1338a0536c8cb45b19034c43e5",
-                (252.557312e6 + 37.461248e6) / (2048 * 96)),
+                "97e409e9deecfbdedbc6c10149ab48bf3cac264e9e0a0ff5bb85eb405c4adeb2",
+                (252.55808e6 + 37.754368e6) / (2048 * 96)),
     # decode kernels: the difference of captures at 128 and 64 requests (both above L2), so
     # that the written lines still in L2 at the end of a launch cancel
     # (profiles/decode_traffic_B64_B128_H96.md)
@@ -89,8 +89,8 @@ TRAFFIC = {
                                    ((903500288 - 451118336) + (784547584 - 361533952)) / (64 * 96)),
     # the layer mode of the tensor-core kernel (profiles/layer_core_kernel_T2048_H96.md)
     "layer": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-              "eb65d12c9d4f46b55e0e5a7251f643b1ba2cea1338a0536c8cb45b19034c43e5",
-              (252.798976e6 + 37.718528e6) / (2048 * 96)),
+              "97e409e9deecfbdedbc6c10149ab48bf3cac264e9e0a0ff5bb85eb405c4adeb2",
+              (252.819968e6 + 38.206464e6) / (2048 * 96)),
 }
 # GB300's nominal HBM3e bandwidth (NVIDIA's product figure), reported beside the measured copy
 # bandwidth: a kernel that streams a little faster than torch's copy_ reads above 1.0 of the
