@@ -126,13 +126,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_tokens_kernel(const 
             const void *src;
             __nv_bfloat16 *dst;
             if (row < 3 * rows_x) {
-                const int s = row / rows_x, r = row % rows_x;
+                // stream s and window row r of `row` (compares: no division by a runtime value)
+                int s = 0, r = row;
+                if (r >= rows_x) {
+                    r -= rows_x;
+                    s = 1;
+                    if (r >= rows_x) {
+                        r -= rows_x;
+                        s = 2;
+                    }
+                }
                 dst = &sm.x[s][r][4 * qd];
                 src = r < kHist ? cpool + ((size_t)(3 * s + (kHist - 1 - r)) * HD + (size_t)h * kD + 4 * qd)
                                 : (s == 0 ? a.qp : s == 1 ? a.kp : a.vp) +
                                       (((size_t)(t_begin + r - kHist) * H + h) * kD + 4 * qd);
             } else {
-                const int rr = row - 3 * rows_x, which = rr / ntok, r = rr % ntok;
+                const int rr = row - 3 * rows_x, which = rr >= ntok ? 1 : 0, r = rr - which * ntok;
                 dst = which == 0 ? &sm.z[r][4 * qd] : &sm.g[r][4 * qd];
                 src = (which == 0 ? a.z : a.g) + (((size_t)(t_begin + r) * H + h) * kD + 4 * qd);
             }
