@@ -21,9 +21,10 @@
 //
 // Layout: 256 threads per CTA, two CTAs per SM.  Warp w owns state rows [16w, 16w+16);
 // lane l owns columns [4l, 4l+4).  Tokens are copied kTB at a time and widened to fp32
-// once per batch.  Per token: decay and the two column reductions (packed fp32x2), one
-// barrier, then every warp forms u for its own columns from the partials and applies the
-// rank-1 write; lanes 0-15 of each warp write 16 columns of o~.
+// once per batch.  Per token: decay and the two column reductions (packed fp32x2), a
+// barrier, then warp w finishes columns [16w, 16w+16) once (lanes 0-15 u = beta (v - r),
+// lanes 16-31 o~), a barrier, and every warp reads u for its own columns and applies the
+// rank-1 write.
 #include "kda_common.cuh"
 #include "tc_primitives.cuh"
 
@@ -65,9 +66,6 @@ __device__ __forceinline__ float2 lo2(float4 x) { return make_float2(x.x, x.y); 
 __device__ __forceinline__ float2 hi2(float4 x) { return make_float2(x.z, x.w); }
 __device__ __forceinline__ float4 cat4(float2 a, float2 b) { return make_float4(a.x, a.y, b.x, b.y); }
 __device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
-__device__ __forceinline__ float4 add4(float4 a, float4 b) {
-    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-}
 
 // Shared memory (dynamic): the next unit's state, the batch as fp32 (q, k, v, alpha) and as
 // copied (q, k, v in the input type, log alpha), beta, and the per-warp column partials of r
@@ -80,6 +78,7 @@ struct Smem {
     float rla[kTB][kD];
     float rb[kTB], b[kTB];
     float red_r[2][kWarps][kD], red_p[2][kWarps][kD];
+    float u[2][kD];  // u of every column, double-buffered by token parity
     float kq[2];
     uint64_t bar;
 };
@@ -248,29 +247,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_tokens_kernel(con
                     if (lane == 0) sm.kq[par] = kq;
                 }
                 __syncthreads();
-                // u = beta (v - r) for this lane's four columns (the same values in every
-                // warp); lanes 0-15 of warp w write o~ = scale (p + (k.q) u) of column
-                // 16 w + lane.
-                float4 rr = *reinterpret_cast<const float4 *>(&sm.red_r[par][0][4 * lane]);
+                // Warp w finishes columns 16 w .. 16 w + 15 once: lanes 0-15 sum r over the
+                // warps' partials and form u = beta (v - r), lanes 16-31 sum p and write
+                // o~ = scale (p + (k.q) u) with u from their partner lane.  u goes to shared
+                // memory, and after a second barrier each lane reads its four columns of it.
+                {
+                    const int c = 16 * warp + (lane & 15);
+                    const float(*part)[kD] = lane < 16 ? sm.red_r[par] : sm.red_p[par];
+                    float x = 0.f;
 #pragma unroll
-                for (int w = 1; w < kWarps; ++w)
-                    rr = add4(rr, *reinterpret_cast<const float4 *>(&sm.red_r[par][w][4 * lane]));
-                const float4 v4 = *reinterpret_cast<const float4 *>(&sm.v[tt][4 * lane]);
-                const float bt = sm.b[tt];
-                const float4 u4 = make_float4(bt * (v4.x - rr.x), bt * (v4.y - rr.y),
-                                              bt * (v4.z - rr.z), bt * (v4.w - rr.w));
-                if (lane < 16) {
-                    const int c = 16 * warp + lane;
-                    float rc = 0.f, pc = 0.f;
-#pragma unroll
-                    for (int w = 0; w < kWarps; ++w) {
-                        rc += sm.red_r[par][w][c];
-                        pc += sm.red_p[par][w][c];
-                    }
-                    const float uc = bt * (sm.v[tt][c] - rc);
-                    Elem<Tout>::store(o + ((size_t)(t0 + tt) * H + cur.h) * kD + c,
-                                      a.scale * fmaf(sm.kq[par], uc, pc));
+                    for (int w = 0; w < kWarps; ++w) x += part[w][c];
+                    const float uc = sm.b[tt] * (sm.v[tt][c] - x);  // lanes 0-15
+                    const float uo = __shfl_sync(0xffffffffu, uc, lane & 15);
+                    if (lane < 16)
+                        sm.u[par][c] = uc;
+                    else
+                        Elem<Tout>::store(o + ((size_t)(t0 + tt) * H + cur.h) * kD + c,
+                                          a.scale * fmaf(sm.kq[par], uo, x));
                 }
+                __syncthreads();
+                const float4 u4 = *reinterpret_cast<const float4 *>(&sm.u[par][4 * lane]);
                 // Rank-1 write S = S' + k u^T.
                 const float2 u01 = lo2(u4), u23 = hi2(u4);
 #pragma unroll
