@@ -21,8 +21,9 @@
 // state streams into registers (warp w owns rows [16w, 16w+16), lane l columns
 // [4l, 4l+4)).  Front end: two tasks per token, (q, k) and (v, decay), over the warps,
 // lane l channels [4l, 4l+4), so each token's L2 sums are warp reductions.
-// Recurrence: per token the decay and both column reductions (packed fp32x2), one CTA
-// barrier, u for each lane's columns from the per-warp partials, the rank-1 write.  Gate:
+// Recurrence: per token the decay and both column reductions (packed fp32x2), a CTA
+// barrier, warp w finishing columns [16w, 16w+16) once (u and o~), a barrier, the rank-1
+// write with each lane's four columns of u.  Gate:
 // warp w again takes tokens w and w + 8.
 #include "kda_common.cuh"
 #include "tc_primitives.cuh"
@@ -52,9 +53,6 @@ __device__ __forceinline__ float2 lo2(float4 x) { return make_float2(x.x, x.y); 
 __device__ __forceinline__ float2 hi2(float4 x) { return make_float2(x.z, x.w); }
 __device__ __forceinline__ float4 cat4(float2 a, float2 b) { return make_float4(a.x, a.y, b.x, b.y); }
 __device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
-__device__ __forceinline__ float4 add4(float4 a, float4 b) {
-    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-}
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
@@ -84,6 +82,7 @@ struct Smem {
     float4 cw[3][4][32];  // this head's taps (w0 .. w3) of channel 4 l + e at [stream][e][l]
     float b[kMaxTok];
     float red_r[2][kWarps][kD], red_p[2][kWarps][kD];
+    float u[2][kD];  // u of every column, double-buffered by token parity
     float kq[2];
 };
 
@@ -241,24 +240,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_layer_tokens_kernel(const 
             if (lane == 0) sm.kq[par] = kq;
         }
         __syncthreads();
-        float4 rr = *reinterpret_cast<const float4 *>(&sm.red_r[par][0][4 * lane]);
+        // Warp w finishes columns 16 w .. 16 w + 15 once: lanes 0-15 sum r over the warps'
+        // partials and form u = beta (v - r), lanes 16-31 sum p and form o~ with u from their
+        // partner lane; after a second barrier each lane reads its four columns of u.
+        {
+            const int c = 16 * warp + (lane & 15);
+            const float(*part)[kD] = lane < 16 ? sm.red_r[par] : sm.red_p[par];
+            float x = 0.f;
 #pragma unroll
-        for (int w = 1; w < kWarps; ++w)
-            rr = add4(rr, *reinterpret_cast<const float4 *>(&sm.red_r[par][w][4 * lane]));
-        const float4 v4 = *reinterpret_cast<const float4 *>(&sm.v[tt][4 * lane]);
-        const float bt = sm.b[tt];
-        const float4 u4 = make_float4(bt * (v4.x - rr.x), bt * (v4.y - rr.y), bt * (v4.z - rr.z),
-                                      bt * (v4.w - rr.w));
-        if (lane < 16) {  // o~ of column 16 w + lane
-            const int c = 16 * warp + lane;
-            float rc = 0.f, pc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                rc += sm.red_r[par][w][c];
-                pc += sm.red_p[par][w][c];
-            }
-            sm.ot[tt][c] = a.scale * fmaf(sm.kq[par], bt * (sm.v[tt][c] - rc), pc);
+            for (int w = 0; w < kWarps; ++w) x += part[w][c];
+            const float uc = sm.b[tt] * (sm.v[tt][c] - x);  // lanes 0-15
+            const float uo = __shfl_sync(0xffffffffu, uc, lane & 15);
+            if (lane < 16)
+                sm.u[par][c] = uc;
+            else
+                sm.ot[tt][c] = a.scale * fmaf(sm.kq[par], uo, x);
         }
+        __syncthreads();
+        const float4 u4 = *reinterpret_cast<const float4 *>(&sm.u[par][4 * lane]);
         const float2 u01 = lo2(u4), u23 = hi2(u4);
 #pragma unroll
         for (int i4 = 0; i4 < kRowsPerWarp; i4 += 4) {
