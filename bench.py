@@ -76,17 +76,17 @@ TRAFFIC = {
     # a few tokens per request (4, the bench leg's draft), same difference method
     # (profiles/decode_tokens_traffic_B64_B128_H96.md)
     "decode_tokens_verify": ("gated_delta_rule_kda_gb300/csrc/kda_decode_tokens.cu",
-                             "85e8a08ee610b59f11a965b8d2397b2e6fe9844ffd3524b82120926693c439d2",
-                             ((868478464 - 434237952) + (14044416 - 7197952)) / (64 * 96)),
+                             "3232adf7ab34665c383f704299e401b80f84f6d70b26b44cb953a7491b6aa8f0",
+                             ((868494080 - 434240256) + (14455040 - 7170560)) / (64 * 96)),
     "decode_tokens_replay": ("gated_delta_rule_kda_gb300/csrc/kda_decode_tokens.cu",
-                             "85e8a08ee610b59f11a965b8d2397b2e6fe9844ffd3524b82120926693c439d2",
-                             ((868482304 - 434240768) + (755365120 - 346715392)) / (64 * 96)),
+                             "3232adf7ab34665c383f704299e401b80f84f6d70b26b44cb953a7491b6aa8f0",
+                             ((868481024 - 434250752) + (755483136 - 346855936)) / (64 * 96)),
     "decode_layer_tokens_verify": ("gated_delta_rule_kda_gb300/csrc/kda_decode_layer_tokens.cu",
-                                   "e83fc7ca81254769df6bb07fa8f05a1b7e38552aa3dd2833214bb34876169960",
-                                   ((897444352 - 449020160) + (12886016 - 5880064)) / (64 * 96)),
+                                   "a264d1f312ef272f361cf3e1ae5a121e93ce66e1d325810b841455ed33228cc7",
+                                   ((897339648 - 449056000) + (12546304 - 6044928)) / (64 * 96)),
     "decode_layer_tokens_replay": ("gated_delta_rule_kda_gb300/csrc/kda_decode_layer_tokens.cu",
-                                   "e83fc7ca81254769df6bb07fa8f05a1b7e38552aa3dd2833214bb34876169960",
-                                   ((903500288 - 451118336) + (784547584 - 361533952)) / (64 * 96)),
+                                   "a264d1f312ef272f361cf3e1ae5a121e93ce66e1d325810b841455ed33228cc7",
+                                   ((902062080 - 450789632) + (784907008 - 361729792)) / (64 * 96)),
     # the layer mode of the tensor-core kernel (profiles/layer_core_kernel_T2048_H96.md)
     "layer": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
               "97e409e9deecfbdedbc6c10149ab48bf3cac264e9e0a0ff5bb85eb405c4adeb2",
