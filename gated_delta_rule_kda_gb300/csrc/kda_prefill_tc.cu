@@ -132,8 +132,9 @@ constexpr int kNumBars = 13;
 // ---- TMEM column map (512 columns) -----------------------------------------
 constexpr uint32_t TM_ST = 0;    // state X^T (lane c, column j), fp32
 constexpr uint32_t TM_OPS = 128; // M3's A operand S0^T hi (64) | lo (64); then U^T hi (16) | lo (16)
-constexpr uint32_t TM_D3A = 256; // M3, K steps 0-3: [(W S0)^T | (Q~ S0)^T (+ M4)]
-constexpr uint32_t TM_D3B = 320; // M3, K steps 4-7
+constexpr uint32_t TM_D3A = 256; // M3 [(W S0)^T | (Q~ S0)^T (+ M4)]: K steps 0-3 (prefill),
+                                 // the hi.hi and lo.hi products (layer mode)
+constexpr uint32_t TM_D3B = 320; // M3: K steps 4-7 (prefill), the hi.lo products (layer mode)
 constexpr uint32_t TM_DG = 384;  // Gram, K steps 0-3
 constexpr uint32_t TM_DU = 416;  // Gram, K steps 4-7
 constexpr uint32_t TM_UT = 448;  // U~^T (32 columns)
@@ -1303,9 +1304,32 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
             }
         }
         publish(kChainBar);
-        if (tid == kCA || tid == kCB) {
-            // M3: [(W S0)^T | (Q~ S0)^T] = S0^T [W ; Q~]^T, K steps 0-3 -> D3A, 4-7 -> D3B
-            // ([W ; Q~] read MN-major: K step k = rows 16 k .. 16 k + 15 of the key-channel-major tile)
+        // M3: [(W S0)^T | (Q~ S0)^T] = S0^T [W ; Q~]^T ([W ; Q~] read MN-major: K step k = rows
+        // 16 k .. 16 k + 15 of the key-channel-major tile).  The tensor pipe shares its slots
+        // among the threads issuing at once, and M3 runs while the prep group issues its Gram
+        // from two threads.  The prefill, where this group sets the pace, issues M3 from two
+        // threads too (K steps 0-3 -> D3A, 4-7 -> D3B, three products of N = 64 each).  Layer
+        // mode, where the prep group sets it, issues M3 from one thread as 16 MMAs: S0 hi .
+        // [B hi | B lo] (N = 128 through the descriptor's second 64-element block, 16 KB on) into
+        // D3A (hi.hi) and D3B (hi.lo), then S0 lo . B hi (N = 64) onto D3A; fewer, wider MMAs
+        // and a larger share of the pipe for the Gram.  Either way the U split and the readout
+        // read D3A + D3B.
+        if constexpr (kLayer) {
+            if (tid == kCA) {
+                const uint32_t id128 = idesc_bf16_f32(128, 128) | kIdescBMN;
+                const uint32_t id64 = idesc_bf16_f32(128, 64) | kIdescBMN;
+                const uint32_t bh = smem_u32(wq);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t bd = sw128_desc_mn(bh + 2048 * k, 16384);
+                    mma_bf16_tmem_a(tb + TM_D3A, tb + TM_OPS + 8 * k, bd, id128, k > 0);
+                    mma_bf16_tmem_a(tb + TM_D3A, tb + TM_OPS + 64 + 8 * k, bd, id64, 1);
+                }
+                mma_commit(bar + B_CA);
+            } else if (tid == kCB) {
+                mma_commit(bar + B_CB);  // (no products: keeps B_CB at one phase per product group)
+            }
+        } else if (tid == kCA || tid == kCB) {
             const uint32_t id = idesc_bf16_f32(128, 64) | kIdescBMN;
             const int s0 = tid == kCA ? 0 : 4;
             const uint32_t d = tb + (tid == kCA ? TM_D3A : TM_D3B);
