@@ -161,6 +161,43 @@ def test_fused_full_varlen_sampled_heads(kda):
     assert_fused_o_tilde_close(kda, inp, ref_ot, heads)
 
 
+@pytest.mark.parametrize("entry", ["kda_layer_core_fused", "kda_layer_core_fused_unbounded_decay"])
+def test_fused_varlen_bit_exact_packing(kda, entry):
+    """The fused layer core gives a sequence the same bits alone, packed, or packed in another
+    order (so its convolution never reads across a sequence boundary of the packed layout), and
+    leaves the output rows around the batch untouched; for both gates."""
+    fn = getattr(kda, entry)
+    lens = [77, 200, 3, 64, 0, 129, 33]
+    H = 3
+    inp = synthetic.layer_inputs(lens, H, seed=46, s0_std=0.1, device="cuda")
+    T = int(inp.cu_seqlens[-1])
+    canary = 8
+    o_buf = torch.full((T + 2 * canary, H, 128), 1234.5, dtype=torch.bfloat16, device="cuda")
+    o = o_buf[canary:canary + T]
+    _, Sf = fn(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b, inp.beta_logit, inp.g,
+               inp.cu_seqlens, inp.S0, o=o)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status()[0] == 0
+    assert (o_buf[:canary] == 1234.5).all() and (o_buf[canary + T:] == 1234.5).all()
+    cu = inp.cu_seqlens.tolist()
+    for n, L in enumerate(lens):  # each sequence alone
+        a, b = cu[n], cu[n + 1]
+        solo_cu = torch.tensor([0, L], dtype=torch.int32, device="cuda")
+        o_n, S_n = fn(inp.qp[a:b], inp.kp[a:b], inp.vp[a:b], inp.conv_w, inp.z[a:b], inp.A, inp.b,
+                      inp.beta_logit[a:b], inp.g[a:b], solo_cu, inp.S0[n:n + 1].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(o_n, o[a:b]), f"sequence {n} output differs when run alone"
+        assert torch.equal(S_n[0], Sf[n]), f"sequence {n} state differs when run alone"
+    perm = [5, 2, 0, 6, 4, 3, 1]  # the same sequences packed in another order
+    idx = torch.cat([torch.arange(cu[n], cu[n + 1]) for n in perm]).cuda()
+    cu_p = synthetic.cu_from_lengths([lens[n] for n in perm], "cuda")
+    pick = lambda t: t[idx].contiguous()
+    o_p, S_p = fn(pick(inp.qp), pick(inp.kp), pick(inp.vp), inp.conv_w, pick(inp.z), inp.A, inp.b,
+                  pick(inp.beta_logit), pick(inp.g), cu_p, inp.S0[perm].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(o_p, o[idx]) and torch.equal(S_p, Sf[perm])
+
+
 def test_fused_deterministic(kda):
     inp = synthetic.layer_inputs([300, 77], 3, seed=45, device="cuda")
     a, Sa = kda.kda_layer_core_fused(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b,
