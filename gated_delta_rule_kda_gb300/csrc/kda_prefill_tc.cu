@@ -880,40 +880,47 @@ __device__ __forceinline__ void prep_group(const Params &p, unsigned char *sm, u
                 for (int m = 0; m < 16; ++m) sT[(o + m) * kLdT + o + j] = x[m];
             }
             group_sync(kPrepBar);
-            {  // 32 x 32: T_10 = -T_11 (A_10 T_00), one entry per thread (row 16 + r, column i)
-                const int r = pt >> 4, i = pt & 15;
-                float x0 = 0.f, x1 = 0.f;
+            if constexpr (kLayer) {
+                // Layer mode: this group sets the pace there, so the chain group forms T_10 and
+                // Tb itself; A_10 goes to T's upper-right block (which T never uses) for it.
+                const int r = pt >> 4, m = pt & 15;
+                sT[r * kLdT + 16 + m] = sAt[m * 32 + 16 + r];
+            } else {
+                {  // 32 x 32: T_10 = -T_11 (A_10 T_00), one entry per thread (row 16 + r, column i)
+                    const int r = pt >> 4, i = pt & 15;
+                    float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-                for (int m = 0; m < 16; m += 2) {
-                    x0 = fmaf(sAt[m * 32 + 16 + r], sT[m * kLdT + i], x0);
-                    x1 = fmaf(sAt[(m + 1) * 32 + 16 + r], sT[(m + 1) * kLdT + i], x1);
+                    for (int m = 0; m < 16; m += 2) {
+                        x0 = fmaf(sAt[m * 32 + 16 + r], sT[m * kLdT + i], x0);
+                        x1 = fmaf(sAt[(m + 1) * 32 + 16 + r], sT[(m + 1) * kLdT + i], x1);
+                    }
+                    // X = A_10 T_00 (row r, column i) goes to T's upper-right block, which T never uses
+                    sT[r * kLdT + 16 + i] = x0 + x1;
+                    group_sync(kPrepBar);
+                    float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                    for (int m = 0; m < 16; m += 2) {
+                        y0 = fmaf(sT[(16 + r) * kLdT + 16 + m], sT[m * kLdT + 16 + i], y0);
+                        y1 = fmaf(sT[(16 + r) * kLdT + 17 + m], sT[(m + 1) * kLdT + 16 + i], y1);
+                    }
+                    sT[(16 + r) * kLdT + i] = -(y0 + y1);
                 }
-                // X = A_10 T_00 (row r, column i) goes to T's upper-right block, which T never uses
-                sT[r * kLdT + 16 + i] = x0 + x1;
                 group_sync(kPrepBar);
-                float y0 = 0.f, y1 = 0.f;
+                // ---- Tb = T diag(beta) (32 rows x K 32) -> slot s: one 16-byte chunk per thread ----
+                if (pt < 128) {
+                    const int r = pt >> 2, cc = pt & 3;
+                    float x[8];
 #pragma unroll
-                for (int m = 0; m < 16; m += 2) {
-                    y0 = fmaf(sT[(16 + r) * kLdT + 16 + m], sT[m * kLdT + 16 + i], y0);
-                    y1 = fmaf(sT[(16 + r) * kLdT + 17 + m], sT[(m + 1) * kLdT + 16 + i], y1);
+                    for (int e = 0; e < 8; ++e) {
+                        const int i = 8 * cc + e;
+                        x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
+                    }
+                    // a quarter-warp holds rows r and r + 1: odd rows store their lo chunk first, so
+                    // that each instruction's 8 chunks fall in 8 distinct 16-byte bank groups
+                    unsigned char *tbs = sm + S_TB + s * TB_SIZE;
+                    store_split_chunk(tbs + sw128_chunk_offset(32, r, cc), tbs + sw128_chunk_offset(32, r, 4 + cc),
+                                      x, (r & 1) != 0);
                 }
-                sT[(16 + r) * kLdT + i] = -(y0 + y1);
-            }
-            group_sync(kPrepBar);
-            // ---- Tb = T diag(beta) (32 rows x K 32) -> slot s: one 16-byte chunk per thread ----
-            if (pt < 128) {
-                const int r = pt >> 2, cc = pt & 3;
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = 8 * cc + e;
-                    x[e] = i <= r ? sT[r * kLdT + i] * beta_s[i] : 0.f;
-                }
-                // a quarter-warp holds rows r and r + 1: odd rows store their lo chunk first, so
-                // that each instruction's 8 chunks fall in 8 distinct 16-byte bank groups
-                unsigned char *tbs = sm + S_TB + s * TB_SIZE;
-                store_split_chunk(tbs + sw128_chunk_offset(32, r, cc), tbs + sw128_chunk_offset(32, r, 4 + cc),
-                                  x, (r & 1) != 0);
             }
         }
         if constexpr (kUnb) {
@@ -1133,6 +1140,56 @@ __device__ __forceinline__ void chain_group(const Params &p, unsigned char *sm, 
                 mbar_arrive(bar + B_EMPTY + s);
             }
         } else {
+        if constexpr (kLayer) {
+            // ---- layer mode: T_10 = -T_11 (A_10 T_00) and Tb = T diag(beta) for slot s, here
+            //      (the prep group, the slower one in layer mode, left T_00, T_11 and A_10 in the
+            //      slot's T: A_10 in the upper-right block, which T never uses) ----
+            float *sTs = reinterpret_cast<float *>(sm + S_TS) + s * (32 * kLdT);
+            const float *beta_s = reinterpret_cast<const float *>(sm + S_BETA + 128 * s);
+            const int r = tid >> 4, i = tid & 15;  // entries (r, i) and (r + 8, i)
+            float x[2];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {  // X = A_10 T_00
+                const int rr = r + 8 * hh;
+                float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; m += 2) {
+                    x0 = fmaf(sTs[rr * kLdT + 16 + m], sTs[m * kLdT + i], x0);
+                    x1 = fmaf(sTs[rr * kLdT + 17 + m], sTs[(m + 1) * kLdT + i], x1);
+                }
+                x[hh] = x0 + x1;
+            }
+            group_sync(kChainBar);  // every read of A_10 is done: X goes in its place
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) sTs[(r + 8 * hh) * kLdT + 16 + i] = x[hh];
+            group_sync(kChainBar);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {  // T_10 = -T_11 X
+                const int rr = r + 8 * hh;
+                float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; m += 2) {
+                    y0 = fmaf(sTs[(16 + rr) * kLdT + 16 + m], sTs[m * kLdT + 16 + i], y0);
+                    y1 = fmaf(sTs[(16 + rr) * kLdT + 17 + m], sTs[(m + 1) * kLdT + 16 + i], y1);
+                }
+                sTs[(16 + rr) * kLdT + i] = -(y0 + y1);
+            }
+            group_sync(kChainBar);
+            {  // Tb (32 rows x K 32) -> slot s: one 16-byte chunk per thread
+                const int r2 = tid >> 2, cc = tid & 3;
+                float xb[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i2 = 8 * cc + e;
+                    xb[e] = i2 <= r2 ? sTs[r2 * kLdT + i2] * beta_s[i2] : 0.f;
+                }
+                unsigned char *tbs = sm + S_TB + s * TB_SIZE;
+                store_split_chunk(tbs + sw128_chunk_offset(32, r2, cc),
+                                  tbs + sw128_chunk_offset(32, r2, 4 + cc), xb, (r2 & 1) != 0);
+            }
+            fence_proxy_async_smem();  // Tb is M2's and M2b's operand
+            group_sync(kChainBar);
+        }
         // (Tb, W's k E and Q~ came with the slot: the prep group published them)
         if (tid == kCA) {  // M2: U~^T = V^T Tb^T  (V read MN-major: exact bf16, or hi + lo)
             const uint32_t th = smem_u32(sm + S_TB + s * TB_SIZE);
