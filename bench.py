@@ -62,8 +62,8 @@ E2E_SEGMENTS = 8  # end-to-end leg: token ranges per step (copies overlap the ke
 # kernel is byte-identical: comments, host code).
 TRAFFIC = {
     "prefill": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-                "16fb4e6c5f9355f2c989efe1fd82bb50f724ad679a1b258faa2388e1394d800d",
-                (252.717568e6 + 38.153728e6) / (2048 * 96)),
+                "96aa5677145d985ef43f0bd70fb60eebd6361d95ec47882349e5b26bf6da0c78",
+                (252.561408e6 + 37.64352e6) / (2048 * 96)),
     # decode kernels: the difference of captures at 128 and 64 requests (both above L2), so
     # that the written lines still in L2 at the end of a launch cancel
     # (profiles/decode_traffic_B64_B128_H96.md)
@@ -89,8 +89,8 @@ TRAFFIC = {
                                    ((902062080 - 450789632) + (784907008 - 361729792)) / (64 * 96)),
     # the layer mode of the tensor-core kernel (profiles/layer_core_kernel_T2048_H96.md)
     "layer": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
-              "16fb4e6c5f9355f2c989efe1fd82bb50f724ad679a1b258faa2388e1394d800d",
-              (252.797184e6 + 37.745664e6) / (2048 * 96)),
+              "96aa5677145d985ef43f0bd70fb60eebd6361d95ec47882349e5b26bf6da0c78",
+              (252.79872e6 + 37.424384e6) / (2048 * 96)),
 }
 # GB300's nominal HBM3e bandwidth (NVIDIA's product figure), reported beside the measured copy
 # bandwidth: a kernel that streams a little faster than torch's copy_ reads above 1.0 of the
