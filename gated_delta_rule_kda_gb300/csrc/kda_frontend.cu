@@ -11,10 +11,10 @@
 // floor K3 puts under it"), log_alpha = -e^{A_h} softplus(z + b), in (-inf, 0).
 // Output gate (same equation list): o^g = sigmoid(g) * o~ / sqrt(mean(o~^2) + eps).
 //
-// Both kernels give one warp to one (token, head) row of 128 channels: lane l
-// owns channels [4l, 4l+4), so every row access is one coalesced 256-byte
-// (bf16) or 512-byte (fp32) transaction and the per-head reductions are warp
-// shuffles.
+// Lane l owns channels [4l, 4l+4) of a (token, head) row, so every row access is one
+// coalesced 256-byte (bf16) or 512-byte (fp32) transaction and the per-head reductions are
+// warp shuffles.  The gate gives one warp one row; the front end gives one warp two
+// consecutive tokens of one head.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -37,71 +37,100 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
-// Start of the sequence that owns token t (largest n with cu[n] <= t).
-__device__ __forceinline__ int seq_start(const int32_t *cu, int num_seqs, int t) {
-    int lo = 0, hi = num_seqs;  // invariant: cu[lo] <= t < cu[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cu[mid] <= t) lo = mid;
-        else hi = mid;
-    }
-    return cu[lo];
-}
-
+// One warp takes tokens t0 = 2 tp and t0 + 1 of head h: the head's taps are loaded once for
+// both, and the five input rows t0 - 3 .. t0 + 1 once per stream (the two tokens' windows
+// overlap in three of them).  The rows are requested before the search for the sequence start,
+// so the two overlap; rows before a token's sequence start are zeroed afterwards (token t0 + 1
+// may open the next sequence).
 template <typename Tout>
 __global__ void __launch_bounds__(kThreads)
 frontend_kernel(FrontendArgs a) {
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-    const int H = a.num_heads;
-    if (row >= (int64_t)a.total_tokens * H) return;
-    const int t = (int)(row / H), h = (int)(row % H);
-    const int start = seq_start(a.cu_seqlens, a.num_seqs, t);
+    const int H = a.num_heads, T = a.total_tokens;
+    const int64_t wi = (int64_t)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (wi >= (int64_t)((T + 1) / 2) * H) return;
+    const int tp = (int)(wi / H), h = (int)(wi - (int64_t)tp * H);
+    const int t0 = 2 * tp;
+    const bool two = t0 + 1 < T;
     const int c0 = 4 * lane;
     const __nv_bfloat16 *src[3] = {a.qp, a.kp, a.vp};
     void *dst[3] = {a.q_hat, a.k_hat, a.v_out};
+    auto row_ptr = [&](const __nv_bfloat16 *base, int t) {
+        return base + ((size_t)t * H + h) * kD + c0;
+    };
+    // stream 0's rows first: in flight while the sequence start is looked up
+    float4 xr[5];  // rows t0 - 3 .. t0 + 1
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const int t = t0 - 3 + k;
+        xr[k] = t >= 0 && t < T ? load4(row_ptr(src[0], t)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    // starts of t0's sequence and of t0 + 1's (t0 + 1 opens the next one when it is a cu entry)
+    int lo = 0, hi = a.num_seqs;  // invariant: cu[lo] <= t0 < cu[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (a.cu_seqlens[mid] <= t0) lo = mid;
+        else hi = mid;
+    }
+    const int start0 = a.cu_seqlens[lo];
+    const int start1 = a.cu_seqlens[lo + 1] == t0 + 1 ? t0 + 1 : start0;
 
 #pragma unroll
     for (int s = 0; s < 3; ++s) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (s > 0) {
+#pragma unroll
+            for (int k = 0; k < 5; ++k) {
+                const int t = t0 - 3 + k;
+                xr[k] = t >= 0 && t < T ? load4(row_ptr(src[s], t)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
         const float *w = a.conv_w + ((size_t)s * H * kD + (size_t)h * kD + c0) * 4;
         float4 wt[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) wt[c] = *reinterpret_cast<const float4 *>(w + 4 * c);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            // taps before the sequence start read as zero (predicated, so all four loads of a
-            // stream are in flight at once)
-            const float4 x = t - j >= start ? load4(src[s] + ((size_t)(t - j) * H + h) * kD + c0)
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-            const float xs[4] = {x.x, x.y, x.z, x.w};
+        for (int u = 0; u < 2; ++u) {  // token t0 + u: taps j = 0..3 read row t0 + u - j
+            if (u == 1 && !two) break;
+            const int st = u == 0 ? start0 : start1;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float wj = j == 0 ? wt[c].x : j == 1 ? wt[c].y : j == 2 ? wt[c].z : wt[c].w;
-                acc[c] = fmaf(wj, xs[c], acc[c]);
+            for (int j = 0; j < 4; ++j) {
+                const int k = 3 + u - j;  // index of row t0 + u - j in xr
+                const bool in = t0 + u - j >= st;
+                const float xs[4] = {xr[k].x, xr[k].y, xr[k].z, xr[k].w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float wj = j == 0 ? wt[c].x : j == 1 ? wt[c].y : j == 2 ? wt[c].z : wt[c].w;
+                    acc[c] = fmaf(wj, in ? xs[c] : 0.f, acc[c]);
+                }
             }
+            float4 y = make_float4(siluf_(acc[0]), siluf_(acc[1]), siluf_(acc[2]), siluf_(acc[3]));
+            if (s < 2) {
+                const float ss = warp_sum(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w);
+                const float inv = rsqrtf(ss + a.l2_eps);
+                y.x *= inv; y.y *= inv; y.z *= inv; y.w *= inv;
+            }
+            store4(static_cast<Tout *>(dst[s]) + ((size_t)(t0 + u) * H + h) * kD + c0, y);
         }
-        float4 y = make_float4(siluf_(acc[0]), siluf_(acc[1]), siluf_(acc[2]), siluf_(acc[3]));
-        if (s < 2) {
-            const float ss = warp_sum(y.x * y.x + y.y * y.y + y.z * y.z + y.w * y.w);
-            const float inv = rsqrtf(ss + a.l2_eps);
-            y.x *= inv; y.y *= inv; y.z *= inv; y.w *= inv;
-        }
-        store4(static_cast<Tout *>(dst[s]) + (size_t)row * kD + c0, y);
     }
 
     const float eA = expf(a.A[h]);
-    const float4 z = load4(a.z + (size_t)row * kD + c0);
     float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
     if (a.b != nullptr) b = *reinterpret_cast<const float4 *>(a.b + (size_t)h * kD + c0);
     const bool ub = a.unbounded_decay != 0;
-    float4 la;
-    la.x = log_decay(eA, z.x + b.x, ub);
-    la.y = log_decay(eA, z.y + b.y, ub);
-    la.z = log_decay(eA, z.z + b.z, ub);
-    la.w = log_decay(eA, z.w + b.w, ub);
-    *reinterpret_cast<float4 *>(a.log_alpha + (size_t)row * kD + c0) = la;
-    if (lane == 0) a.beta[row] = sigmoidf_(__bfloat162float(a.beta_logit[row]));
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        if (u == 1 && !two) break;
+        const size_t row = (size_t)(t0 + u) * H + h;
+        const float4 z = load4(a.z + row * kD + c0);
+        float4 la;
+        la.x = log_decay(eA, z.x + b.x, ub);
+        la.y = log_decay(eA, z.y + b.y, ub);
+        la.z = log_decay(eA, z.z + b.z, ub);
+        la.w = log_decay(eA, z.w + b.w, ub);
+        *reinterpret_cast<float4 *>(a.log_alpha + row * kD + c0) = la;
+        if (lane == 0) a.beta[row] = sigmoidf_(__bfloat162float(a.beta_logit[row]));
+    }
 }
 
 template <typename Tin, typename Tout>
@@ -127,9 +156,9 @@ gate_kernel(int64_t rows, const Tin *__restrict__ ot, const __nv_bfloat16 *__res
 }  // namespace
 
 cudaError_t launch_frontend(const FrontendArgs &a, cudaStream_t stream) {
-    const int64_t rows = (int64_t)a.total_tokens * a.num_heads;
-    if (rows == 0) return cudaSuccess;
-    const unsigned blocks = (unsigned)((rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    const int64_t warps = (int64_t)((a.total_tokens + 1) / 2) * a.num_heads;  // token pairs x heads
+    if (warps == 0) return cudaSuccess;
+    const unsigned blocks = (unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
     if (a.out_dtype == KDA_BF16) frontend_kernel<__nv_bfloat16><<<blocks, kThreads, 0, stream>>>(a);
     else frontend_kernel<float><<<blocks, kThreads, 0, stream>>>(a);
     return cudaGetLastError();
