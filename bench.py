@@ -470,7 +470,7 @@ def run_ours(args, world, rank, local):
     # S_final (chunk boundaries stay aligned, so the result is the single call's): the
     # inputs of segment i+1 travel host -> device on a copy stream while segment i
     # runs, and each finished segment's output goes back on two device -> host
-    # streams (one stream reaches only ~70 GB/s device -> host on this machine).
+    # streams (one stream has measured as low as ~70 GB/s device -> host).
     seg = T // E2E_SEGMENTS
     cu_seg = torch.tensor([0, seg], dtype=torch.int32, device=dev)
     h2d_stream = torch.cuda.Stream(device=dev)

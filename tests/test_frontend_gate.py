@@ -26,9 +26,12 @@ def small_layer(lens, H=4, seed=31):
     return inp
 
 
+# the second list puts several sequence starts (and an empty sequence) inside one warp's
+# group of consecutive tokens
+@pytest.mark.parametrize("lens", [[37, 1, 0, 90, 3], [1, 2, 1, 1, 0, 3, 1, 7, 1, 2, 5, 1]])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_frontend_matches_oracle(kda, out_dtype):
-    inp = small_layer([37, 1, 0, 90, 3])
+def test_frontend_matches_oracle(kda, out_dtype, lens):
+    inp = small_layer(lens)
     outs = kda.kda_frontend(inp.qp, inp.kp, inp.vp, inp.conv_w, inp.z, inp.A, inp.b,
                             inp.beta_logit, inp.cu_seqlens, 1e-6, out_dtype=out_dtype)
     torch.cuda.synchronize()
