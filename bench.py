@@ -87,6 +87,15 @@ TRAFFIC = {
     "decode_layer_tokens_replay": ("gated_delta_rule_kda_gb300/csrc/kda_decode_layer_tokens.cu",
                                    "a264d1f312ef272f361cf3e1ae5a121e93ce66e1d325810b841455ed33228cc7",
                                    ((902062080 - 450789632) + (784907008 - 361729792)) / (64 * 96)),
+    # the per-head decay instantiation (one log alpha per (token, head)) and the contents
+    # check: differences of captures at two sizes above L2
+    # (profiles/head_decay_prefill_and_check_traffic_H96.md)
+    "prefill_head_decay": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
+                           "96aa5677145d985ef43f0bd70fb60eebd6361d95ec47882349e5b26bf6da0c78",
+                           ((305234688 - 152663808) + (81304576 - 31443200)) / (2048 * 96)),
+    "check": ("gated_delta_rule_kda_gb300/csrc/kda_checks.cu",
+              "7b0b2e284c9fb61fdb605e513724e58d4e1da61af677c2a0e2a024e48482c146",
+              ((805327360 - 402670336) + (2753024 - 2741504)) / (8192 * 96)),
     # the layer mode of the tensor-core kernel (profiles/layer_core_kernel_T2048_H96.md)
     "layer": ("gated_delta_rule_kda_gb300/csrc/kda_prefill_tc.cu",
               "96aa5677145d985ef43f0bd70fb60eebd6361d95ec47882349e5b26bf6da0c78",
@@ -378,7 +387,8 @@ def run_ours(args, world, rank, local):
                                    "achieved": check_bytes / (ch_launch / 1e3) / 1e9,
                                    "peak": hbm, "unit": "GB/s",
                                    "frac": check_bytes / (ch_launch / 1e3) / 1e9 / hbm,
-                                   "traffic": None, "peak_kind": peak_kind,
+                                   "traffic": traffic_bytes("check", T * H),
+                                   "peak_kind": peak_kind,
                                    "kernel": "kda_check_prefill_inputs"}}
 
     # ---------------- the Gated DeltaNet case: one decay per (token, head) ----------------
@@ -397,7 +407,8 @@ def run_ours(args, world, rank, local):
                   "roofline": {"bound": "hbm", "achieved": hd_bytes / (hd_launch / 1e3) / 1e9,
                                "peak": hbm, "unit": "GB/s",
                                "frac": hd_bytes / (hd_launch / 1e3) / 1e9 / hbm,
-                               "traffic": None, "peak_kind": peak_kind,
+                               "traffic": traffic_bytes("prefill_head_decay", T * H),
+                               "peak_kind": peak_kind,
                                "kernel": "kda_prefill_head_decay"}}
     del la_head
 
@@ -739,6 +750,26 @@ def run_only(args, local):
         fn = lambda: kda.kda_prefill(inp.q, inp.k, inp.v, inp.log_alpha, inp.beta,
                                      inp.cu_seqlens, None, o=o, S_final=Sf)
         units = T
+    elif args.only == "prefill_head_decay":
+        # kda_prefill_head_decay on the prefill workload's inputs, one decay per (token, head):
+        # 2048 (--small) or 8192 tokens, or --tokens, 96 heads
+        T = args.tokens or (2048 if args.small else 8192)
+        inp = synthetic.prefill_inputs([T], 96, torch.bfloat16, seed=synthetic.BASE_SEED + 2,
+                                       device=dev)
+        la_head = inp.log_alpha[:, :, 0].contiguous()
+        o = torch.empty((T, 96, D), dtype=torch.bfloat16, device=dev)
+        Sf = torch.empty((1, 96, D, D), dtype=torch.float32, device=dev)
+        fn = lambda: kda.kda_prefill_head_decay(inp.q, inp.k, inp.v, la_head, inp.beta,
+                                                inp.cu_seqlens, None, o=o, S_final=Sf)
+        units = T
+    elif args.only == "check":
+        # kda_check_prefill_inputs over the prefill workload's log alpha (8192 tokens, or
+        # --tokens, 96 heads)
+        T = args.tokens or 8192
+        inp = synthetic.prefill_inputs([T], 96, torch.bfloat16, seed=synthetic.BASE_SEED + 2,
+                                       device=dev)
+        fn = lambda: kda.kda_check_prefill_inputs(inp.cu_seqlens, inp.log_alpha)
+        units = T
     elif args.only == "prefill_fp32":
         # the token-by-token kernel (fp32 inputs): 8 sequences x 1024 tokens (--small) or
         # 16 x 8192, 96 heads
@@ -824,7 +855,8 @@ def main():
                     help="skip the 131,072-token prefill leg (19 GB of inputs)")
     ap.add_argument("--skip-staged-layer-core", action="store_true",
                     help="time only the fused layer core, not the three-launch composition")
-    ap.add_argument("--only", choices=["prefill", "prefill_fp32", "decode", "decode_layer",
+    ap.add_argument("--only", choices=["prefill", "prefill_head_decay", "check", "prefill_fp32",
+                                       "decode", "decode_layer",
                                        "decode_tokens", "decode_layer_tokens", "layer",
                                        "staged_layer"],
                     default=None,
@@ -833,6 +865,8 @@ def main():
                     help="with --only: a smaller case sized for ncu captures")
     ap.add_argument("--batch", type=int, default=0,
                     help="with --only and a decode kind: this many requests")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="with --only prefill_head_decay / check: this many tokens")
     ap.add_argument("--write-back", type=int, default=1,
                     help="with --only decode_tokens / decode_layer_tokens: 0 verify, 1 replay")
     args = ap.parse_args()
