@@ -9,7 +9,8 @@
 // are transposed butterflies over the eight lanes: at each of three xor steps a
 // lane sends half of the partial sums it holds and keeps the other half, so it
 // ends with the full sum of one column (four shuffles for four columns); a
-// value per column goes back to all eight lanes in three more shuffles.
+// value per column goes back to all eight lanes in three more shuffles.  Each lane keeps its
+// four columns in a lane-dependent order (lane_order) that makes both free of selects.
 #pragma once
 
 #include "kda_common.cuh"
@@ -27,30 +28,35 @@ __device__ __forceinline__ int prow(int row) { return row + 4 * (row >> 4); }
 // Column of its quad whose full sum a lane holds after quad_reduce (row group rq = lane & 7).
 __device__ __forceinline__ int quad_col(int rq) { return 2 * ((rq >> 2) & 1) + ((rq >> 1) & 1); }
 
-// Sum of x (one partial sum per column of the quad) over the 8 lanes of a row-group set
-// (lanes that differ in bits 0-2): the lane returns the sum for column quad_col(rq).
-__device__ __forceinline__ float quad_reduce(float4 x, int rq) {
-    const bool hi = (rq & 4) != 0;  // keeps columns 2, 3; its partner keeps 0, 1
-    float a = hi ? x.z : x.x, b = hi ? x.w : x.y;
-    const float sa = hi ? x.x : x.z, sb = hi ? x.y : x.w;
-    a += __shfl_xor_sync(kFull, sa, 4);
-    b += __shfl_xor_sync(kFull, sb, 4);
-    const bool mid = (rq & 2) != 0;  // keeps the odd column of the pair
-    float c = mid ? b : a;
-    const float sc = mid ? a : b;
-    c += __shfl_xor_sync(kFull, sc, 2);
+// Register order of a lane's four columns.  Component m of the lane's float4s holds column
+// quad_col(rq) ^ m of its quad: first the column whose full sum the lane ends with, then that
+// column's pair partner, then the other pair in the same order.  With this order every step
+// of the butterflies below keeps components 0-1 and sends 2-3 (or keeps 0 and sends 1) on
+// every lane, so they need no lane-dependent selects.  The map is its own inverse.
+__device__ __forceinline__ float4 lane_order(float4 x, int jc) {
+    const bool b2 = (jc & 2) != 0, b1 = (jc & 1) != 0;
+    const float p0 = b2 ? x.z : x.x, p1 = b2 ? x.w : x.y;
+    const float p2 = b2 ? x.x : x.z, p3 = b2 ? x.y : x.w;
+    return b1 ? make_float4(p1, p0, p3, p2) : make_float4(p0, p1, p2, p3);
+}
+
+// Sum of y (one partial sum per column of the quad, in lane order) over the 8 lanes of a
+// row-group set (lanes that differ in bits 0-2): the lane returns the sum for column
+// quad_col(rq).  The xor-4 partner holds this lane's two columns in its components 2-3, the
+// xor-2 partner this lane's column in its component 1, the xor-1 partner the same column.
+__device__ __forceinline__ float quad_reduce(float4 y) {
+    const float a = y.x + __shfl_xor_sync(kFull, y.z, 4);
+    const float b = y.y + __shfl_xor_sync(kFull, y.w, 4);
+    float c = a + __shfl_xor_sync(kFull, b, 2);
     c += __shfl_xor_sync(kFull, c, 1);
     return c;
 }
 
-// The four columns' values to every lane of the row-group set, from x held for column
-// quad_col(rq) (lanes rq and rq ^ 1 hold the same column).
-__device__ __forceinline__ float4 quad_gather(float x, int rq) {
-    const float xo = __shfl_xor_sync(kFull, x, 2);  // the other column of the pair
-    const bool mid = (rq & 2) != 0;
-    const float p0 = mid ? xo : x, p1 = mid ? x : xo;  // columns 2 hi, 2 hi + 1
-    const float o0 = __shfl_xor_sync(kFull, p0, 4), o1 = __shfl_xor_sync(kFull, p1, 4);
-    return (rq & 4) ? make_float4(o0, o1, p0, p1) : make_float4(p0, p1, o0, o1);
+// The four columns' values to every lane of the row-group set, in lane order, from x held
+// for column quad_col(rq) (lanes rq and rq ^ 1 hold the same column).
+__device__ __forceinline__ float4 quad_gather(float x) {
+    const float xo = __shfl_xor_sync(kFull, x, 2);  // the pair partner column
+    return make_float4(x, xo, __shfl_xor_sync(kFull, x, 4), __shfl_xor_sync(kFull, xo, 4));
 }
 
 }  // namespace quads

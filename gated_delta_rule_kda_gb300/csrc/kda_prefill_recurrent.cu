@@ -13,7 +13,10 @@
 // over rows per token are transposed butterflies: at each of three xor steps a
 // lane sends half of the partial sums it holds and keeps the other half, so that
 // it ends with the full sum of one column (four shuffles for four columns); u is
-// gathered back to all eight lanes in three more shuffles.  No state ever leaves
+// gathered back to all eight lanes in three more shuffles.  Each lane keeps its four
+// columns in a lane-dependent register order (column quad_col(rq) ^ m in component m),
+// which lets every butterfly step run without lane-dependent selects; the order is
+// applied when the state is loaded and undone when it is stored.  No state ever leaves
 // registers until the sequence ends.
 //
 // Each token costs one pass over the state: the delta write and readout of
@@ -41,6 +44,7 @@ using quads::prow;
 using quads::quad_col;
 using quads::quad_gather;
 using quads::quad_reduce;
+using quads::lane_order;
 
 template <typename Tin, typename Tout, bool kCkpt, bool kHeadDecay>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
@@ -71,7 +75,8 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     if (S0 != nullptr) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
-            s[i] = *reinterpret_cast<const float4 *>(S0 + state_off + my_off + (size_t)i * kD);
+            s[i] = lane_order(*reinterpret_cast<const float4 *>(S0 + state_off + my_off + (size_t)i * kD),
+                              jc);
     } else {
 #pragma unroll
         for (int i = 0; i < kRows; ++i) s[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -138,7 +143,7 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     float4 u = make_float4(0.f, 0.f, 0.f, 0.f);  // the current token's u, all four columns
     // u of column jc from its prediction r (held for column jc) and token (B, tn)
     auto u_of = [&](const Batch &B, int tn, float rj) {
-        return quad_gather(B.b[tn] * (B.v[tn][4 * cq + jc] - rj), rq);
+        return quad_gather(B.b[tn] * (B.v[tn][4 * cq + jc] - rj));
     };
     if (t_begin < t_end) {
         fetch(t_begin);
@@ -166,7 +171,7 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                     r23 = tc::fma2(x23, k2, r23);
                 }
             }
-            u = u_of(sb[0], 0, quad_reduce(make_float4(r01.x, r01.y, r23.x, r23.y), rq));
+            u = u_of(sb[0], 0, quad_reduce(make_float4(r01.x, r01.y, r23.x, r23.y)));
         }
     }
     int cur = 0;
@@ -217,7 +222,7 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 if (kCkpt && snap != nullptr) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        *reinterpret_cast<float4 *>(snap + (size_t)(i + e) * kD) = s[i + e];
+                        *reinterpret_cast<float4 *>(snap + (size_t)(i + e) * kD) = lane_order(s[i + e], jc);
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {  // decay and prediction of token t + 1
@@ -230,8 +235,8 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                     r23 = tc::fma2(x23, n2, r23);
                 }
             }
-            const float pj = quad_reduce(make_float4(p01.x, p01.y, p23.x, p23.y), rq);
-            const float rj = quad_reduce(make_float4(r01.x, r01.y, r23.x, r23.y), rq);
+            const float pj = quad_reduce(make_float4(p01.x, p01.y, p23.x, p23.y));
+            const float rj = quad_reduce(make_float4(r01.x, r01.y, r23.x, r23.y));
             if ((rq & 1) == 0) s_o[tt][4 * cq + jc] = scale * pj;
             u = u_of(N, tn, rj);
         }
@@ -246,7 +251,7 @@ prefill_recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     if (S_final != nullptr) {
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
-            *reinterpret_cast<float4 *>(S_final + state_off + my_off + (size_t)i * kD) = s[i];
+            *reinterpret_cast<float4 *>(S_final + state_off + my_off + (size_t)i * kD) = lane_order(s[i], jc);
     }
 }
 
