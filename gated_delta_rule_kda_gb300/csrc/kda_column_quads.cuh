@@ -1,5 +1,5 @@
-// Column-quad layout of a 128 x 128 fp32 state held in registers, shared by the
-// token-by-token kernels (prefill and multi-token decode).
+// Column-quad layout of a 128 x 128 fp32 state held in registers, used by the
+// token-by-token prefill kernel.
 //
 // Value columns of the KDA state evolve independently: column c needs only k,
 // alpha, beta and v[c] of each token.  Eight adjacent lanes (row groups
@@ -9,8 +9,9 @@
 // are transposed butterflies over the eight lanes: at each of three xor steps a
 // lane sends half of the partial sums it holds and keeps the other half, so it
 // ends with the full sum of one column (four shuffles for four columns); a
-// value per column goes back to all eight lanes in three more shuffles.  Each lane keeps its
-// four columns in a lane-dependent order (lane_order) that makes both free of selects.
+// value per column goes back to all eight lanes in three more shuffles.  Each
+// lane keeps its four columns in a lane-dependent order (lane_order) that makes
+// both free of selects.
 #pragma once
 
 #include "kda_common.cuh"
