@@ -42,8 +42,10 @@ __device__ __forceinline__ float warp_sum(float x) {
 // overlap in three of them).  The rows are requested before the search for the sequence start,
 // so the two overlap; rows before a token's sequence start are zeroed afterwards (token t0 + 1
 // may open the next sequence).
+// Five blocks per SM (48 registers a thread, a few spilled): 4.9 % faster than four
+// (64 registers, none spilled); more warps in flight matter more here than the spills.
 template <typename Tout>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 5)
 frontend_kernel(FrontendArgs a) {
     const int lane = threadIdx.x & 31;
     const int H = a.num_heads, T = a.total_tokens;
